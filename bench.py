@@ -1,0 +1,486 @@
+#!/usr/bin/env python
+"""Benchmark: decode steps of the CSA2 decoder over an FP4 main KV cache.
+
+Workload (the batched Full-mode decode shapes): 32 sequences with
+L_b ~ U{32768..65536} tokens (n_b = L_b/4 compressed entries, capacity
+16384), 576-channel FP4 entries (512 latent + 64 RoPE), 64 query heads, FP8
+indexer 4 x 64, Top-512, pool of 2048 x 8.  One step is one decode token
+through the decoder's 20 CSA2 layers as the pages schedule them (group 0: 1
+Full + 3 Reuse; groups 1-4: 1 Reindex + 3 Reuse), so every row of the path
+runs each step: FP4 append (quantise), Full scoring, pool build, Reindex
+scoring, Top-512, sparse FP4 attention, Reuse.  Each layer attends over its
+own FP4 KV (the worst case for bytes).
+
+Metric: CSA2 decode token-layers per second (B x 20 per step), plus the
+dominant kernel's achieved HBM bandwidth against the measured GB300 copy
+bandwidth.  Inputs are resident in HBM; four disjoint input sets rotate so no
+step finds the previous step's data in L2.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode CSA2 token-layers/s (B x layers per decode step)"
+UNIT = "token-layers/s"
+B, NCAP, D, DV, H, K, P = 32, 16384, 576, 512, 64, 512, 2048
+LAYERS = 20
+ROTATE = 4
+
+
+def _workload_config(extra=None):
+    cfg = {"workload": "csa2_decoder_step_b32_ctx32k-64k_n16384_d576_h64_top512_pool2048x8_20layers",
+           "batch": B, "entries_cap": NCAP, "D": D, "dv": DV, "heads": H, "topk": K, "pool_blocks": P,
+           "layers": LAYERS, "schedule": "1Full+3Reuse, 4x(1Reindex+3Reuse)", "kv": "FP4 E2M1 + E4M3/16, per layer",
+           "indexer": "FP8 E4M3 4x64", "l2": "4 rotating disjoint input sets, each step's working set > L2"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background (100 ms)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.samples.append((time.time(), ln.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, ln in self.samples:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((ts, float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside and rows:  # timed region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def _fill_instance(st, seed):
+    import torch
+    import gen
+    w = gen.scaled(gen.FULL_BATCHED_DECODE, seed=seed)
+    dev = st.device
+    st.kv_len.copy_(gen.kv_lengths(w).to(dev))
+    for layer in range(st.n_kv):
+        rows = gen.kv_rows(seed, 100 + layer, B * NCAP, D, rms=True, device=dev)
+        c, s = st.kv_planes(layer)
+        import sparse_attention_fp4_quantize_gb300 as csa2
+        csa2.csa2_quantize_kv_fp4(rows, c, s)
+        del rows
+    st.k_idx.copy_(gen.normal_e4m3(seed, 19, (B, NCAP, 64), device=dev))
+    for gi in range(len(st.groups)):
+        st.inputs["q_idx"][gi].copy_(gen.normal_e4m3(seed, 20 + 3 * gi, (B, 1, 4, 64), device=dev))
+        st.inputs["w_idx"][gi].copy_(gen.uniform01(seed, 21 + 3 * gi, (B, 1, 4), device=dev))
+    for layer in range(LAYERS):
+        st.inputs["q"][layer].copy_(gen.normal_bf16(seed, 200 + layer, (B, 1, H, D), device=dev))
+    st.inputs["new_rows"].copy_(gen.kv_rows(seed, 70, st.n_kv * B, D, device=dev))
+    st.set_append_slots()
+    torch.cuda.synchronize()
+
+
+def _algorithmic_bytes(st):
+    """Indexer keys read + selected FP4 entries gathered + outputs, per step."""
+    import torch
+    n = st.kv_len.to(torch.int64)
+    keys_full = int(n.sum()) * 64
+    # Reindex layers score the pool's candidates: min(n, 8 * 2048) keys per sequence
+    keys_re = int(torch.clamp(n, max=8 * P).sum()) * 64
+    n_full = sum(1 for m in st.shape.schedule if m == "full")
+    n_re = sum(1 for m in st.shape.schedule if m == "reindex")
+    gathered = LAYERS * B * K * (D // 2 + D // 16)
+    outputs = LAYERS * B * H * DV * 4
+    return {"keys": keys_full * n_full + keys_re * n_re, "gathered": gathered, "outputs": outputs,
+            "attn_per_launch": B * K * (D // 2 + D // 16) + B * H * DV * 4}
+
+
+def _kernel_breakdown(steps, stream, nsteps):
+    """Per-call GPU durations from CUDA events around every library call of
+    eager (non-graph) steps on the launching stream."""
+    import torch
+    import sparse_attention_fp4_quantize_gb300 as csa2
+    names = {"csa2_quantize_kv_fp4": "quantize", "csa2_index_score": "index_score",
+             "csa2_build_pool": "build_pool", "csa2_topk": "topk", "csa2_sparse_attn_fp4": "sparse_attn"}
+    import sparse_attention_fp4_quantize_gb300.decode as dec
+    orig = {n: getattr(dec, n) for n in names}
+    recs = []
+
+    def wrap(n, fn):
+        def inner(*a, **kw):
+            mode = a[0] if n in ("csa2_index_score", "csa2_topk") else None
+            if mode == csa2.MODE_REUSE:
+                return fn(*a, **kw)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(*a, **kw)
+            e1.record(stream)
+            recs.append((names[n], e0, e1))
+        return inner
+
+    for n, fn in orig.items():
+        setattr(dec, n, wrap(n, fn))
+    try:
+        with torch.cuda.stream(stream):
+            for i in range(nsteps):
+                steps[i % len(steps)].run(stream=stream)
+        torch.cuda.synchronize()
+    finally:
+        for n, fn in orig.items():
+            setattr(dec, n, fn)
+    agg = {}
+    for name, e0, e1 in recs:
+        d = agg.setdefault(name, [0.0, 0])
+        d[0] += e0.elapsed_time(e1) * 1e-3
+        d[1] += 1
+    return {k: {"launches_per_step": v[1] / nsteps, "avg_s": v[0] / v[1], "total_s_per_step": v[0] / nsteps}
+            for k, v in agg.items()}
+
+
+def _traffic_record(kernel):
+    """DRAM bytes per launch from the committed ncu summary, valid only while
+    the kernel's source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else None
+    if h != rec.get("source_sha256_16"):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.device_count() >= world else "gloo")
+    import sparse_attention_fp4_quantize_gb300 as csa2  # noqa: F401  (fails loudly without libcsa2.so)
+    from sparse_attention_fp4_quantize_gb300.decode import DecoderStep, StepShape
+
+    steps = []
+    for r in range(ROTATE):
+        st = DecoderStep(StepShape(B=B, N=NCAP, D=D, dv=DV, H=H, K=K, P=P), device=dev)
+        _fill_instance(st, seed=1 + 1000 * rank + 17 * r)
+        steps.append(st)
+    stream = torch.cuda.Stream(device=dev)
+    # warm the library (attributes, module load) eagerly, then capture one graph per input set
+    with torch.cuda.stream(stream):
+        for st in steps:
+            st.run(stream=stream)
+    torch.cuda.synchronize()
+    graphs = []
+    for st in steps:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            st.run(stream=stream)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- device-resident timed region
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % ROTATE].replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[i % ROTATE].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    time.sleep(0.15)
+    clocks.stop()
+    sec = e0.elapsed_time(e1) * 1e-3
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([sec], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        sec = float(tt.item())
+    st0 = steps[0]
+    tl = st0.token_layers
+    value = tl * args.steps * world / sec
+    errs = [int(s.err.item()) for s in steps]
+
+    # ---- end to end through the public API with pinned host buffers
+    host_in = []
+    for st in steps:
+        host_in.append({k: v.to("cpu").pin_memory() for k, v in st.inputs.items()})
+    host_out = torch.empty_like(st0.out[-1], device="cpu").pin_memory()
+    host_lse = torch.empty_like(st0.lse[-1], device="cpu").pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in[0].values())
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    e2e_steps = max(3, min(args.steps, 200))
+    barrier()
+    torch.cuda.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for i in range(e2e_steps):
+            st = steps[i % ROTATE]
+            for k_, v in host_in[i % ROTATE].items():
+                st.inputs[k_].copy_(v, non_blocking=True)
+            graphs[i % ROTATE].replay()
+            host_out.copy_(st.out[-1], non_blocking=True)
+            host_lse.copy_(st.lse[-1], non_blocking=True)
+        f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_sec = f0.elapsed_time(f1) * 1e-3
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_sec], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_sec = float(tt.item())
+    e2e_value = tl * e2e_steps * world / e2e_sec
+
+    # ---- per-kernel durations (events around each call, eager steps on the same stream)
+    brk = _kernel_breakdown(steps, stream, nsteps=2 * ROTATE)
+    alg = _algorithmic_bytes(st0)
+    peak, peak_kind = _peaks()
+    dom = max(brk.items(), key=lambda kv: kv[1]["total_s_per_step"])
+    per_launch_bytes = {"sparse_attn": alg["attn_per_launch"],
+                        "index_score": None, "topk": None, "build_pool": None, "quantize": None}
+    kname = dom[0]
+    if kname == "sparse_attn":
+        ab = alg["attn_per_launch"]
+    elif kname == "index_score":
+        ab = alg["keys"] / 5
+    else:
+        ab = None
+    achieved = (ab / dom[1]["avg_s"] / 1e9) if ab else None
+    roof = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": (achieved / peak) if achieved else None, "peak_kind": "burst copy (" + peak_kind + ")",
+            "algorithmic_bytes_per_launch": ab,
+            "traffic": _traffic_record({"sparse_attn": "sparse_attn_kernel"}.get(kname, kname)),
+            "avg_launch_us": dom[1]["avg_s"] * 1e6}
+    path_bytes = alg["keys"] + alg["gathered"] + alg["outputs"]
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(budget_s=args.cpu_budget)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp4/fp8 in, f16 mma, f32 accumulate",
+        "data": "synthetic (seeded; shapes of the pages' 64K-context batched decode)",
+        "config": _workload_config(),
+        "path_hbm_gbs": path_bytes / (sec / args.steps) / 1e9,
+        "path_bytes_per_step": path_bytes,
+        "roofline": roof,
+        "kernels": {k: {"avg_us": v["avg_s"] * 1e6, "launches_per_step": v["launches_per_step"],
+                        "share": v["total_s_per_step"] / sum(x["total_s_per_step"] for x in brk.values())}
+                    for k, v in brk.items()},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": st0.launches_per_step() * args.steps,
+        "clocks": clocks.summary(t0, t1),
+        "device_error_flags": errs,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+def _oracle_sample(n_seq, n_layers=LAYERS, seed=1):
+    """Inputs of n_seq sequences for the oracle decode step (CPU, seeded)."""
+    import gen
+    w = gen.scaled(gen.FULL_BATCHED_DECODE, seed=seed)
+    kv_len = gen.as_numpy(gen.kv_lengths(w))[:n_seq].copy()
+    k = gen.as_numpy(gen.normal_e4m3(seed, 19, (n_seq, NCAP, 64)))
+    q_idx = [gen.as_numpy(gen.normal_e4m3(seed, 20 + 3 * g, (n_seq, 1, 4, 64))) for g in range(5)]
+    w_idx = [gen.as_numpy(gen.uniform01(seed, 21 + 3 * g, (n_seq, 1, 4))) for g in range(5)]
+    q = [gen.as_numpy(gen.normal_bf16(seed, 200 + l, (n_seq, 1, H, D))) for l in range(n_layers)]
+    planes = [tuple(gen.as_numpy(t) for t in gen.fp4_planes(seed, 100 + l, n_seq * NCAP, D)) for l in range(n_layers)]
+    new_rows = gen.as_numpy(gen.kv_rows(seed, 70, n_layers * n_seq, D))
+    return dict(kv_len=kv_len, k=k, q_idx=q_idx, w_idx=w_idx, q=q, planes=planes, new_rows=new_rows)
+
+
+def _oracle_step(orc, s, n_seq, schedule):
+    """The decode step of the oracle on the sample (all sequences at once)."""
+    import numpy as np
+    sm = 1.0 / D ** 0.5
+    L = len(schedule)
+    orc.quantize_kv_fp4(s["new_rows"][: L * n_seq])             # the step's FP4 appends
+    gi = -1
+    pool = idx = None
+    for layer, mode in enumerate(schedule):
+        if mode == "full":
+            gi += 1
+            sc = orc.index_score(orc.FULL, s["q_idx"][gi], orc.FP8_E4M3, s["w_idx"][gi], s["k"], orc.FP8_E4M3,
+                                 s["kv_len"]).astype(np.float32)
+            if layer == 0:
+                pool = orc.build_pool(sc, s["kv_len"], P=P)
+            idx = orc.topk(orc.FULL, sc, s["kv_len"], K=K)
+        elif mode == "reindex":
+            gi += 1
+            rs = orc.index_score(orc.REINDEX, s["q_idx"][gi], orc.FP8_E4M3, s["w_idx"][gi], s["k"], orc.FP8_E4M3,
+                                 s["kv_len"], pool=pool).astype(np.float32)
+            idx = orc.topk(orc.REINDEX, rs, None, pool=pool, K=K)
+        codes, scales = s["planes"][layer]
+        orc.sparse_attn(s["q"][layer], codes, scales, NCAP, idx, s["kv_len"], sm, DV)
+
+
+def cpu_baseline(budget_s=15.0, per_step_budget=None):
+    """Time the oracle as it stands (single-threaded C, fp64) on a bounded
+    sample of the workload: whole sequences through the 20-layer schedule."""
+    import oracle as orc
+    from sparse_attention_fp4_quantize_gb300.decode import DECODER_SCHEDULE
+    orc.build()
+    s1 = _oracle_sample(1)
+    t = time.perf_counter()
+    _oracle_step(orc, s1, 1, DECODER_SCHEDULE)
+    t1 = time.perf_counter() - t
+    n_seq = int(max(1, min(B, budget_s // max(t1, 1e-3))))
+    s = _oracle_sample(n_seq)
+    t = time.perf_counter()
+    _oracle_step(orc, s, n_seq, DECODER_SCHEDULE)
+    el = time.perf_counter() - t
+    return {"value": n_seq * LAYERS / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d of %d sequences x %d layers (one decode step), single-threaded C fp64; %.1f s"
+                      % (n_seq, B, LAYERS, el)}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle as orc
+    from sparse_attention_fp4_quantize_gb300.decode import DECODER_SCHEDULE
+    orc.build()
+    s1 = _oracle_sample(1)
+    t = time.perf_counter()
+    _oracle_step(orc, s1, 1, DECODER_SCHEDULE)
+    t_full = time.perf_counter() - t
+    # each step: one sequence through the schedule (or its first group if K+W steps would run too long)
+    sched = DECODER_SCHEDULE if t_full * (args.steps + args.warmup) <= 240 else DECODER_SCHEDULE[:4]
+    for _ in range(args.warmup):
+        _oracle_step(orc, s1, 1, sched)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(orc, s1, 1, sched)
+    el = time.perf_counter() - t
+    value = len(sched) * args.steps / el
+    sample = "1 of %d sequences x %d layers per step, single-threaded C fp64" % (B, len(sched))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": _workload_config({"sample": sample}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -230,3 +230,13 @@ def as_numpy(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.int16:
         return t.numpy().view(np.uint16)
     return t.numpy()
+
+
+def fp4_planes(seed, stream, rows, D, device="cpu"):
+    """Random FP4 cache planes (codes uint8 [rows, D/2], scales uint8
+    [rows, D/16]) for timing-only work: uniform code bytes and scale bytes in
+    [0x20, 0x38) (E4M3 values 0.125 .. 0.9, the range N(0,1) groups give)."""
+    g = _g(seed, stream, device)
+    codes = torch.randint(0, 256, (rows, D // 2), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+    scales = torch.randint(0x20, 0x38, (rows, D // 16), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+    return codes, scales

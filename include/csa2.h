@@ -1,0 +1,214 @@
+/*
+ * csa2.h -- C ABI of libcsa2: the decode-time hot path of CSA2 compressed
+ * sparse attention over an FP4 main KV cache, as hand-written CUDA kernels
+ * for GB300 (sm_103a).
+ *
+ * The method is described on web pages about the DeepSeek-V4.1-Flash report:
+ *  [ENG]  "DeepSeek-V4.1-Flash：把 KV Cache 压缩到极限的百万上下文 MoE"
+ *  [HUNT] "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression"
+ *  [55ZB] "552B参数干掉1.6T：DeepSeek V4.1 Flash技术深度解析"
+ * The pages state the problem (three layer modes, the FP4 format, the
+ * candidate pool, Top-512) but no interface; these calls follow that
+ * statement.  Section names are cited per call.
+ *
+ * Conventions shared by every call
+ *  - Every tensor pointer is DEVICE memory owned by the caller.  The library
+ *    allocates nothing; scratch comes through a caller-provided workspace
+ *    sized by the matching *_workspace_bytes() call.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  No call synchronises.
+ *  - Every call returns a csa2_status; no exception crosses the ABI.
+ *    Argument errors are found on the host before any launch and leave every
+ *    output untouched.  csa2_last_error() gives a thread-local detail string.
+ *  - Data errors found on the device (an index outside its valid range) never
+ *    fault: the offending element is skipped and a bit is OR-ed into
+ *    *err_flag (a caller-owned device uint32, nullable).  Read it after the
+ *    stream has synchronised.
+ *  - Layouts are dense row-major C arrays unless stated.  Shapes below use
+ *    B batch, T query tokens per sequence, N entry capacity per sequence,
+ *    D KV channels (last 64 carry RoPE), H attention heads, K selected
+ *    entries, P pool blocks.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *csa2_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    CSA2_OK = 0,
+    CSA2_ERR_INVALID_ARG = 1,  /* bad shape, null or misaligned pointer, bad mode */
+    CSA2_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. a D/dv pair)  */
+    CSA2_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required     */
+    CSA2_ERR_CUDA = 4,         /* a CUDA runtime error at launch                 */
+    CSA2_ERR_DEVICE_FLAG = 5,  /* reserved for callers that map *err_flag        */
+    CSA2_ERR_TIMEOUT = 6       /* reserved: no kernel here spin-waits            */
+} csa2_status;
+
+typedef enum {
+    CSA2_MODE_FULL = 0,     /* layer computes its own scores and Top-K          */
+    CSA2_MODE_REINDEX = 1,  /* rescore inside the pool with the layer's own q   */
+    CSA2_MODE_REUSE = 2     /* reuse the source layer's indices unchanged       */
+} csa2_mode;
+
+typedef enum { CSA2_BF16 = 0, CSA2_FP8_E4M3 = 1, CSA2_FP32 = 2 } csa2_dtype;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define CSA2_FLAG_BAD_INDEX 0x1u  /* attention idx outside [-1, kv_len)              */
+#define CSA2_FLAG_BAD_POOL 0x2u   /* pool block id outside [-1, ceil(N/8))           */
+#define CSA2_FLAG_BAD_SLOT 0x4u   /* quantise dst_slot outside [0, n_slots)          */
+
+/* Fixed indexer shape: 4 heads of dimension 64, one 64-dim key per entry. */
+#define CSA2_INDEX_HEADS 4
+#define CSA2_INDEX_DIM 64
+#define CSA2_POOL_BLOCK 8      /* positions per pool block                           */
+#define CSA2_MAX_POOL 2048     /* at most 2048 blocks x 8 = 16384 candidates          */
+#define CSA2_MAX_K 2048
+
+/*
+ * csa2_quantize_kv_fp4 -- quantise post-RoPE KV rows to the FP4 main-cache
+ * format.  [ENG] section "效率组件四件", item 4 "FP4 主 KV Cache": E2M1 values
+ * with one E4M3 scale per 16 channels, no second-level global scale,
+ * quantised after RoPE; [HUNT] CSA2 paragraph (same format).
+ *
+ * For row r, group g (channels 16g..16g+15):
+ *   s = E4M3(amax/6) rounded to nearest even, saturating at 448;
+ *   code_c = sign(x_c) << 3 | E2M1(|x_c|/s) rounded to nearest, ties to the
+ *   even code, saturating at 6 (magnitude 0 when s == 0).
+ * The sign bit of a code is the sign bit of its input, also for zeros.
+ *
+ * kv        bf16 [rows, kv_row_stride] (first D of each row used); 16-byte
+ *           aligned, kv_row_stride a multiple of 8 elements.
+ * rows      >= 0 (0 is a no-op).     D: multiple of 16, 16..4096.
+ * dst_slot  int64 [rows] or NULL: row r is written to cache slot dst_slot[r]
+ *           (else slot r).  A slot outside [0, n_slots) is skipped and sets
+ *           CSA2_FLAG_BAD_SLOT.
+ * n_slots   capacity of the cache planes, in slots.
+ * codes     uint8 [n_slots, D/2]: channel 2i in the low nibble of byte i,
+ *           2i+1 in the high nibble; 4-byte aligned.
+ * scales    uint8 [n_slots, D/16]: the E4M3 scale of each group.
+ * Bytes per entry: D/2 + D/16 (324 for D = 576).
+ */
+csa2_status csa2_quantize_kv_fp4(const void *kv, int64_t rows, int D, int64_t kv_row_stride,
+                                 const int64_t *dst_slot, int64_t n_slots, uint8_t *codes,
+                                 uint8_t *scales, uint32_t *err_flag, csa2_stream_t stream);
+
+/*
+ * csa2_index_score -- indexer scores of query tokens against compressed
+ * entries.  [ENG] section "Hierarchical Sparse Indexer——索引成本变常数": Full
+ * layers score every entry (cost linear in context); later Reindex layers
+ * score only inside the candidate pool (constant cost); [HUNT] CSA2
+ * paragraph: Reindex reuses the KV and rescores with its own indexer Q.
+ * The pages give no score formula; this library computes
+ *   score = sum_{h<4} w_h * ReLU(sum_{d<64} q_hd * k_d)
+ * with exact products and fp32 accumulation.
+ *
+ * mode    FULL: scores [B, T, N], entry j scored iff j < kv_len[b*T+t], else
+ *         -inf.  REINDEX: scores [B, T, 8P] in pool-local order l = 8p + i
+ *         for key j = 8*pool_blocks[b,t,p] + i of the SAME sequence b, -inf
+ *         where the block id is -1 or j >= kv_len.  REUSE: returns CSA2_OK
+ *         without work.
+ * q_idx   [B, T, 4, 64], w fp32 [B, T, 4], k_idx [B, N, 64]; q_dt == k_dt,
+ *         either CSA2_FP8_E4M3 (no scale) or CSA2_BF16; q_idx and k_idx
+ *         16-byte aligned.
+ * kv_len  int32 [B*T], visible entries per query token (values > N act as N).
+ * pool_blocks int32 [B, T, P] for REINDEX (1 <= P <= 2048), NULL for FULL.
+ *         A block id outside [-1, ceil(N/8)) scores -inf and sets
+ *         CSA2_FLAG_BAD_POOL.
+ */
+csa2_status csa2_index_score(csa2_mode mode, int B, int T, int64_t N, const void *q_idx,
+                             csa2_dtype q_dt, const float *w, const void *k_idx, csa2_dtype k_dt,
+                             const int32_t *kv_len, const int32_t *pool_blocks, int P,
+                             float *scores, uint32_t *err_flag, csa2_stream_t stream);
+
+/*
+ * csa2_build_pool -- the hierarchical candidate pool.  [ENG] section
+ * "Hierarchical Sparse Indexer": the decoder's first Full layer builds a
+ * block-level pool of at most 2048 blocks x 8 positions = 16384 candidates.
+ * Block beta covers positions [8*beta, 8*beta + 8); its score is the max of
+ * scores[b,t,j] over its positions j < kv_len (a partial last block counts).
+ * The pool is the Top-min(P, #blocks with a finite score) blocks, written
+ * to pool_blocks [B, T, P] as block ids, -1 padded, in unspecified order.
+ *
+ * scores fp32 [B, T, N] (16-byte aligned when N % 4 == 0); kv_len int32
+ * [B*T]; 1 <= P <= 2048; G must be 8; ceil(N/8) <= 131072.
+ * workspace: csa2_build_pool_workspace_bytes() bytes (currently 0; NULL ok).
+ */
+csa2_status csa2_build_pool(int B, int T, int64_t N, const float *scores, const int32_t *kv_len,
+                            int P, int G, int32_t *pool_blocks, void *workspace, size_t ws_bytes,
+                            csa2_stream_t stream);
+size_t csa2_build_pool_workspace_bytes(int B, int T, int64_t N, int P);
+
+/*
+ * csa2_topk -- Top-K selection per query token.  [ENG] CSA2 section (Top-512
+ * in every layer); [55ZB] DeepSelect paragraph (the sparse attention's
+ * Top-K kernel).  Selects the K largest finite scores; -inf is never
+ * selected; fewer than K candidates leaves -1 in the remaining slots.  Ties
+ * at the K-th value are taken toward the lower candidate position.  Output
+ * order is unspecified.
+ *
+ * mode   FULL: scores [B, T, M], candidates j < min(kv_len[b*T+t], M) (kv_len
+ *        may be NULL: all M); idx holds positions j.
+ *        REINDEX: scores [B, T, 8P] from csa2_index_score(REINDEX), M == 8P;
+ *        a selected l = 8p + i is written as 8*pool_blocks[b,t,p] + i.
+ *        REUSE: returns CSA2_OK, idx untouched (the layer consumes its source
+ *        layer's idx buffer).
+ * idx    int32 [B, T, K], 1 <= K <= 2048.  M <= 524288.
+ * workspace: csa2_topk_workspace_bytes() bytes (currently 0; NULL ok).
+ */
+csa2_status csa2_topk(csa2_mode mode, int B, int T, int64_t M, const float *scores,
+                      const int32_t *kv_len, const int32_t *pool_blocks, int P, int K, int32_t *idx,
+                      void *workspace, size_t ws_bytes, csa2_stream_t stream);
+size_t csa2_topk_workspace_bytes(int B, int T, int64_t M, int K);
+
+/*
+ * csa2_sparse_attn_fp4 -- attention of each query head over its selected FP4
+ * entries.  The pages give no formula (the [ENG] inference bullet names
+ * FlashMLA fused attention as the kernel of Reuse layers); read MLA-style:
+ * for query row (b,t,h) and valid selected entries J,
+ *   z_j = sm_scale * sum_{c<D} q[c] * Khat[j][c]
+ *   out[c] = sum_j softmax(z)_j * Khat[j][c]   for c < dv
+ *   lse = log sum_j exp(z_j)
+ * Khat is the dequantised entry (E2M1 value x its group's E4M3 scale),
+ * computed in registers from the FP4 planes; V is its first dv channels.
+ * An empty J gives out = 0 and lse = -inf.
+ * mode  any: REUSE layers pass their source layer's idx (and KV, or their
+ *       own KV) unchanged ([ENG] CSA2 section; [55ZB], [HUNT] CSA2 paragraphs).
+ *
+ * q       bf16 [B, T, H, D], 16-byte aligned.  Supported (D, dv, H):
+ *         D = 576, dv = 512, H a multiple of 64; D = 128, dv = 64, H a
+ *         multiple of 16.
+ * codes   uint8 [B*N, D/2], scales uint8 [B*N, D/16]: entry j of sequence
+ *         b is row b*N + j (the layout csa2_quantize_kv_fp4 writes);
+ *         codes 16-byte aligned, scales 4-byte aligned.
+ * idx     int32 [B, T, K], entries j in [0, kv_len) or -1 (skipped);
+ *         anything else is skipped and sets CSA2_FLAG_BAD_INDEX.  K <= 2048.
+ * kv_len  int32 [B*T] or NULL (= N).
+ * out     fp32 [B, T, H, dv] (out_dt must be CSA2_FP32); lse fp32 [B, T, H]
+ *         or NULL.
+ * workspace csa2_sparse_attn_workspace_bytes() bytes (split-KV partials).
+ */
+csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H, int D, int dv,
+                                 const void *q, const uint8_t *codes, const uint8_t *scales,
+                                 int64_t N, const int32_t *idx, int K, const int32_t *kv_len,
+                                 float sm_scale, void *out, csa2_dtype out_dt, float *lse,
+                                 uint32_t *err_flag, void *workspace, size_t ws_bytes,
+                                 csa2_stream_t stream);
+size_t csa2_sparse_attn_workspace_bytes(int B, int T, int H, int D, int dv, int K);
+
+/* Status helpers. */
+const char *csa2_status_string(csa2_status s);
+const char *csa2_last_error(void); /* thread-local detail of the last non-OK status */
+int csa2_version(void);            /* major*10000 + minor*100 + patch */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

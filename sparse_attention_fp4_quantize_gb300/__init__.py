@@ -1,0 +1,172 @@
+"""Python binding of libcsa2 -- the CSA2 decode hot path over an FP4 main KV
+cache, as hand-written CUDA kernels for GB300 (sm_103a).
+
+Argument marshalling only: every function passes torch tensors' device
+pointers, shapes and the current CUDA stream to the C ABI declared in
+``include/csa2.h`` and raises ``Csa2Error`` on a non-OK status.  There is no
+CPU fallback: if the shared library is missing the import fails loudly.
+
+Names follow the C ABI: ``csa2_quantize_kv_fp4``, ``csa2_index_score``,
+``csa2_build_pool``, ``csa2_topk``, ``csa2_sparse_attn_fp4`` and the
+``*_workspace_bytes`` helpers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcsa2.so")
+
+MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
+BF16, FP8_E4M3, FP32 = 0, 1, 2
+FLAG_BAD_INDEX, FLAG_BAD_POOL, FLAG_BAD_SLOT = 0x1, 0x2, 0x4
+INDEX_HEADS, INDEX_DIM, POOL_BLOCK, MAX_POOL, MAX_K = 4, 64, 8, 2048, 2048
+
+STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3: "CSA2_ERR_WORKSPACE",
+          4: "CSA2_ERR_CUDA", 5: "CSA2_ERR_DEVICE_FLAG", 6: "CSA2_ERR_TIMEOUT"}
+
+
+class Csa2Error(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__("%s: %s" % (STATUS.get(status, status), detail))
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libcsa2.so is not built (run __graft_entry__.build() or "
+                          "python sparse_attention_fp4_quantize_gb300/build.py)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, u64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    sig = {
+        "csa2_quantize_kv_fp4": ([P, i64, i32, i64, P, i64, P, P, P, P], i32),
+        "csa2_index_score": ([i32, i32, i32, i64, P, i32, P, P, i32, P, P, i32, P, P, P], i32),
+        "csa2_build_pool": ([i32, i32, i64, P, P, i32, i32, P, P, u64, P], i32),
+        "csa2_build_pool_workspace_bytes": ([i32, i32, i64, i32], u64),
+        "csa2_topk": ([i32, i32, i32, i64, P, P, P, i32, i32, P, P, u64, P], i32),
+        "csa2_topk_workspace_bytes": ([i32, i32, i64, i32], u64),
+        "csa2_sparse_attn_fp4": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P, P,
+                                  P, u64, P], i32),
+        "csa2_sparse_attn_workspace_bytes": ([i32, i32, i32, i32, i32, i32], u64),
+        "csa2_status_string": ([i32], ctypes.c_char_p),
+        "csa2_last_error": ([], ctypes.c_char_p),
+        "csa2_version": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def exported_symbols():
+    return ["csa2_quantize_kv_fp4", "csa2_index_score", "csa2_build_pool", "csa2_build_pool_workspace_bytes",
+            "csa2_topk", "csa2_topk_workspace_bytes", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes",
+            "csa2_status_string", "csa2_last_error", "csa2_version"]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise Csa2Error(rc, _lib.csa2_last_error().decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return FP8_E4M3
+    if t.dtype in (torch.bfloat16, torch.int16):
+        return BF16
+    raise TypeError("indexer tensors must be FP8 E4M3 (uint8/float8_e4m3fn) or bf16 (bfloat16/int16 bits)")
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def version() -> int:
+    return _lib.csa2_version()
+
+
+def csa2_quantize_kv_fp4(kv, codes, scales, dst_slot=None, err_flag=None, stream=None):
+    """kv bf16 [R, D] (or int16 bits) -> codes uint8 [S, D/2], scales uint8 [S, D/16]."""
+    _cuda(kv, codes, scales, dst_slot, err_flag)
+    R, D = kv.shape
+    if kv.stride(1) != 1:
+        raise ValueError("kv rows must be contiguous")
+    n_slots = codes.shape[0]
+    _check(_lib.csa2_quantize_kv_fp4(_ptr(kv), R, D, kv.stride(0), _ptr(dst_slot), n_slots, _ptr(codes),
+                                     _ptr(scales), _ptr(err_flag), _stream(stream)))
+
+
+def csa2_index_score(mode, q_idx, w, k_idx, kv_len, scores, pool_blocks=None, err_flag=None, stream=None):
+    """q_idx [B,T,4,64], w fp32 [B,T,4], k_idx [B,N,64], kv_len int32 [B*T] ->
+    scores fp32 [B,T,N] (FULL) or [B,T,8P] (REINDEX)."""
+    _cuda(q_idx, w, k_idx, kv_len, scores, pool_blocks, err_flag)
+    B, T = q_idx.shape[0], q_idx.shape[1]
+    N = k_idx.shape[1]
+    P = 0 if pool_blocks is None else pool_blocks.shape[-1]
+    _check(_lib.csa2_index_score(int(mode), B, T, N, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), _ptr(k_idx),
+                                 _dtype_code(k_idx), _ptr(kv_len), _ptr(pool_blocks), P, _ptr(scores),
+                                 _ptr(err_flag), _stream(stream)))
+
+
+def csa2_build_pool(scores, kv_len, pool_blocks, workspace=None, stream=None):
+    """scores fp32 [B,T,N], kv_len int32 [B*T] -> pool_blocks int32 [B,T,P]."""
+    _cuda(scores, kv_len, pool_blocks, workspace)
+    B, T, N = scores.shape
+    P = pool_blocks.shape[-1]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.csa2_build_pool(B, T, N, _ptr(scores), _ptr(kv_len), P, POOL_BLOCK, _ptr(pool_blocks),
+                                _ptr(workspace), ws, _stream(stream)))
+
+
+def csa2_topk(mode, scores, idx, kv_len=None, pool_blocks=None, workspace=None, stream=None):
+    """scores fp32 [B,T,M] -> idx int32 [B,T,K]."""
+    _cuda(scores, idx, kv_len, pool_blocks, workspace)
+    B, T, M = scores.shape
+    K = idx.shape[-1]
+    P = 0 if pool_blocks is None else pool_blocks.shape[-1]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.csa2_topk(int(mode), B, T, M, _ptr(scores), _ptr(kv_len), _ptr(pool_blocks), P, K, _ptr(idx),
+                          _ptr(workspace), ws, _stream(stream)))
+
+
+def csa2_sparse_attn_workspace_bytes(B, T, H, D, dv, K) -> int:
+    return int(_lib.csa2_sparse_attn_workspace_bytes(B, T, H, D, dv, K))
+
+
+def csa2_sparse_attn_fp4(mode, q, codes, scales, N, idx, out, sm_scale, kv_len=None, lse=None, err_flag=None,
+                         workspace=None, stream=None):
+    """q bf16 [B,T,H,D]; codes [B*N, D/2], scales [B*N, D/16]; idx int32
+    [B,T,K] -> out fp32 [B,T,H,dv], lse fp32 [B,T,H] (optional)."""
+    _cuda(q, codes, scales, idx, out, kv_len, lse, err_flag, workspace)
+    B, T, H, D = q.shape
+    dv = out.shape[-1]
+    K = idx.shape[-1]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.csa2_sparse_attn_fp4(int(mode), B, T, H, D, dv, _ptr(q), _ptr(codes), _ptr(scales), int(N),
+                                     _ptr(idx), K, _ptr(kv_len), float(sm_scale), _ptr(out), FP32, _ptr(lse),
+                                     _ptr(err_flag), _ptr(workspace), ws, _stream(stream)))
+
+
+def workspace_for_attn(B, T, H, D, dv, K, device="cuda"):
+    """Allocate (through torch) the scratch csa2_sparse_attn_fp4 needs, or None."""
+    n = csa2_sparse_attn_workspace_bytes(B, T, H, D, dv, K)
+    return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=device)

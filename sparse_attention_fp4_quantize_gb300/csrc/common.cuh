@@ -1,0 +1,78 @@
+// Internal helpers shared by the libcsa2 translation units (host argument
+// checks, thread-local error text, small device utilities).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "csa2.h"
+
+namespace csa2 {
+
+// ---------------------------------------------------------------- host side
+void set_error(const char *fmt, ...);
+void clear_error();
+int num_sms();                 // SM count of the current device (cached per device)
+int max_smem_optin();          // max dynamic shared memory per block (opt-in)
+
+#define CSA2_REQUIRE(cond, ...)                 \
+    do {                                        \
+        if (!(cond)) {                          \
+            ::csa2::set_error(__VA_ARGS__);     \
+            return CSA2_ERR_INVALID_ARG;        \
+        }                                       \
+    } while (0)
+
+#define CSA2_LAUNCH_CHECK(what)                                              \
+    do {                                                                     \
+        cudaError_t e_ = cudaGetLastError();                                 \
+        if (e_ != cudaSuccess) {                                             \
+            ::csa2::set_error("%s: %s", what, cudaGetErrorString(e_));      \
+            return CSA2_ERR_CUDA;                                            \
+        }                                                                    \
+    } while (0)
+
+#define CSA2_CUDA_CALL(call, what)                                           \
+    do {                                                                     \
+        cudaError_t e_ = (call);                                             \
+        if (e_ != cudaSuccess) {                                             \
+            ::csa2::set_error("%s: %s", what, cudaGetErrorString(e_));      \
+            return CSA2_ERR_CUDA;                                            \
+        }                                                                    \
+    } while (0)
+
+static inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Raise a kernel's dynamic shared-memory limit once per device (so that only
+// kernel launches are issued while a caller captures a CUDA graph).
+// `done` is per-kernel storage for up to 64 devices.
+static inline cudaError_t ensure_smem_limit(const void *func, int bytes, bool *done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return e;
+}
+static inline cudaStream_t stream_of(csa2_stream_t s) { return (cudaStream_t)s; }
+
+// --------------------------------------------------------------- device side
+// Order-preserving map of an fp32 score to uint32: larger score -> larger key.
+// -inf (and NaN bit patterns that would sort below it) map to 0, the
+// "not a candidate" key; every finite value maps to a key >= 0x00800000.
+// -0 and +0 map to the same key.
+__device__ __forceinline__ uint32_t score_key(float f) {
+    uint32_t u = (f == 0.0f) ? 0u : __float_as_uint(f);
+    uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (k <= 0x007FFFFFu) ? 0u : k;
+}
+
+__device__ __forceinline__ void flag_error(uint32_t *err_flag, uint32_t bit) {
+    if (err_flag) atomicOr(err_flag, bit);
+}
+
+}  // namespace csa2
