@@ -13,8 +13,8 @@ HEADER = os.path.join(ROOT, "include", "csa2.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from sparse_attention_fp4_quantize_gb300 import build as b
-    path = b.build()
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
     return ctypes.CDLL(path)
 
 
