@@ -106,10 +106,10 @@ def version() -> int:
 
 def csa2_quantize_kv_fp4(kv, codes, scales, dst_slot=None, err_flag=None, stream=None):
     """kv bf16 [R, D] (or int16 bits) -> codes uint8 [S, D/2], scales uint8 [S, D/16]."""
-    _cuda(kv, codes, scales, dst_slot, err_flag)
+    _cuda(codes, scales, dst_slot, err_flag)
     R, D = kv.shape
-    if kv.stride(1) != 1:
-        raise ValueError("kv rows must be contiguous")
+    if not kv.is_cuda or kv.stride(1) != 1:
+        raise ValueError("kv must be a CUDA tensor with contiguous rows (any row stride)")
     n_slots = codes.shape[0]
     _check(_lib.csa2_quantize_kv_fp4(_ptr(kv), R, D, kv.stride(0), _ptr(dst_slot), n_slots, _ptr(codes),
                                      _ptr(scales), _ptr(err_flag), _stream(stream)))
