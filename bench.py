@@ -465,6 +465,20 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_profile_case(args):
+    """One input set (about 3.6 GB on the device), three eager decode steps:
+    a small, self-terminating case for a full ncu capture of one kernel."""
+    import torch
+    import sparse_attention_fp4_quantize_gb300  # noqa: F401
+    from sparse_attention_fp4_quantize_gb300.decode import DecoderStep, StepShape
+    st = DecoderStep(StepShape(B=B, N=NCAP, D=D, dv=DV, H=H, K=K, P=P), device="cuda")
+    _fill_instance(st, seed=1)
+    for _ in range(3):
+        st.run()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": "decoder_step", "steps": 3, "error_flag": int(st.err.item())}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -473,10 +487,13 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", action="store_true", help="3 eager steps on one input set (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -203,6 +203,34 @@ csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H, int D, int
                                  csa2_stream_t stream);
 size_t csa2_sparse_attn_workspace_bytes(int B, int T, int H, int D, int dv, int K);
 
+/*
+ * csa2_sparse_attn_fp4_noalloc -- csa2_sparse_attn_fp4 without a caller
+ * workspace.  The pages have no counterpart to this call: it exists for
+ * callers that may not allocate device memory at all, such as an engine that
+ * plans every byte of its device memory before it starts serving, or code
+ * that must not call cudaMalloc/cudaFree because those calls can synchronise
+ * the device.  The split-KV scratch lives in one array built into the library
+ * (csa2_sparse_attn_noalloc_max_scratch_bytes() bytes, 20 MiB; every
+ * supported shape fits on a 152-SM GB300) that every GPU
+ * loading the library holds until the process exits.
+ *
+ * Arguments, layouts, results and errors are those of csa2_sparse_attn_fp4
+ * (minus workspace/ws_bytes); the call allocates nothing.  A shape whose
+ * scratch (csa2_sparse_attn_workspace_bytes) exceeds the array returns
+ * CSA2_ERR_WORKSPACE with an explanation.  The first call on each device
+ * looks up the array's device address with that device current; make that
+ * first call before any stream capture.  All calls on a device share the
+ * array and it keeps the previous call's contents (each call overwrites every
+ * partial it reads, so no clearing is needed): calls that overlap on the GPU
+ * (for instance on two streams of the same device) race.
+ */
+csa2_status csa2_sparse_attn_fp4_noalloc(csa2_mode mode, int B, int T, int H, int D, int dv,
+                                         const void *q, const uint8_t *codes, const uint8_t *scales,
+                                         int64_t N, const int32_t *idx, int K, const int32_t *kv_len,
+                                         float sm_scale, void *out, csa2_dtype out_dt, float *lse,
+                                         uint32_t *err_flag, csa2_stream_t stream);
+size_t csa2_sparse_attn_noalloc_max_scratch_bytes(void);
+
 /* Status helpers. */
 const char *csa2_status_string(csa2_status s);
 const char *csa2_last_error(void); /* thread-local detail of the last non-OK status */

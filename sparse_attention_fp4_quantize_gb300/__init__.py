@@ -51,6 +51,9 @@ def _load() -> ctypes.CDLL:
         "csa2_sparse_attn_fp4": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P, P,
                                   P, u64, P], i32),
         "csa2_sparse_attn_workspace_bytes": ([i32, i32, i32, i32, i32, i32], u64),
+        "csa2_sparse_attn_fp4_noalloc": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P,
+                                          P, P], i32),
+        "csa2_sparse_attn_noalloc_max_scratch_bytes": ([], u64),
         "csa2_status_string": ([i32], ctypes.c_char_p),
         "csa2_last_error": ([], ctypes.c_char_p),
         "csa2_version": ([], i32),
@@ -68,6 +71,7 @@ _lib = _load()
 def exported_symbols():
     return ["csa2_quantize_kv_fp4", "csa2_index_score", "csa2_build_pool", "csa2_build_pool_workspace_bytes",
             "csa2_topk", "csa2_topk_workspace_bytes", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes",
+            "csa2_sparse_attn_fp4_noalloc", "csa2_sparse_attn_noalloc_max_scratch_bytes",
             "csa2_status_string", "csa2_last_error", "csa2_version"]
 
 
@@ -170,3 +174,20 @@ def workspace_for_attn(B, T, H, D, dv, K, device="cuda"):
     """Allocate (through torch) the scratch csa2_sparse_attn_fp4 needs, or None."""
     n = csa2_sparse_attn_workspace_bytes(B, T, H, D, dv, K)
     return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def csa2_sparse_attn_fp4_noalloc(mode, q, codes, scales, N, idx, out, sm_scale, kv_len=None, lse=None,
+                                 err_flag=None, stream=None):
+    """csa2_sparse_attn_fp4 for callers that may not allocate device memory:
+    the split-KV scratch is the library's built-in array (see the header)."""
+    _cuda(q, codes, scales, idx, out, kv_len, lse, err_flag)
+    B, T, H, D = q.shape
+    dv = out.shape[-1]
+    K = idx.shape[-1]
+    _check(_lib.csa2_sparse_attn_fp4_noalloc(int(mode), B, T, H, D, dv, _ptr(q), _ptr(codes), _ptr(scales), int(N),
+                                             _ptr(idx), K, _ptr(kv_len), float(sm_scale), _ptr(out), FP32,
+                                             _ptr(lse), _ptr(err_flag), _stream(stream)))
+
+
+def noalloc_max_scratch_bytes() -> int:
+    return int(_lib.csa2_sparse_attn_noalloc_max_scratch_bytes())

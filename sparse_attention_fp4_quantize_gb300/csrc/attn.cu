@@ -23,6 +23,8 @@
 //    fp32 accumulate); P is rounded to f16 (11-bit mantissa) for P V.
 //  - Online softmax in the log2 domain; split-KV partials (normalised O and
 //    lse per split) are merged by a small combine kernel.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace csa2 {
@@ -527,4 +529,74 @@ extern "C" csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H,
     }
     if (D == 576) return launch_attn<576, 512, 4>(a, stream_of(stream));
     return launch_attn<128, 64, 1>(a, stream_of(stream));
+}
+
+// ---------------------------------------------------------------------------
+// No-allocation variant of csa2_sparse_attn_fp4.
+//
+// The split-KV attention needs scratch memory for its per-split partial
+// outputs.  csa2_sparse_attn_fp4 takes that scratch from the caller; callers
+// that may not allocate device memory at all (an engine that hands out every
+// byte from a pool planned before serving starts, or code that must not call
+// cudaMalloc/cudaFree because those calls can synchronise the device) use
+// this entry point instead.  Its scratch is one file-scope device array of
+// kNoAllocScratchBytes that is part of the library image: every GPU that
+// loads the library holds it until the process exits.  The split policy keeps
+// splits x query tokens x head blocks <= the SM count, so a shape needs at most
+// SMs x 64 heads x (512 + 1) x 4 bytes (19.96 MB on a 152-SM GB300); larger
+// GPUs may meet shapes that do not fit, which are rejected.
+namespace csa2 {
+namespace {
+constexpr size_t kNoAllocScratchBytes = (size_t)20 << 20;  // 20 MiB
+}
+}  // namespace csa2
+
+static __device__ __align__(256) unsigned char g_noalloc_attn_scratch[csa2::kNoAllocScratchBytes];
+
+namespace csa2 {
+namespace {
+// Device address of the scratch array, looked up once per device with that
+// device current (in host code the array's name is only a host-side stand-in).
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64];
+
+cudaError_t noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_attn_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+}  // namespace csa2
+
+extern "C" size_t csa2_sparse_attn_noalloc_max_scratch_bytes(void) { return csa2::kNoAllocScratchBytes; }
+
+extern "C" csa2_status csa2_sparse_attn_fp4_noalloc(csa2_mode mode, int B, int T, int H, int D, int dv,
+                                                    const void *q, const uint8_t *codes, const uint8_t *scales,
+                                                    int64_t N, const int32_t *idx, int K, const int32_t *kv_len,
+                                                    float sm_scale, void *out, csa2_dtype out_dt, float *lse,
+                                                    uint32_t *err_flag, csa2_stream_t stream) {
+    clear_error();
+    const size_t need = csa2_sparse_attn_workspace_bytes(B, T, H, D, dv, K);
+    if (need > kNoAllocScratchBytes) {
+        set_error("sparse_attn_noalloc: this shape needs %zu bytes of scratch, the built-in array holds %zu; "
+                  "use csa2_sparse_attn_fp4 with a caller workspace",
+                  need, kNoAllocScratchBytes);
+        return CSA2_ERR_WORKSPACE;
+    }
+    void *scratch = nullptr;
+    if (need > 0) CSA2_CUDA_CALL(noalloc_scratch(&scratch), "sparse_attn_noalloc: scratch address");
+    // Every split rewrites all of its partial rows (empty splits write zeros
+    // and lse = -inf), so nothing in the array needs clearing between calls.
+    return csa2_sparse_attn_fp4(mode, B, T, H, D, dv, q, codes, scales, N, idx, K, kv_len, sm_scale, out, out_dt,
+                                lse, err_flag, scratch, need > 0 ? kNoAllocScratchBytes : 0, stream);
 }
