@@ -64,6 +64,7 @@ typedef enum { CSA2_BF16 = 0, CSA2_FP8_E4M3 = 1, CSA2_FP32 = 2 } csa2_dtype;
 #define CSA2_FLAG_BAD_INDEX 0x1u  /* attention idx outside [-1, kv_len)              */
 #define CSA2_FLAG_BAD_POOL 0x2u   /* pool block id outside [-1, ceil(N/8))           */
 #define CSA2_FLAG_BAD_SLOT 0x4u   /* quantise dst_slot outside [0, n_slots)          */
+#define CSA2_FLAG_TIMEOUT 0x8u    /* a bounded on-chip wait gave up (results invalid)  */
 
 /* Fixed indexer shape: 4 heads of dimension 64, one 64-dim key per entry. */
 #define CSA2_INDEX_HEADS 4

@@ -481,6 +481,7 @@ using namespace csa2;
 
 extern "C" size_t csa2_sparse_attn_workspace_bytes(int B, int T, int H, int D, int dv, int K) {
     if (B <= 0 || T <= 0 || H <= 0 || K <= 0 || !supported(D, dv, H)) return 0;
+    if (sparse_attn_tc_supported(D, dv, H, K)) return 0;  // cluster-merged, no scratch
     const int64_t bt = (int64_t)B * T;
     const int splits = choose_splits(bt * (H / heads_per_cta(D)), K);
     if (splits <= 1) return 0;
@@ -509,6 +510,10 @@ extern "C" csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H,
     CSA2_REQUIRE(aligned(q, 16) && aligned(codes, 16) && aligned(scales, 4), "sparse_attn: q/codes need 16-byte, scales 4-byte alignment");
     CSA2_REQUIRE(aligned(out, 16) && aligned(idx, 4), "sparse_attn: out needs 16-byte alignment");
     CSA2_REQUIRE((int64_t)B * T <= 0x7FFFFFFFLL && H / heads_per_cta(D) <= 65535, "sparse_attn: too many query tokens or heads");
+
+    if (sparse_attn_tc_supported(D, dv, H, K))
+        return launch_sparse_attn_tc(B, T, H, K, N, q, codes, scales, idx, kv_len, sm_scale, (float *)out, lse,
+                                     err_flag, stream_of(stream));
 
     AttnArgs a = {};
     a.B = B; a.T = T; a.H = H; a.K = K; a.N = N;

@@ -25,8 +25,8 @@ DEV = "cuda"
 ATTN_RTOL = 2e-3
 
 
-def _inputs(seed, B, N, K=512, H=64, D=576):
-    w = gen.scaled(gen.FULL_BATCHED_DECODE, B=B, N=N, K=K, H=H, seed=seed)
+def _inputs(seed, B, N, K, H, D):
+    w = gen.scaled(gen.FULL_BATCHED_DECODE, B=B, N=N, K=K, H=H, D=D, dv=D - 64, seed=seed)
     codes, scales = gen.fp4_planes(seed, 1, B * N, D, device=DEV)
     kl = torch.full((B,), N, dtype=torch.int32)
     idx = gen.random_indices(w, kl, frac_pad=0.05)
@@ -43,25 +43,30 @@ def _rel_err(a, b):
     return float((num / den).max())
 
 
+# shapes that take the split-KV path (and so need scratch): 128-channel
+# entries, and 576-channel entries with more than 1024 selected
+CASES = [(11, 8, 3000, 512, 16, 128), (12, 3, 5000, 512, 32, 128), (13, 2, 4000, 1536, 64, 576)]
+
+
 def test_noalloc_matches_workspace_entry_point_twice():
     import sparse_attention_fp4_quantize_gb300 as csa2
     lib = csa2._lib
-    sm = 1.0 / 576 ** 0.5
-    for call, seed in enumerate((11, 12)):
-        B, N = (8, 3000) if call == 0 else (32, 5000)
-        q, codes, scales, idx, kl = _inputs(seed, B, N)
-        need = csa2.csa2_sparse_attn_workspace_bytes(B, 1, 64, 576, 512, 512)
+    for seed, B, N, K, H, D in CASES:
+        dv = D - 64
+        sm = 1.0 / D ** 0.5
+        q, codes, scales, idx, kl = _inputs(seed, B, N, K, H, D)
+        need = csa2.csa2_sparse_attn_workspace_bytes(B, 1, H, D, dv, K)
         assert 0 < need <= csa2.noalloc_max_scratch_bytes()
-        ref = torch.empty(B, 1, 64, 512, device=DEV)
-        ref_lse = torch.empty(B, 1, 64, device=DEV)
+        ref = torch.empty(B, 1, H, dv, device=DEV)
+        ref_lse = torch.empty(B, 1, H, device=DEV)
         ws = torch.empty(need, dtype=torch.uint8, device=DEV)
         csa2.csa2_sparse_attn_fp4(0, q, codes, scales, N, idx, ref, sm, kv_len=kl, lse=ref_lse, workspace=ws)
-        out = torch.full((B, 1, 64, 512), 9.0, device=DEV)
-        lse = torch.full((B, 1, 64), 9.0, device=DEV)
+        out = torch.full((B, 1, H, dv), 9.0, device=DEV)
+        lse = torch.full((B, 1, H), 9.0, device=DEV)
         stream = torch.cuda.current_stream().cuda_stream
         P = ctypes.c_void_p
-        rc = lib.csa2_sparse_attn_fp4_noalloc(0, B, 1, 64, 576, 512, P(q.data_ptr()), P(codes.data_ptr()),
-                                              P(scales.data_ptr()), N, P(idx.data_ptr()), 512, P(kl.data_ptr()),
+        rc = lib.csa2_sparse_attn_fp4_noalloc(0, B, 1, H, D, dv, P(q.data_ptr()), P(codes.data_ptr()),
+                                              P(scales.data_ptr()), N, P(idx.data_ptr()), K, P(kl.data_ptr()),
                                               sm, P(out.data_ptr()), 2, P(lse.data_ptr()), None, P(stream))
         assert rc == 0, lib.csa2_last_error().decode()
         torch.cuda.synchronize()
@@ -77,5 +82,6 @@ def test_noalloc_scratch_covers_every_shape_on_this_gpu():
     worst = sms * 64 * 513 * 4 + 256
     if worst > csa2.noalloc_max_scratch_bytes():
         pytest.skip("larger GPU: some shapes are rejected by design")
-    for B, H in [(1, 64), (2, 128), (32, 64), (152, 64), (5, 64 * 30)]:
-        assert csa2.csa2_sparse_attn_workspace_bytes(B, 1, H, 576, 512, 512) <= csa2.noalloc_max_scratch_bytes()
+    for B, H, D, K in [(1, 64, 576, 2048), (2, 128, 576, 1100), (1, 16, 128, 512), (9, 64 * 16, 576, 2048),
+                       (1, 16 * 150, 128, 2048)]:
+        assert csa2.csa2_sparse_attn_workspace_bytes(B, 1, H, D, D - 64, K) <= csa2.noalloc_max_scratch_bytes()
