@@ -60,7 +60,7 @@ constexpr uint32_t OFF_LSE = OFF_W + HB * 4;     // float[64] final lse (natural
 constexpr uint32_t SMEM = OFF_LSE + HB * 4;
 constexpr uint32_t TMEM_COLS = 512;             // S^T: 64 cols, O^T: 4 x 64 cols
 constexpr uint32_t S_COL = 0, O_COL = 64;
-constexpr uint32_t MAX_POLLS = 1u << 26;
+constexpr uint32_t MAX_POLLS = 1u << 22;  // about a second of polling at most
 static_assert(HB * PO_STRIDE * 4 <= KT_BYTES, "partial O must fit in the Khat region");
 static_assert(ST_BYTES + (HB / 8) * P_SBO <= Q_BYTES, "S^T copy and P must fit in the Q region");
 static_assert(SMEM <= 227 * 1024, "shared memory");
