@@ -161,47 +161,62 @@ def _algorithmic_bytes(st):
             "attn_per_launch": B * K * (D // 2 + D // 16) + B * H * DV * 4}
 
 
-def _kernel_breakdown(steps, stream, nsteps):
-    """Per-call GPU durations from CUDA events around every library call of
-    eager (non-graph) steps on the launching stream."""
+def _kernel_breakdown(steps, stream, rounds):
+    """Device time per launch of each kernel kind, with CUDA events on the
+    launching stream: for every input set, a CUDA graph holding only that
+    kind's launches of one decode step (the other calls are left out; their
+    output buffers still hold the previous step's valid data) is replayed
+    ``rounds`` times in rotation between two events."""
     import torch
     import sparse_attention_fp4_quantize_gb300 as csa2
-    names = {"csa2_quantize_kv_fp4": "quantize", "csa2_index_score": "index_score",
-             "csa2_build_pool": "build_pool", "csa2_topk": "topk", "csa2_sparse_attn_fp4": "sparse_attn"}
     import sparse_attention_fp4_quantize_gb300.decode as dec
-    orig = {n: getattr(dec, n) for n in names}
-    recs = []
+    kinds = {"quantize": "csa2_quantize_kv_fp4", "index_score": "csa2_index_score", "build_pool": "csa2_build_pool",
+             "topk": "csa2_topk", "sparse_attn": "csa2_sparse_attn_fp4"}
+    orig = {fn: getattr(dec, fn) for fn in kinds.values()}
+    out = {}
+    for kind, keep in kinds.items():
+        count = [0]
 
-    def wrap(n, fn):
-        def inner(*a, **kw):
-            mode = a[0] if n in ("csa2_index_score", "csa2_topk") else None
-            if mode == csa2.MODE_REUSE:
+        def make(fn_name, fn):
+            def inner(*a, **kw):
+                if fn_name != keep:
+                    return None
+                if fn_name in ("csa2_index_score", "csa2_topk") and a[0] == csa2.MODE_REUSE:
+                    return fn(*a, **kw)          # no launch
+                count[0] += 1
                 return fn(*a, **kw)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn(*a, **kw)
-            e1.record(stream)
-            recs.append((names[n], e0, e1))
-        return inner
+            return inner
 
-    for n, fn in orig.items():
-        setattr(dec, n, wrap(n, fn))
-    try:
+        for fn_name, fn in orig.items():
+            setattr(dec, fn_name, make(fn_name, fn))
+        try:
+            graphs = []
+            for st in steps:
+                count[0] = 0
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    st.run(stream=stream)
+                graphs.append(g)
+            per_graph = count[0]
+        finally:
+            for fn_name, fn in orig.items():
+                setattr(dec, fn_name, fn)
+        if per_graph == 0:
+            continue
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            for i in range(nsteps):
-                steps[i % len(steps)].run(stream=stream)
+            for i in range(len(graphs)):
+                graphs[i].replay()
+            e0.record(stream)
+            for i in range(rounds):
+                graphs[i % len(graphs)].replay()
+            e1.record(stream)
         torch.cuda.synchronize()
-    finally:
-        for n, fn in orig.items():
-            setattr(dec, n, fn)
-    agg = {}
-    for name, e0, e1 in recs:
-        d = agg.setdefault(name, [0.0, 0])
-        d[0] += e0.elapsed_time(e1) * 1e-3
-        d[1] += 1
-    return {k: {"launches_per_step": v[1] / nsteps, "avg_s": v[0] / v[1], "total_s_per_step": v[0] / nsteps}
-            for k, v in agg.items()}
+        sec = e0.elapsed_time(e1) * 1e-3
+        out[kind] = {"launches_per_step": per_graph, "avg_s": sec / (rounds * per_graph),
+                     "total_s_per_step": sec / rounds}
+    return out
 
 
 def _traffic_record(kernel):
@@ -323,7 +338,7 @@ def run_gpu(args):
     e2e_value = tl * e2e_steps * world / e2e_sec
 
     # ---- per-kernel durations (events around each call, eager steps on the same stream)
-    brk = _kernel_breakdown(steps, stream, nsteps=2 * ROTATE)
+    brk = _kernel_breakdown(steps, stream, rounds=max(40, min(args.steps, 400)))
     alg = _algorithmic_bytes(st0)
     peak, peak_kind = _peaks()
     dom = max(brk.items(), key=lambda kv: kv[1]["total_s_per_step"])
@@ -338,9 +353,10 @@ def run_gpu(args):
         ab = None
     achieved = (ab / dom[1]["avg_s"] / 1e9) if ab else None
     roof = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": (achieved / peak) if achieved else None, "peak_kind": "burst copy (" + peak_kind + ")",
+            "frac": (achieved / peak) if achieved else None,
+            "peak_kind": "burst copy (%s; the kernel is timed alone)" % peak_kind,
             "algorithmic_bytes_per_launch": ab,
-            "traffic": _traffic_record({"sparse_attn": "sparse_attn_kernel"}.get(kname, kname)),
+            "traffic": _traffic_record({"sparse_attn": "sparse_attn_tc_kernel", "index_score": "index_score_decode_kernel", "topk": "topk_radix_kernel"}.get(kname, kname)),
             "avg_launch_us": dom[1]["avg_s"] * 1e6}
     path_bytes = alg["keys"] + alg["gathered"] + alg["outputs"]
 
@@ -360,6 +376,7 @@ def run_gpu(args):
         "kernels": {k: {"avg_us": v["avg_s"] * 1e6, "launches_per_step": v["launches_per_step"],
                         "share": v["total_s_per_step"] / sum(x["total_s_per_step"] for x in brk.values())}
                     for k, v in brk.items()},
+        "kernels_timing": "per kind: CUDA graphs of that kind's launches, replayed alone with events",
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
         "gpu_launches": st0.launches_per_step() * args.steps,

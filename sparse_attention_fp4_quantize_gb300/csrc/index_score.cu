@@ -185,6 +185,110 @@ __global__ void __launch_bounds__(kThreads) index_score_kernel(ScoreArgs a) {
     }
 }
 
+// Decode-shaped scoring (Full with one query token per sequence, or Reindex):
+// one warp takes a chunk of CH consecutive 16-key groups of one row and
+// issues every key load of the chunk (and, for Reindex, the chunk's pool ids
+// in one lane-parallel load) before any arithmetic, so each warp keeps
+// CH x 1 KB of keys in flight.
+template <bool FP8>
+__global__ void __launch_bounds__(kThreads, 2) index_score_decode_kernel(ScoreArgs a) {
+    constexpr int ES = FP8 ? 1 : 2;
+    constexpr int NV = FP8 ? 1 : 2;          // 16-byte loads per 16 d-values
+    constexpr int CH = FP8 ? 8 : 4;          // groups per warp chunk
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+    const float NEG_INF = __int_as_float(0xff800000);
+    const int64_t nblocks_n = (a.N + 7) / 8;
+    const bool full = a.mode == CSA2_MODE_FULL;
+    const int64_t rows = full ? (int64_t)a.B : (int64_t)a.B * a.T;
+    const int64_t cpr = (a.groups + CH - 1) / CH;   // chunks per row
+    const int64_t M = full ? a.N : (int64_t)a.P * 8;
+
+    for (int64_t ch = warp; ch < rows * cpr; ch += nwarps) {
+        const int64_t row = ch / cpr;
+        const int64_t g0 = (ch - row * cpr) * CH;
+        const int64_t b = full ? row : row / a.T;
+        int64_t len = a.kv_len[row];
+        len = len < a.N ? len : a.N;
+        int32_t myblk = -1;
+        if (!full && lane < 2 * CH) {
+            const int64_t pidx = 2 * g0 + lane;
+            if (pidx < a.P) {
+                int64_t blk = a.pool[row * a.P + pidx];
+                if (blk < -1 || blk >= nblocks_n) {
+                    flag_error(a.err_flag, CSA2_FLAG_BAD_POOL);
+                    blk = -1;
+                }
+                myblk = (int32_t)blk;
+            }
+        }
+        uint4 raw[CH][2][NV];
+        bool v[CH][2];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                int64_t j;
+                if (full) {
+                    j = (g0 + c) * 16 + g + 8 * r;
+                } else {
+                    const int32_t blk = __shfl_sync(0xFFFFFFFFu, myblk, 2 * c + r);
+                    j = (blk >= 0) ? (int64_t)blk * 8 + g : -1;
+                }
+                v[c][r] = (g0 + c) < a.groups && j >= 0 && j < len;
+                const uint4 *src = reinterpret_cast<const uint4 *>(a.k + ((b * a.N + (v[c][r] ? j : 0)) * 64 + 16 * t4) * ES);
+#pragma unroll
+                for (int u = 0; u < NV; ++u) raw[c][r][u] = v[c][r] ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
+            }
+        }
+        uint32_t qf[8];
+        load_row16<FP8>(a.q + ((row * 4 + (g & 3)) * 64 + 16 * t4) * ES, (g >> 2) == 0, qf);
+        const float w0 = (t4 < 2) ? a.w[row * 4 + 2 * t4] : 0.f;
+        const float w1 = (t4 < 2) ? a.w[row * 4 + 2 * t4 + 1] : 0.f;
+        float *out = a.scores + row * M;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            uint32_t ka[8], kb[8];
+            if constexpr (FP8) {
+                const uint32_t wa[4] = {raw[c][0][0].x, raw[c][0][0].y, raw[c][0][0].z, raw[c][0][0].w};
+                const uint32_t wb[4] = {raw[c][1][0].x, raw[c][1][0].y, raw[c][1][0].z, raw[c][1][0].w};
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2) {
+                    ka[2 * s2] = e4m3x2_to_f16x2(wa[s2] & 0xFFFFu);
+                    ka[2 * s2 + 1] = e4m3x2_to_f16x2(wa[s2] >> 16);
+                    kb[2 * s2] = e4m3x2_to_f16x2(wb[s2] & 0xFFFFu);
+                    kb[2 * s2 + 1] = e4m3x2_to_f16x2(wb[s2] >> 16);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    uint32_t *d = r ? kb : ka;
+                    d[0] = raw[c][r][0].x; d[1] = raw[c][r][0].y; d[2] = raw[c][r][0].z; d[3] = raw[c][r][0].w;
+                    d[4] = raw[c][r][NV - 1].x; d[5] = raw[c][r][NV - 1].y; d[6] = raw[c][r][NV - 1].z; d[7] = raw[c][r][NV - 1].w;
+                }
+            }
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2) {
+                const uint32_t af[4] = {ka[2 * s2], kb[2 * s2], ka[2 * s2 + 1], kb[2 * s2 + 1]};
+                const uint32_t bf[2] = {qf[2 * s2], qf[2 * s2 + 1]};
+                mma16816<FP8>(acc, af, bf);
+            }
+            float s0 = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);
+            float s1 = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);
+            s0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
+            s1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
+            if (t4 == 0) {
+                const int64_t l0 = (g0 + c) * 16 + g, l1 = l0 + 8;
+                if (l0 < M) out[l0] = v[c][0] ? s0 : NEG_INF;
+                if (l1 < M) out[l1] = v[c][1] ? s1 : NEG_INF;
+            }
+        }
+    }
+}
+
 }  // namespace
 }  // namespace csa2
 
@@ -227,10 +331,23 @@ extern "C" csa2_status csa2_index_score(csa2_mode mode, int B, int T, int64_t N,
     int64_t want = (a.tasks + (kThreads / 32) - 1) / (kThreads / 32);
     int64_t cap = (int64_t)num_sms() * 8;
     int blocks = (int)(want < cap ? want : cap);
-    if (q_dt == CSA2_FP8_E4M3)
+    const bool decode = (mode == CSA2_MODE_REINDEX) || T == 1;
+    if (decode) {
+        const int ch = (q_dt == CSA2_FP8_E4M3) ? 8 : 4;
+        const int64_t rows = (mode == CSA2_MODE_FULL) ? (int64_t)B : (int64_t)B * T;
+        const int64_t chunks = rows * ((a.groups + ch - 1) / ch);
+        int64_t want_d = (chunks + (kThreads / 32) - 1) / (kThreads / 32);
+        int64_t cap_d = (int64_t)num_sms() * 2;
+        int blocks_d = (int)(want_d < cap_d ? want_d : cap_d);
+        if (q_dt == CSA2_FP8_E4M3)
+            index_score_decode_kernel<true><<<blocks_d, kThreads, 0, stream_of(stream)>>>(a);
+        else
+            index_score_decode_kernel<false><<<blocks_d, kThreads, 0, stream_of(stream)>>>(a);
+    } else if (q_dt == CSA2_FP8_E4M3) {
         index_score_kernel<true><<<blocks, kThreads, 0, stream_of(stream)>>>(a);
-    else
+    } else {
         index_score_kernel<false><<<blocks, kThreads, 0, stream_of(stream)>>>(a);
+    }
     CSA2_LAUNCH_CHECK("index_score_kernel");
     return CSA2_OK;
 }
