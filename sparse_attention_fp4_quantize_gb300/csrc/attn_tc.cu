@@ -210,8 +210,12 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
                 const int lb = 2 * i + gg;           // group index within this half (0..17)
                 uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                 if (valid) {
-                    const int byte_idx = lb + 2 * half;  // scale byte within the loaded words
-                    const uint32_t sb = (sw[byte_idx >> 2] >> (8 * (byte_idx & 3))) & 0xFFu;
+                    // scale byte lb + 2*half of the loaded words: both candidates use
+                    // compile-time indices (a runtime index would put sw in local memory)
+                    constexpr int b0 = 0;
+                    const uint32_t s_lo = (sw[(lb + b0) >> 2] >> (8 * ((lb + b0) & 3))) & 0xFFu;
+                    const uint32_t s_hi = (sw[(lb + 2) >> 2] >> (8 * ((lb + 2) & 3))) & 0xFFu;
+                    const uint32_t sb = half ? s_hi : s_lo;
                     const uint32_t sc = e4m3_to_f16x2_bcast(sb);
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
@@ -350,13 +354,19 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         const int c_lo = rank * ch_per;
         const int c_hi = min(DV, c_lo + ch_per);
         const int n4 = (c_hi > c_lo) ? (c_hi - c_lo) / 4 : 0;
+        const float *src[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) src[r] = cluster.map_shared_rank(sPO, r < S ? r : 0);
         for (int t = tid; t < HB * n4; t += THREADS) {
             const int h = t / n4, c = c_lo + 4 * (t - h * n4);
+            float4 v[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)   // all remote loads first, then the sum
+                if (r < S) v[r] = *reinterpret_cast<const float4 *>(src[r] + h * PO_STRIDE + c);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int r = 0; r < S; ++r) {
-                const float4 v = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(sPO, r) + h * PO_STRIDE + c);
-                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                if (r < S) { acc.x += v[r].x; acc.y += v[r].y; acc.z += v[r].z; acc.w += v[r].w; }
             *reinterpret_cast<float4 *>(a.out + ((bt * a.H) + h0 + h) * (int64_t)DV + c) = acc;
         }
         if (rank == 0 && a.lse && tid < HB) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
