@@ -1,5 +1,6 @@
 // Sparse FP4 attention on the 5th-generation tensor cores (tcgen05, TMEM),
-// for 576-channel entries (512 latent + 64 RoPE), dv = 512, 64-head blocks.
+// for 576-channel entries (512 latent + 64 RoPE), dv = 512, 64-head blocks,
+// up to 512 selected entries.
 // Sources: "DeepSeek-V4.1-Flash：把 KV Cache 压缩到极限的百万上下文 MoE", section
 // "效率组件四件" item 4 (FP4 main KV) and the inference bullet of
 // "优化器与训练基础设施" (Reuse layers run a fused attention kernel; prior art);
@@ -7,21 +8,24 @@
 // paragraph.  The attention itself is the MLA-style reading (K = all 576
 // channels, V = the first 512).
 //
-// Layout of the work.  A thread-block cluster of S = ceil(K/128) CTAs serves
+// Layout of the work.  A thread-block cluster of S in {1, 2, 4} CTAs serves
 // one query token and 64 heads; CTA c owns selected entries [128c, 128c+128).
-// Every matrix product is a 128-row tcgen05.mma with fp32 accumulators in TMEM:
-//   S^T [128 entries x 64 heads] = Khat [128 x 576] . Q^T      (36 MMAs, K=16)
-//   O^T [512 ch x 64 heads]     += Vhat^T [512 x 128] . P^T    (4 x 8 MMAs)
-// Khat is written ONCE to shared memory by the dequantiser (E2M1 x E4M3 ->
-// exact f16) in the no-swizzle core-matrix layout; the S product reads it
-// K-major and the P V product reads the same bytes MN-major as Vhat^T.
-// Q (bf16) is scaled per head by a power of two into f16 (exact) and the
-// scale is folded into the logit factor.  Softmax runs on a transposed copy
-// of S^T in shared memory; P is rounded to f16 for the second product.
-// The S CTAs then merge their partial outputs through distributed shared
-// memory (no global scratch, no second kernel): each CTA scales its O by
-// 2^(m_c - M) / L per head and CTA c sums channel slice c over the cluster.
-// Waits on the MMA completion barrier are bounded; on timeout the kernel sets
+//  1. The TMA engine gathers the operands: one bulk copy per Q head row
+//     (1152 B) and one per selected entry's code row (288 B), completing on
+//     one mbarrier; the 36-byte scale rows (not 16-byte sized) are plain loads.
+//  2. Q (bf16) is scaled per head by a power of two into f16 (exact; the scale
+//     is folded into the logit factor); the entries are dequantised once
+//     (E2M1 x E4M3 -> exact f16) into a no-swizzle core-matrix tile.
+//  3. S^T [128 entries x 64 heads] = Khat . Q^T  (36 tcgen05.mma, M128 N64 K16)
+//  4. softmax on a transposed copy of S^T in shared memory; P -> f16.
+//  5. O^T [512 ch x 64 heads] = Vhat^T . P^T  (4 x 8 MMAs; the same Khat bytes
+//     read MN-major), fp32 accumulators in TMEM.
+//  6. Merge across the cluster by PUSHING: every CTA stores its raw O slices
+//     and its per-head (max, sum) into the shared memory of the CTA that owns
+//     each channel slice (fire-and-forget distributed-shared-memory stores),
+//     one cluster barrier, then each owner combines its slice locally with
+//     weights 2^(m_c - M) / L and writes it out.
+// Waits on the mbarriers are bounded; on timeout the kernel sets
 // CSA2_FLAG_TIMEOUT and still runs every cluster barrier, so it always ends.
 #include <cooperative_groups.h>
 
@@ -36,32 +40,38 @@ namespace {
 constexpr int TM = 128;                    // entries per CTA (MMA M)
 constexpr int D = 576, DV = 512, HB = 64;  // channels, value channels, heads per cluster
 constexpr int THREADS = 256;
-constexpr uint32_t KT_SBO = (D / 8) * 128;      // 9216: bytes per 8-entry group of the Khat tile
+constexpr int MAX_S = 4;                   // CTAs per cluster
+constexpr uint32_t KT_SBO = (D / 8) * 128;        // 9216: bytes per 8-entry group of the Khat tile
 constexpr uint32_t KT_BYTES = (TM / 8) * KT_SBO;  // 147456
-constexpr uint32_t Q_SBO = (D / 8) * 128;        // 9216: bytes per 8-head group of the Q tile
-constexpr uint32_t Q_BYTES = (HB / 8) * Q_SBO;   // 73728
-constexpr int ST_STRIDE = TM + 4;               // fp32 row stride of the transposed S (132)
-constexpr uint32_t ST_BYTES = HB * ST_STRIDE * 4;  // 33792
-constexpr uint32_t P_SBO = (TM / 8) * 128;       // 2048: bytes per 8-head group of the P tile
-constexpr int PO_STRIDE = DV + 4;               // fp32 row stride of the partial O (516)
+constexpr uint32_t Q_SBO = (D / 8) * 128;         // 9216: bytes per 8-head group of the Q tile
+constexpr uint32_t Q_BYTES = (HB / 8) * Q_SBO;    // 73728
+constexpr uint32_t QRAW_STRIDE = D * 2 + 16;      // 1168: staged bf16 Q rows (padded: conflict-free reads)
+constexpr uint32_t CRAW_STRIDE = D / 2 + 16;      // 304: staged code rows (padded)
+constexpr uint32_t OFF_QRAW = 0;                  // staging lives in the Khat region before dequant
+constexpr uint32_t OFF_CRAW = HB * QRAW_STRIDE;   // 74752
+constexpr int ST_STRIDE = TM + 4;                 // fp32 row stride of the transposed S (132)
+constexpr uint32_t ST_BYTES = HB * ST_STRIDE * 4; // 33792
+constexpr uint32_t P_SBO = (TM / 8) * 128;        // 2048: bytes per 8-head group of the P tile
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_Q = OFF_K + KT_BYTES;
-constexpr uint32_t OFF_ST = OFF_Q;              // reuses the Q tile after S is computed
+constexpr uint32_t OFF_ST = OFF_Q;                // reuses the Q tile after S is computed
 constexpr uint32_t OFF_P = OFF_Q + ST_BYTES;
 constexpr uint32_t OFF_MISC = OFF_Q + Q_BYTES;
-constexpr uint32_t OFF_BAR = OFF_MISC;          // 2 mbarriers
-constexpr uint32_t OFF_TMEM = OFF_BAR + 16;
-constexpr uint32_t OFF_VALID = OFF_TMEM + 16;   // int[128]
-constexpr uint32_t OFF_CS = OFF_VALID + TM * 4;  // float[64] logit factor per head
-constexpr uint32_t OFF_M = OFF_CS + HB * 4;      // float[64] row max (log2 domain)
-constexpr uint32_t OFF_L = OFF_M + HB * 4;       // float[64] row sum
-constexpr uint32_t OFF_W = OFF_L + HB * 4;       // float[64] merge weight
-constexpr uint32_t OFF_LSE = OFF_W + HB * 4;     // float[64] final lse (natural log)
+constexpr uint32_t OFF_BAR = OFF_MISC;            // 3 mbarriers
+constexpr uint32_t OFF_TMEM = OFF_BAR + 32;
+constexpr uint32_t OFF_VALID = OFF_TMEM + 16;     // int[128]
+constexpr uint32_t OFF_CS = OFF_VALID + TM * 4;   // float[64] logit factor per head
+constexpr uint32_t OFF_M = OFF_CS + HB * 4;       // float[64] row max (log2 domain)
+constexpr uint32_t OFF_L = OFF_M + HB * 4;        // float[64] row sum
+constexpr uint32_t OFF_XCH = OFF_L + HB * 4;      // float[MAX_S][2][64] received (max, sum)
+constexpr uint32_t OFF_W = OFF_XCH + MAX_S * 2 * HB * 4;  // float[MAX_S][64] merge weights
+constexpr uint32_t OFF_LSE = OFF_W + MAX_S * HB * 4;      // float[64]
 constexpr uint32_t SMEM = OFF_LSE + HB * 4;
-constexpr uint32_t TMEM_COLS = 512;             // S^T: 64 cols, O^T: 4 x 64 cols
+constexpr uint32_t TMEM_COLS = 512;               // S^T: 64 cols, O^T: 4 x 64 cols
 constexpr uint32_t S_COL = 0, O_COL = 64;
-constexpr uint32_t MAX_POLLS = 1u << 22;  // about a second of polling at most
-static_assert(HB * PO_STRIDE * 4 <= KT_BYTES, "partial O must fit in the Khat region");
+constexpr uint32_t MAX_POLLS = 1u << 22;          // about a second of polling at most
+static_assert(OFF_CRAW + TM * CRAW_STRIDE <= KT_BYTES, "staging must fit in the Khat region");
+static_assert(HB * (DV + 4 * MAX_S) * 4 <= KT_BYTES, "received partials must fit in the Khat region");
 static_assert(ST_BYTES + (HB / 8) * P_SBO <= Q_BYTES, "S^T copy and P must fit in the Q region");
 static_assert(SMEM <= 227 * 1024, "shared memory");
 
@@ -108,6 +118,28 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Bulk global -> shared copy (TMA engine) completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Store to the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ void st_remote(const void *local_ptr, uint32_t rank, float v) {
+    uint32_t la = tc::smem_u32(local_ptr), ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+
 __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     cg::cluster_group cluster = cg::this_cluster();
@@ -127,50 +159,61 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     uint8_t *sQ = smem + OFF_Q;
     float *sT = reinterpret_cast<float *>(smem + OFF_ST);
     uint8_t *sP = smem + OFF_P;
-    float *sPO = reinterpret_cast<float *>(smem + OFF_K);  // partial O after P V
+    float *sRecv = reinterpret_cast<float *>(smem + OFF_K);  // received partial O after P V
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     int *sValid = reinterpret_cast<int *>(smem + OFF_VALID);
     float *sCs = reinterpret_cast<float *>(smem + OFF_CS);
     float *sM = reinterpret_cast<float *>(smem + OFF_M);
     float *sL = reinterpret_cast<float *>(smem + OFF_L);
+    float *sXch = reinterpret_cast<float *>(smem + OFF_XCH);
     float *sW = reinterpret_cast<float *>(smem + OFF_W);
     float *sLse = reinterpret_cast<float *>(smem + OFF_LSE);
-    const uint32_t bar_s = tc::smem_u32(smem + OFF_BAR);
-    const uint32_t bar_o = bar_s + 8;
+    const uint32_t bar_ld = tc::smem_u32(smem + OFF_BAR);
+    const uint32_t bar_s = bar_ld + 8;
+    const uint32_t bar_o = bar_ld + 16;
 
-    // ---- 1. issue every global load of this CTA first: the entry's codes/scales, Q
+    if (tid == 0) {
+        tc::mbar_init(bar_ld, TM);   // one arrival per entry thread
+        tc::mbar_init(bar_s, 1);
+        tc::mbar_init(bar_o, 1);
+        tc::mbar_init_fence();
+    }
+    if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
+    __syncthreads();
+
+    // ---- 1. gather: TMA bulk copies of Q rows and the selected code rows
     const int e = tid & (TM - 1);   // entry of this thread in the tile
     const int half = tid >> 7;      // which 288 channels of the entry
     const int sel = rank * TM + e;
     int64_t j = (sel < a.K) ? (int64_t)__ldg(a.idx + bt * a.K + sel) : -1;
     const bool valid = j >= 0 && j < len;
-    if (!valid && j != -1 && half == 0) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
-    uint4 cw[9];
     uint32_t sw[5];
     if (valid) {
-        const uint8_t *crow = a.codes + (b * a.N + j) * (D / 2) + half * 144;
         const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + (b * a.N + j) * (D / 16)) + 4 * half;
-#pragma unroll
-        for (int i = 0; i < 9; ++i) cw[i] = __ldg(reinterpret_cast<const uint4 *>(crow) + i);
 #pragma unroll
         for (int i = 0; i < 5; ++i) sw[i] = __ldg(srow + i);
     }
-    const int hq = warp * 8 + (lane & 7);   // head (within the block) whose Q this lane loads
-    const uint16_t *qrow = a.q + ((bt * a.H) + h0 + hq) * (int64_t)D;
-    uint4 qv[18];
-#pragma unroll
-    for (int i = 0; i < 18; ++i) qv[i] = __ldg(reinterpret_cast<const uint4 *>(qrow) + (lane >> 3) + 4 * i);
-
-    if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
-    if (tid == 0) {
-        tc::mbar_init(bar_s, 1);
-        tc::mbar_init(bar_o, 1);
-        tc::mbar_init_fence();
+    if (half == 0) {
+        if (!valid && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
+        sValid[e] = valid ? 1 : 0;
+        if (e < HB) {
+            const uint16_t *qrow = a.q + ((bt * a.H) + h0 + e) * (int64_t)D;
+            mbar_expect_tx(bar_ld, D * 2);
+            bulk_g2s(tc::smem_u32(smem + OFF_QRAW + e * QRAW_STRIDE), qrow, D * 2, bar_ld);
+        }
+        mbar_arrive_expect_tx(bar_ld, valid ? D / 2 : 0);
+        if (valid)
+            bulk_g2s(tc::smem_u32(smem + OFF_CRAW + e * CRAW_STRIDE), a.codes + (b * a.N + j) * (D / 2), D / 2, bar_ld);
     }
-    if (half == 0) sValid[e] = valid ? 1 : 0;
+    bool ok = tc::mbar_wait(bar_ld, 0, MAX_POLLS);
 
-    // ---- 2. Q -> f16 with a per-head power-of-two scale, core-matrix layout [head][channel]
+    // ---- 2a. staged Q -> registers, per-head power-of-two scale, f16 core-matrix tile [head][channel]
     {
+        const int hq = warp * 8 + (lane & 7);
+        const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE;
+        uint4 qv[18];
+#pragma unroll
+        for (int i = 0; i < 18; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + ((lane >> 3) + 4 * i) * 16);
         float mx = 0.f;
 #pragma unroll
         for (int i = 0; i < 18; ++i) {
@@ -193,30 +236,33 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
-            const int c8 = (lane >> 3) + 4 * i;
-            *reinterpret_cast<uint4 *>(qdst + c8 * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(qdst + ((lane >> 3) + 4 * i) * 128) = make_uint4(o[0], o[1], o[2], o[3]);
         }
         if ((lane >> 3) == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
     }
-
-    // ---- 3. dequantise this thread's 288 channels of its entry into the Khat tile
+    // ---- 2b. staged codes -> registers (the Khat tile overwrites the staging area)
+    uint4 cw[9];
+    {
+        const uint8_t *craw = smem + OFF_CRAW + e * CRAW_STRIDE + half * 144;
+#pragma unroll
+        for (int i = 0; i < 9; ++i) cw[i] = valid ? *reinterpret_cast<const uint4 *>(craw + 16 * i) : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    // ---- 2c. dequantise this thread's 288 channels of its entry into the Khat tile
     {
         uint8_t *kdst = sK + (e >> 3) * KT_SBO + (e & 7) * 16;
 #pragma unroll
         for (int i = 0; i < 9; ++i) {
             const uint32_t w4[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
 #pragma unroll
-            for (int gg = 0; gg < 2; ++gg) {          // the two 16-channel groups of this chunk
-                const int lb = 2 * i + gg;           // group index within this half (0..17)
+            for (int gg = 0; gg < 2; ++gg) {           // the two 16-channel groups of this chunk
+                const int lb = 2 * i + gg;            // group index within this half (0..17)
                 uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
                 if (valid) {
-                    // scale byte lb + 2*half of the loaded words: both candidates use
-                    // compile-time indices (a runtime index would put sw in local memory)
-                    constexpr int b0 = 0;
-                    const uint32_t s_lo = (sw[(lb + b0) >> 2] >> (8 * ((lb + b0) & 3))) & 0xFFu;
+                    // scale byte lb + 2*half of the loaded words, compile-time indices only
+                    const uint32_t s_lo = (sw[lb >> 2] >> (8 * (lb & 3))) & 0xFFu;
                     const uint32_t s_hi = (sw[(lb + 2) >> 2] >> (8 * ((lb + 2) & 3))) & 0xFFu;
-                    const uint32_t sb = half ? s_hi : s_lo;
-                    const uint32_t sc = e4m3_to_f16x2_bcast(sb);
+                    const uint32_t sc = e4m3_to_f16x2_bcast(half ? s_hi : s_lo);
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
                         const uint32_t wd = w4[2 * gg + k];
@@ -236,7 +282,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // ---- 4. S^T = Khat . Q^T  (M = 128 entries, N = 64 heads, K = 576)
+    // ---- 3. S^T = Khat . Q^T  (M = 128 entries, N = 64 heads, K = 576)
     if (tid == 0) {
         const uint32_t a0 = tc::smem_u32(sK), b0 = tc::smem_u32(sQ);
         constexpr uint32_t idesc = tc::idesc_f16_f32(TM, HB, false, false);
@@ -246,10 +292,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
                         tc::desc_noswizzle(b0 + ks * 256, 128, Q_SBO), idesc, ks > 0);
         tc::commit(bar_s);
     }
-    bool ok = tc::mbar_wait(bar_s, 0, MAX_POLLS);
+    ok = tc::mbar_wait(bar_s, 0, MAX_POLLS) && ok;
     tc::fence_after();
 
-    // ---- 5. S^T -> shared memory, transposed to [head][entry] (the Q tile is free now)
+    // ---- 4a. S^T -> shared memory, transposed to [head][entry] (the Q tile is free now)
     const int quarter = warp & 3, hh = warp >> 2;
     {
         uint32_t r[32];
@@ -265,7 +311,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     }
     __syncthreads();
 
-    // ---- 6. softmax per head over this CTA's entries; P -> f16 core-matrix layout [head][entry]
+    // ---- 4b. softmax per head over this CTA's entries; P -> f16 core-matrix tile [head][entry]
     {
         const int h = tid >> 2, part = tid & 3;
         float z[32];
@@ -299,7 +345,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     __syncthreads();
     tc::fence_after();
 
-    // ---- 7. O^T = Vhat^T . P^T  (4 blocks of M = 128 channels, N = 64 heads, K = 128 entries)
+    // ---- 5. O^T = Vhat^T . P^T  (4 blocks of M = 128 channels, N = 64 heads, K = 128 entries)
     if (tid == 0) {
         const uint32_t a0 = tc::smem_u32(sK), b0 = tc::smem_u32(sP);
         constexpr uint32_t idesc = tc::idesc_f16_f32(TM, HB, true, false);
@@ -314,64 +360,62 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     tc::fence_after();
     if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
 
-    // ---- 8. merge weights across the cluster: M = max_c m_c, L = sum_c l_c 2^(m_c - M)
-    cluster.sync();
+    // ---- 6. push raw O slices and (max, sum) to the owners of the channel slices
+    const int W = DV / S;                     // channels per owner
+    const int RS = W + 4;                     // row stride of a received slice
+    tc::fence_before();
+    cluster.sync();                           // every CTA finished reading its Khat tile
     if (tid < HB) {
-        float M = -INFINITY;
-        for (int c = 0; c < S; ++c) M = fmaxf(M, cluster.map_shared_rank(sM, c)[tid]);
-        float L = 0.f;
-        if (M != -INFINITY)
-            for (int c = 0; c < S; ++c) {
-                const float mc = cluster.map_shared_rank(sM, c)[tid];
-                if (mc != -INFINITY) L += cluster.map_shared_rank(sL, c)[tid] * ex2(mc - M);
-            }
-        const float mine = sM[tid];
-        sW[tid] = (L > 0.f && mine != -INFINITY) ? ex2(mine - M) / L : 0.f;
-        sLse[tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+        for (int o = 0; o < S; ++o) {
+            st_remote(sXch + (rank * 2 + 0) * HB + tid, (uint32_t)o, sM[tid]);
+            st_remote(sXch + (rank * 2 + 1) * HB + tid, (uint32_t)o, sL[tid]);
+        }
     }
-    __syncthreads();
-
-    // ---- 9. scaled partial O -> shared memory [head][channel] (the Khat tile is free now)
 #pragma unroll 1
     for (int mb = 0; mb < DV / 128; ++mb) {
         uint32_t r[32];
         tc::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * HB + 32 * hh, r);
         tc::tmem_ld_wait();
         const int ch = mb * 128 + 32 * quarter + lane;
+        const int owner = ch / W;
+        float *dst = sRecv + (rank * HB) * RS + (ch - owner * W);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int h = 32 * hh + jj;
-            sPO[h * PO_STRIDE + ch] = __uint_as_float(r[jj]) * sW[h];
-        }
+        for (int jj = 0; jj < 32; ++jj) st_remote(dst + (32 * hh + jj) * RS, (uint32_t)owner, __uint_as_float(r[jj]));
     }
     tc::fence_before();
-    cluster.sync();  // every CTA's scaled partial is in its shared memory
+    cluster.sync();                           // all partials delivered
 
-    // ---- 10. CTA `rank` sums its channel slice over the cluster and writes out
+    // ---- 7. combine this CTA's channel slice: weights 2^(m_c - M) / L per head
+    if (tid < HB) {
+        float M = -INFINITY;
+        for (int c = 0; c < S; ++c) M = fmaxf(M, sXch[(c * 2) * HB + tid]);
+        float L = 0.f;
+        for (int c = 0; c < S; ++c) {
+            const float mc = sXch[(c * 2) * HB + tid];
+            const float wc = (M == -INFINITY || mc == -INFINITY) ? 0.f : ex2(mc - M);
+            sW[c * HB + tid] = wc;
+            L += wc * sXch[(c * 2 + 1) * HB + tid];
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int c = 0; c < S; ++c) sW[c * HB + tid] *= inv;
+        sLse[tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();
     {
-        int ch_per = (DV + S - 1) / S;
-        ch_per = (ch_per + 3) & ~3;
-        const int c_lo = rank * ch_per;
-        const int c_hi = min(DV, c_lo + ch_per);
-        const int n4 = (c_hi > c_lo) ? (c_hi - c_lo) / 4 : 0;
-        const float *src[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) src[r] = cluster.map_shared_rank(sPO, r < S ? r : 0);
+        const int c_lo = rank * W;
+        const int n4 = W / 4;
         for (int t = tid; t < HB * n4; t += THREADS) {
-            const int h = t / n4, c = c_lo + 4 * (t - h * n4);
-            float4 v[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r)   // all remote loads first, then the sum
-                if (r < S) v[r] = *reinterpret_cast<const float4 *>(src[r] + h * PO_STRIDE + c);
+            const int h = t / n4, c = 4 * (t - h * n4);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-                if (r < S) { acc.x += v[r].x; acc.y += v[r].y; acc.z += v[r].z; acc.w += v[r].w; }
-            *reinterpret_cast<float4 *>(a.out + ((bt * a.H) + h0 + h) * (int64_t)DV + c) = acc;
+            for (int src = 0; src < S; ++src) {
+                const float w = sW[src * HB + h];
+                const float4 v = *reinterpret_cast<const float4 *>(sRecv + (src * HB + h) * RS + c);
+                acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+            }
+            *reinterpret_cast<float4 *>(a.out + ((bt * a.H) + h0 + h) * (int64_t)DV + c_lo + c) = acc;
         }
         if (rank == 0 && a.lse && tid < HB) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
     }
-    cluster.sync();  // remote reads done before any CTA leaves
     tc::fence_after();
     if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -379,7 +423,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
 }  // namespace
 
 bool sparse_attn_tc_supported(int D_, int dv, int H, int K) {
-    return D_ == D && dv == DV && H % HB == 0 && K >= 1 && K <= 8 * TM;
+    return D_ == D && dv == DV && H % HB == 0 && K >= 1 && K <= MAX_S * TM;
 }
 
 csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const void *q, const uint8_t *codes,
@@ -390,7 +434,8 @@ csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const v
                    "sparse_attn_tc: smem attribute");
     TcArgs a;
     a.T = T; a.H = H; a.K = K; a.N = N;
-    a.csize = (K + TM - 1) / TM;
+    const int tiles = (K + TM - 1) / TM;
+    a.csize = tiles <= 1 ? 1 : (tiles <= 2 ? 2 : 4);   // 1, 2 or 4: the channel slices divide 512
     a.hblocks = H / HB;
     a.q = (const uint16_t *)q; a.codes = codes; a.scales = scales; a.idx = idx; a.kv_len = kv_len;
     a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.err_flag = err_flag;
