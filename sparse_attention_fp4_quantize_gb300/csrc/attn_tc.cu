@@ -71,7 +71,7 @@ constexpr uint32_t TMEM_COLS = 512;               // S^T: 64 cols, O^T: 4 x 64 c
 constexpr uint32_t S_COL = 0, O_COL = 64;
 constexpr uint32_t MAX_POLLS = 1u << 22;          // about a second of polling at most
 static_assert(OFF_CRAW + TM * CRAW_STRIDE <= KT_BYTES, "staging must fit in the Khat region");
-static_assert(HB * (DV + 4 * MAX_S) * 4 <= KT_BYTES, "received partials must fit in the Khat region");
+static_assert(DV * (HB + 4) * 4 <= KT_BYTES, "received partials must fit in the Khat region");
 static_assert(ST_BYTES + (HB / 8) * P_SBO <= Q_BYTES, "S^T copy and P must fit in the Q region");
 static_assert(SMEM <= 227 * 1024, "shared memory");
 
@@ -133,11 +133,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-// Store to the shared memory of CTA `rank` of this cluster.
-__device__ __forceinline__ void st_remote(const void *local_ptr, uint32_t rank, float v) {
+// Stores to the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t remote_addr(const void *local_ptr, uint32_t rank) {
     uint32_t la = tc::smem_u32(local_ptr), ra;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+    return ra;
+}
+
+__device__ __forceinline__ void st_remote(const void *local_ptr, uint32_t rank, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote_addr(local_ptr, rank)), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_remote4(uint32_t raddr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(raddr), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
 }
 
 __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
@@ -361,8 +370,9 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
 
     // ---- 6. push raw O slices and (max, sum) to the owners of the channel slices
+    // received layout on the owner: [source][channel in slice][head] (+4 pad per row)
     const int W = DV / S;                     // channels per owner
-    const int RS = W + 4;                     // row stride of a received slice
+    constexpr int RS = HB + 4;                // row stride (floats) of one received channel
     tc::fence_before();
     cluster.sync();                           // every CTA finished reading its Khat tile
     if (tid < HB) {
@@ -378,9 +388,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         tc::tmem_ld_wait();
         const int ch = mb * 128 + 32 * quarter + lane;
         const int owner = ch / W;
-        float *dst = sRecv + (rank * HB) * RS + (ch - owner * W);
+        const uint32_t dst = remote_addr(sRecv + ((size_t)rank * W + (ch - owner * W)) * RS + 32 * hh, (uint32_t)owner);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) st_remote(dst + (32 * hh + jj) * RS, (uint32_t)owner, __uint_as_float(r[jj]));
+        for (int q4 = 0; q4 < 8; ++q4)
+            st_remote4(dst + 16 * q4, r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
     }
     tc::fence_before();
     cluster.sync();                           // all partials delivered
@@ -402,17 +413,22 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     }
     __syncthreads();
     {
+        // thread -> (4 heads, channel): lanes take consecutive channels, so each
+        // output store of a warp covers 32 consecutive channels of one head
         const int c_lo = rank * W;
-        const int n4 = W / 4;
-        for (int t = tid; t < HB * n4; t += THREADS) {
-            const int h = t / n4, c = 4 * (t - h * n4);
+        for (int t = tid; t < (HB / 4) * W; t += THREADS) {
+            const int h4 = t / W, c = t - h4 * W;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int src = 0; src < S; ++src) {
-                const float w = sW[src * HB + h];
-                const float4 v = *reinterpret_cast<const float4 *>(sRecv + (src * HB + h) * RS + c);
-                acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+                const float4 v = *reinterpret_cast<const float4 *>(sRecv + ((size_t)src * W + c) * RS + 4 * h4);
+                const float *w = sW + src * HB + 4 * h4;
+                acc.x += w[0] * v.x; acc.y += w[1] * v.y; acc.z += w[2] * v.z; acc.w += w[3] * v.w;
             }
-            *reinterpret_cast<float4 *>(a.out + ((bt * a.H) + h0 + h) * (int64_t)DV + c_lo + c) = acc;
+            float *o = a.out + ((bt * a.H) + h0 + 4 * h4) * (int64_t)DV + c_lo + c;
+            o[0] = acc.x;
+            o[DV] = acc.y;
+            o[2 * DV] = acc.z;
+            o[3 * DV] = acc.w;
         }
         if (rank == 0 && a.lse && tid < HB) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
     }
