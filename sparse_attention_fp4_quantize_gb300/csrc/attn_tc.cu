@@ -57,7 +57,7 @@ constexpr uint32_t OFF_Q = OFF_K + KT_BYTES;
 constexpr uint32_t OFF_ST = OFF_Q;                // reuses the Q tile after S is computed
 constexpr uint32_t OFF_P = OFF_Q + ST_BYTES;
 constexpr uint32_t OFF_MISC = OFF_Q + Q_BYTES;
-constexpr uint32_t OFF_BAR = OFF_MISC;            // 3 mbarriers
+constexpr uint32_t OFF_BAR = OFF_MISC;            // 4 mbarriers
 constexpr uint32_t OFF_TMEM = OFF_BAR + 32;
 constexpr uint32_t OFF_VALID = OFF_TMEM + 16;     // int[128]
 constexpr uint32_t OFF_CS = OFF_VALID + TM * 4;   // float[64] logit factor per head
@@ -71,7 +71,8 @@ constexpr uint32_t TMEM_COLS = 512;               // S^T: 64 cols, O^T: 4 x 64 c
 constexpr uint32_t S_COL = 0, O_COL = 64;
 constexpr uint32_t MAX_POLLS = 1u << 22;          // about a second of polling at most
 static_assert(OFF_CRAW + TM * CRAW_STRIDE <= KT_BYTES, "staging must fit in the Khat region");
-static_assert(DV * (HB + 4) * 4 <= KT_BYTES, "received partials must fit in the Khat region");
+static_assert((DV * (HB + 4) + MAX_S * 2 * HB) * 4 <= KT_BYTES, "received partials must fit in the Khat region");
+static_assert(((DV / 2) * (HB + 4) + 2 * HB) * 4 <= Q_BYTES, "a staged slice must fit in the Q region");
 static_assert(ST_BYTES + (HB / 8) * P_SBO <= Q_BYTES, "S^T copy and P must fit in the Q region");
 static_assert(SMEM <= 227 * 1024, "shared memory");
 
@@ -133,6 +134,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Bulk copy from this CTA's shared memory to another CTA's (TMA engine),
+// completing on the destination CTA's mbarrier.
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_remote, uint32_t src_local, uint32_t bytes, uint32_t bar_remote) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_remote),
+                 "r"(src_local), "r"(bytes), "r"(bar_remote)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // Stores to the shared memory of CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t remote_addr(const void *local_ptr, uint32_t rank) {
     uint32_t la = tc::smem_u32(local_ptr), ra;
@@ -180,11 +192,13 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     const uint32_t bar_ld = tc::smem_u32(smem + OFF_BAR);
     const uint32_t bar_s = bar_ld + 8;
     const uint32_t bar_o = bar_ld + 16;
+    const uint32_t bar_rx = bar_ld + 24;
 
     if (tid == 0) {
         tc::mbar_init(bar_ld, TM);   // one arrival per entry thread
         tc::mbar_init(bar_s, 1);
         tc::mbar_init(bar_o, 1);
+        tc::mbar_init(bar_rx, 1);
         tc::mbar_init_fence();
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -369,43 +383,68 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     tc::fence_after();
     if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
 
-    // ---- 6. push raw O slices and (max, sum) to the owners of the channel slices
-    // received layout on the owner: [source][channel in slice][head] (+4 pad per row)
-    const int W = DV / S;                     // channels per owner
-    constexpr int RS = HB + 4;                // row stride (floats) of one received channel
+    // ---- 6. send raw O slices and (max, sum) to the owners of the channel slices
+    // Payload for owner o: [W channels][RS floats: 64 heads + pad] then 64 max + 64 sum.
+    // Slices for other CTAs are staged in this CTA's Q region and moved by the
+    // TMA engine (bulk shared -> remote shared copies completing on the owner's
+    // mbarrier); the own slice is written in place.
+    const int W = DV / S;                      // channels per owner
+    constexpr int RS = HB + 4;                 // floats per received channel row
+    const uint32_t slice_floats = (uint32_t)W * RS + 2 * HB;
+    const uint32_t slice_bytes = slice_floats * 4;
+    float *stage = reinterpret_cast<float *>(smem + OFF_Q);   // free after P V
+    if (tid == 0) asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_rx),
+                               "r"((uint32_t)(S - 1) * slice_bytes) : "memory");
     tc::fence_before();
-    cluster.sync();                           // every CTA finished reading its Khat tile
-    if (tid < HB) {
-        for (int o = 0; o < S; ++o) {
-            st_remote(sXch + (rank * 2 + 0) * HB + tid, (uint32_t)o, sM[tid]);
-            st_remote(sXch + (rank * 2 + 1) * HB + tid, (uint32_t)o, sL[tid]);
+    cluster.sync();                            // every CTA finished with its Khat tile
+    for (int o = 0; o < S; ++o) {
+        const int oo = (rank + 1 + o) % S;     // own slice last
+        float *dst = (oo == rank) ? sRecv + (size_t)rank * slice_floats : stage;
+        if (oo != rank && o > 0) {
+            if (tid == 0) bulk_wait_read0();   // the staging buffer is free again
+            __syncthreads();
+        }
+        for (int mb = oo * W / 128; mb < (oo + 1) * W / 128; ++mb) {
+            uint32_t r[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * HB + 32 * hh, r);
+            tc::tmem_ld_wait();
+            float *row = dst + (size_t)(mb * 128 - oo * W + 32 * quarter + lane) * RS + 32 * hh;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+                *reinterpret_cast<uint4 *>(row + 4 * q4) = make_uint4(r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
+        }
+        if (tid < HB) {
+            dst[(size_t)W * RS + tid] = sM[tid];
+            dst[(size_t)W * RS + HB + tid] = sL[tid];
+        }
+        if (oo != rank) {
+            tc::fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                uint32_t rdst, rbar;
+                const uint32_t ldst = tc::smem_u32(sRecv + (size_t)rank * slice_floats);
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rdst) : "r"(ldst), "r"((uint32_t)oo));
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar_rx), "r"((uint32_t)oo));
+                bulk_s2s(rdst, tc::smem_u32(stage), slice_bytes, rbar);
+                bulk_commit();
+            }
         }
     }
-#pragma unroll 1
-    for (int mb = 0; mb < DV / 128; ++mb) {
-        uint32_t r[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * HB + 32 * hh, r);
-        tc::tmem_ld_wait();
-        const int ch = mb * 128 + 32 * quarter + lane;
-        const int owner = ch / W;
-        const uint32_t dst = remote_addr(sRecv + ((size_t)rank * W + (ch - owner * W)) * RS + 32 * hh, (uint32_t)owner);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-            st_remote4(dst + 16 * q4, r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
-    }
-    tc::fence_before();
-    cluster.sync();                           // all partials delivered
+    if (tid == 0) bulk_wait_read0();           // staging reads done before this CTA may exit
+    ok = tc::mbar_wait(bar_rx, 0, MAX_POLLS) && ok;   // the other CTAs' slices have landed
+    __syncthreads();
+    if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
 
     // ---- 7. combine this CTA's channel slice: weights 2^(m_c - M) / L per head
     if (tid < HB) {
         float M = -INFINITY;
-        for (int c = 0; c < S; ++c) M = fmaxf(M, sXch[(c * 2) * HB + tid]);
+        for (int c = 0; c < S; ++c) M = fmaxf(M, sRecv[(size_t)c * slice_floats + W * RS + tid]);
         float L = 0.f;
         for (int c = 0; c < S; ++c) {
-            const float mc = sXch[(c * 2) * HB + tid];
+            const float mc = sRecv[(size_t)c * slice_floats + W * RS + tid];
             const float wc = (M == -INFINITY || mc == -INFINITY) ? 0.f : ex2(mc - M);
             sW[c * HB + tid] = wc;
-            L += wc * sXch[(c * 2 + 1) * HB + tid];
+            L += wc * sRecv[(size_t)c * slice_floats + W * RS + HB + tid];
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
         for (int c = 0; c < S; ++c) sW[c * HB + tid] *= inv;
@@ -420,7 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
             const int h4 = t / W, c = t - h4 * W;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int src = 0; src < S; ++src) {
-                const float4 v = *reinterpret_cast<const float4 *>(sRecv + ((size_t)src * W + c) * RS + 4 * h4);
+                const float4 v = *reinterpret_cast<const float4 *>(sRecv + (size_t)src * slice_floats + (size_t)c * RS + 4 * h4);
                 const float *w = sW + src * HB + 4 * h4;
                 acc.x += w[0] * v.x; acc.y += w[1] * v.y; acc.z += w[2] * v.z; acc.w += w[3] * v.w;
             }
