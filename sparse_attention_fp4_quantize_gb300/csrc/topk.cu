@@ -312,14 +312,9 @@ csa2_status launch_topk(const TopkArgs &in, int64_t Lmax, cudaStream_t stream) {
         if (c > 1 && region < 2 * (int64_t)c * a.K) region = 2 * (int64_t)c * a.K;
         return (size_t)(region + 2 * (int64_t)a.K) * sizeof(uint32_t);
     };
-    // One CTA per row when there are enough rows to occupy the GPU and a row
-    // fits one CTA (no cluster exchange, no second selection); otherwise split
-    // each row over a cluster so that few, long rows still use many SMs.
     int C = 1;
-    if (a.rows < 16 || Lmax > kMaxKeysPerCta) {
-        while (C < kMaxCluster && a.rows * C * 2 <= sms) C *= 2;
-        while (C > 1 && chunk_for(C) < 1024) C /= 2;
-    }
+    while (C < kMaxCluster && a.rows * C * 2 <= sms) C *= 2;
+    while (C > 1 && chunk_for(C) < 1024) C /= 2;
     while (C < kMaxCluster && (chunk_for(C) > kMaxKeysPerCta || smem_for(C) > smem_cap)) C *= 2;
     if (chunk_for(C) > kMaxKeysPerCta || smem_for(C) > smem_cap) {
         set_error("topk: a row of %lld candidates with K=%d does not fit %d CTAs", (long long)Lmax, a.K, kMaxCluster);
