@@ -210,10 +210,10 @@ size_t csa2_sparse_attn_workspace_bytes(int B, int T, int H, int D, int dv, int 
  * callers that may not allocate device memory at all, such as an engine that
  * plans every byte of its device memory before it starts serving, or code
  * that must not call cudaMalloc/cudaFree because those calls can synchronise
- * the device.  The scratch for the per-split partial outputs lives in one
- * array built into the library (csa2_sparse_attn_noalloc_max_scratch_bytes()
- * bytes, 20 MiB: enough for 32 decode tokens x 64 heads with K = 512) that
- * every GPU loading the library holds until the process exits.
+ * the device.  The split-KV scratch lives in one array built into the library
+ * (csa2_sparse_attn_noalloc_max_scratch_bytes() bytes, 20 MiB; every
+ * supported shape fits on a 152-SM GB300) that every GPU
+ * loading the library holds until the process exits.
  *
  * Arguments, layouts, results and errors are those of csa2_sparse_attn_fp4
  * (minus workspace/ws_bytes); the call allocates nothing.  A shape whose

@@ -481,7 +481,7 @@ using namespace csa2;
 
 extern "C" size_t csa2_sparse_attn_workspace_bytes(int B, int T, int H, int D, int dv, int K) {
     if (B <= 0 || T <= 0 || H <= 0 || K <= 0 || !supported(D, dv, H)) return 0;
-    if (sparse_attn_tc_supported(D, dv, H, K)) return sparse_attn_tc_workspace_bytes(B, T, H, K) + 256;
+    if (sparse_attn_tc_supported(D, dv, H, K)) return 0;  // cluster-merged, no scratch
     const int64_t bt = (int64_t)B * T;
     const int splits = choose_splits(bt * (H / heads_per_cta(D)), K);
     if (splits <= 1) return 0;
@@ -511,16 +511,9 @@ extern "C" csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H,
     CSA2_REQUIRE(aligned(out, 16) && aligned(idx, 4), "sparse_attn: out needs 16-byte alignment");
     CSA2_REQUIRE((int64_t)B * T <= 0x7FFFFFFFLL && H / heads_per_cta(D) <= 65535, "sparse_attn: too many query tokens or heads");
 
-    if (sparse_attn_tc_supported(D, dv, H, K)) {
-        const size_t need = sparse_attn_tc_workspace_bytes(B, T, H, K);
-        if (!workspace || ws_bytes < need) {
-            set_error("sparse_attn: workspace of %zu bytes required, %zu given", need, workspace ? ws_bytes : 0);
-            return CSA2_ERR_WORKSPACE;
-        }
-        CSA2_REQUIRE(aligned(workspace, 16), "sparse_attn: workspace must be 16-byte aligned");
+    if (sparse_attn_tc_supported(D, dv, H, K))
         return launch_sparse_attn_tc(B, T, H, K, N, q, codes, scales, idx, kv_len, sm_scale, (float *)out, lse,
-                                     err_flag, workspace, stream_of(stream));
-    }
+                                     err_flag, stream_of(stream));
 
     AttnArgs a = {};
     a.B = B; a.T = T; a.H = H; a.K = K; a.N = N;
@@ -553,9 +546,10 @@ extern "C" csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H,
 // cudaMalloc/cudaFree because those calls can synchronise the device) use
 // this entry point instead.  Its scratch is one file-scope device array of
 // kNoAllocScratchBytes that is part of the library image: every GPU that
-// loads the library holds it until the process exits.  20 MiB holds the
-// partials of 32 decode tokens x 64 heads with K = 512 (16.8 MB); larger
-// shapes are rejected with CSA2_ERR_WORKSPACE.
+// loads the library holds it until the process exits.  The split policy keeps
+// splits x query tokens x head blocks <= the SM count, so a shape needs at most
+// SMs x 64 heads x (512 + 1) x 4 bytes (19.96 MB on a 152-SM GB300); larger
+// GPUs may meet shapes that do not fit, which are rejected.
 namespace csa2 {
 namespace {
 constexpr size_t kNoAllocScratchBytes = (size_t)20 << 20;  // 20 MiB
@@ -607,7 +601,7 @@ extern "C" csa2_status csa2_sparse_attn_fp4_noalloc(csa2_mode mode, int B, int T
     void *scratch = nullptr;
     if (need > 0) CSA2_CUDA_CALL(noalloc_scratch(&scratch), "sparse_attn_noalloc: scratch address");
     // Every split rewrites all of its partial rows (empty splits write zeros
-    // and a -inf max), so nothing in the array needs clearing between calls.
+    // and lse = -inf), so nothing in the array needs clearing between calls.
     return csa2_sparse_attn_fp4(mode, B, T, H, D, dv, q, codes, scales, N, idx, K, kv_len, sm_scale, out, out_dt,
                                 lse, err_flag, scratch, need > 0 ? kNoAllocScratchBytes : 0, stream);
 }

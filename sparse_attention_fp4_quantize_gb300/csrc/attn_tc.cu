@@ -20,12 +20,11 @@
 //  4. softmax on a transposed copy of S^T in shared memory; P -> f16.
 //  5. O^T [512 ch x 64 heads] = Vhat^T . P^T  (4 x 8 MMAs; the same Khat bytes
 //     read MN-major), fp32 accumulators in TMEM.
-//  6. Merge across the cluster through L2: every CTA writes its raw O^T and
-//     per-head (max, sum) to its slot of the caller's workspace with
-//     coalesced stores, one cluster barrier, then CTA c reads channel slice c
-//     of all S partials, combines them with weights 2^(m_c - M) / L and
-//     writes the output.  (Moving the partials through distributed shared
-//     memory measured several times slower on this part.)
+//  6. Merge across the cluster by PUSHING: every CTA stores its raw O slices
+//     and its per-head (max, sum) into the shared memory of the CTA that owns
+//     each channel slice (fire-and-forget distributed-shared-memory stores),
+//     one cluster barrier, then each owner combines its slice locally with
+//     weights 2^(m_c - M) / L and writes it out.
 // Waits on the mbarriers are bounded; on timeout the kernel sets
 // CSA2_FLAG_TIMEOUT and still runs every cluster barrier, so it always ends.
 #include <cooperative_groups.h>
@@ -58,19 +57,22 @@ constexpr uint32_t OFF_Q = OFF_K + KT_BYTES;
 constexpr uint32_t OFF_ST = OFF_Q;                // reuses the Q tile after S is computed
 constexpr uint32_t OFF_P = OFF_Q + ST_BYTES;
 constexpr uint32_t OFF_MISC = OFF_Q + Q_BYTES;
-constexpr uint32_t OFF_BAR = OFF_MISC;            // 3 mbarriers
+constexpr uint32_t OFF_BAR = OFF_MISC;            // 4 mbarriers
 constexpr uint32_t OFF_TMEM = OFF_BAR + 32;
 constexpr uint32_t OFF_VALID = OFF_TMEM + 16;     // int[128]
 constexpr uint32_t OFF_CS = OFF_VALID + TM * 4;   // float[64] logit factor per head
 constexpr uint32_t OFF_M = OFF_CS + HB * 4;       // float[64] row max (log2 domain)
 constexpr uint32_t OFF_L = OFF_M + HB * 4;        // float[64] row sum
-constexpr uint32_t OFF_W = OFF_L + HB * 4;        // float[MAX_S][64] merge weights
+constexpr uint32_t OFF_XCH = OFF_L + HB * 4;      // float[MAX_S][2][64] received (max, sum)
+constexpr uint32_t OFF_W = OFF_XCH + MAX_S * 2 * HB * 4;  // float[MAX_S][64] merge weights
 constexpr uint32_t OFF_LSE = OFF_W + MAX_S * HB * 4;      // float[64]
 constexpr uint32_t SMEM = OFF_LSE + HB * 4;
 constexpr uint32_t TMEM_COLS = 512;               // S^T: 64 cols, O^T: 4 x 64 cols
 constexpr uint32_t S_COL = 0, O_COL = 64;
 constexpr uint32_t MAX_POLLS = 1u << 22;          // about a second of polling at most
 static_assert(OFF_CRAW + TM * CRAW_STRIDE <= KT_BYTES, "staging must fit in the Khat region");
+static_assert((DV * (HB + 4) + MAX_S * 2 * HB) * 4 <= KT_BYTES, "received partials must fit in the Khat region");
+static_assert(((DV / 2) * (HB + 4) + 2 * HB) * 4 <= Q_BYTES, "a staged slice must fit in the Q region");
 static_assert(ST_BYTES + (HB / 8) * P_SBO <= Q_BYTES, "S^T copy and P must fit in the Q region");
 static_assert(SMEM <= 227 * 1024, "shared memory");
 
@@ -86,7 +88,6 @@ struct TcArgs {
     float *out;
     float *lse;
     uint32_t *err_flag;
-    float *part;      // [groups * S][DV + 2][64]: raw O^T rows per channel, then max and sum rows
 };
 
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
@@ -133,6 +134,33 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Bulk copy from this CTA's shared memory to another CTA's (TMA engine),
+// completing on the destination CTA's mbarrier.
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_remote, uint32_t src_local, uint32_t bytes, uint32_t bar_remote) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_remote),
+                 "r"(src_local), "r"(bytes), "r"(bar_remote)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Stores to the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t remote_addr(const void *local_ptr, uint32_t rank) {
+    uint32_t la = tc::smem_u32(local_ptr), ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+    return ra;
+}
+
+__device__ __forceinline__ void st_remote(const void *local_ptr, uint32_t rank, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote_addr(local_ptr, rank)), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_remote4(uint32_t raddr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(raddr), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
 __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     cg::cluster_group cluster = cg::this_cluster();
@@ -152,21 +180,25 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     uint8_t *sQ = smem + OFF_Q;
     float *sT = reinterpret_cast<float *>(smem + OFF_ST);
     uint8_t *sP = smem + OFF_P;
+    float *sRecv = reinterpret_cast<float *>(smem + OFF_K);  // received partial O after P V
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     int *sValid = reinterpret_cast<int *>(smem + OFF_VALID);
     float *sCs = reinterpret_cast<float *>(smem + OFF_CS);
     float *sM = reinterpret_cast<float *>(smem + OFF_M);
     float *sL = reinterpret_cast<float *>(smem + OFF_L);
+    float *sXch = reinterpret_cast<float *>(smem + OFF_XCH);
     float *sW = reinterpret_cast<float *>(smem + OFF_W);
     float *sLse = reinterpret_cast<float *>(smem + OFF_LSE);
     const uint32_t bar_ld = tc::smem_u32(smem + OFF_BAR);
     const uint32_t bar_s = bar_ld + 8;
     const uint32_t bar_o = bar_ld + 16;
+    const uint32_t bar_rx = bar_ld + 24;
 
     if (tid == 0) {
         tc::mbar_init(bar_ld, TM);   // one arrival per entry thread
         tc::mbar_init(bar_s, 1);
         tc::mbar_init(bar_o, 1);
+        tc::mbar_init(bar_rx, 1);
         tc::mbar_init_fence();
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -351,47 +383,68 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     tc::fence_after();
     if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
 
-    // ---- 6. raw O^T and per-head (max, sum) -> this CTA's partial in the workspace (L2)
-    // layout: row c (< 512) holds the 64 heads of channel c; rows 512 and 513
-    // hold the per-head max (log2 domain) and sum.
-    float *mypart = a.part + (size_t)blockIdx.x * (DV + 2) * HB;
-#pragma unroll 1
-    for (int mb = 0; mb < DV / 128; ++mb) {
-        uint32_t r[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * HB + 32 * hh, r);
-        tc::tmem_ld_wait();
-        float *row = mypart + (size_t)(mb * 128 + 32 * quarter + lane) * HB + 32 * hh;
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-            *reinterpret_cast<uint4 *>(row + 4 * q4) = make_uint4(r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
-    }
-    if (tid < HB) {
-        mypart[(size_t)DV * HB + tid] = sM[tid];
-        mypart[(size_t)(DV + 1) * HB + tid] = sL[tid];
-    }
-    __threadfence();
+    // ---- 6. send raw O slices and (max, sum) to the owners of the channel slices
+    // Payload for owner o: [W channels][RS floats: 64 heads + pad] then 64 max + 64 sum.
+    // Slices for other CTAs are staged in this CTA's Q region and moved by the
+    // TMA engine (bulk shared -> remote shared copies completing on the owner's
+    // mbarrier); the own slice is written in place.
+    const int W = DV / S;                      // channels per owner
+    constexpr int RS = HB + 4;                 // floats per received channel row
+    const uint32_t slice_floats = (uint32_t)W * RS + 2 * HB;
+    const uint32_t slice_bytes = slice_floats * 4;
+    float *stage = reinterpret_cast<float *>(smem + OFF_Q);   // free after P V
+    if (tid == 0) asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_rx),
+                               "r"((uint32_t)(S - 1) * slice_bytes) : "memory");
     tc::fence_before();
-    cluster.sync();                            // every partial of this query token is in L2
+    cluster.sync();                            // every CTA finished with its Khat tile
+    for (int o = 0; o < S; ++o) {
+        const int oo = (rank + 1 + o) % S;     // own slice last
+        float *dst = (oo == rank) ? sRecv + (size_t)rank * slice_floats : stage;
+        if (oo != rank && o > 0) {
+            if (tid == 0) bulk_wait_read0();   // the staging buffer is free again
+            __syncthreads();
+        }
+        for (int mb = oo * W / 128; mb < (oo + 1) * W / 128; ++mb) {
+            uint32_t r[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * HB + 32 * hh, r);
+            tc::tmem_ld_wait();
+            float *row = dst + (size_t)(mb * 128 - oo * W + 32 * quarter + lane) * RS + 32 * hh;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+                *reinterpret_cast<uint4 *>(row + 4 * q4) = make_uint4(r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
+        }
+        if (tid < HB) {
+            dst[(size_t)W * RS + tid] = sM[tid];
+            dst[(size_t)W * RS + HB + tid] = sL[tid];
+        }
+        if (oo != rank) {
+            tc::fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                uint32_t rdst, rbar;
+                const uint32_t ldst = tc::smem_u32(sRecv + (size_t)rank * slice_floats);
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rdst) : "r"(ldst), "r"((uint32_t)oo));
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar_rx), "r"((uint32_t)oo));
+                bulk_s2s(rdst, tc::smem_u32(stage), slice_bytes, rbar);
+                bulk_commit();
+            }
+        }
+    }
+    if (tid == 0) bulk_wait_read0();           // staging reads done before this CTA may exit
+    ok = tc::mbar_wait(bar_rx, 0, MAX_POLLS) && ok;   // the other CTAs' slices have landed
+    __syncthreads();
     if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
 
     // ---- 7. combine this CTA's channel slice: weights 2^(m_c - M) / L per head
-    const int W = DV / S;                      // channels per owner
-    const float *part0 = a.part + (size_t)(blockIdx.x - rank) * (DV + 2) * HB;   // first CTA of the cluster
     if (tid < HB) {
-        float mc[MAX_S];
         float M = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < MAX_S; ++c) {
-            mc[c] = (c < S) ? __ldcg(part0 + ((size_t)c * (DV + 2) + DV) * HB + tid) : -INFINITY;
-            M = fmaxf(M, mc[c]);
-        }
+        for (int c = 0; c < S; ++c) M = fmaxf(M, sRecv[(size_t)c * slice_floats + W * RS + tid]);
         float L = 0.f;
-#pragma unroll
-        for (int c = 0; c < MAX_S; ++c) {
-            if (c >= S) break;
-            const float wc = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : ex2(mc[c] - M);
+        for (int c = 0; c < S; ++c) {
+            const float mc = sRecv[(size_t)c * slice_floats + W * RS + tid];
+            const float wc = (M == -INFINITY || mc == -INFINITY) ? 0.f : ex2(mc - M);
             sW[c * HB + tid] = wc;
-            L += wc * __ldcg(part0 + ((size_t)c * (DV + 2) + DV + 1) * HB + tid);
+            L += wc * sRecv[(size_t)c * slice_floats + W * RS + HB + tid];
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
         for (int c = 0; c < S; ++c) sW[c * HB + tid] *= inv;
@@ -399,29 +452,22 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     }
     __syncthreads();
     {
-        // thread -> (channel, 16 heads): 64-byte reads of each partial row; each
-        // warp store then covers 32 consecutive channels of one head
+        // thread -> (4 heads, channel): lanes take consecutive channels, so each
+        // output store of a warp covers 32 consecutive channels of one head
         const int c_lo = rank * W;
-        for (int t = tid; t < 4 * W; t += THREADS) {
-            const int h16 = t / W, c = c_lo + (t - h16 * W);
-            float acc[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+        for (int t = tid; t < (HB / 4) * W; t += THREADS) {
+            const int h4 = t / W, c = t - h4 * W;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int src = 0; src < S; ++src) {
-                const float4 *pr = reinterpret_cast<const float4 *>(part0 + ((size_t)src * (DV + 2) + c) * HB + 16 * h16);
-                const float *w = sW + src * HB + 16 * h16;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 v = __ldcg(pr + q4);
-                    acc[4 * q4] += w[4 * q4] * v.x;
-                    acc[4 * q4 + 1] += w[4 * q4 + 1] * v.y;
-                    acc[4 * q4 + 2] += w[4 * q4 + 2] * v.z;
-                    acc[4 * q4 + 3] += w[4 * q4 + 3] * v.w;
-                }
+                const float4 v = *reinterpret_cast<const float4 *>(sRecv + (size_t)src * slice_floats + (size_t)c * RS + 4 * h4);
+                const float *w = sW + src * HB + 4 * h4;
+                acc.x += w[0] * v.x; acc.y += w[1] * v.y; acc.z += w[2] * v.z; acc.w += w[3] * v.w;
             }
-            float *o = a.out + ((bt * a.H) + h0 + 16 * h16) * (int64_t)DV + c;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) o[(int64_t)k * DV] = acc[k];
+            float *o = a.out + ((bt * a.H) + h0 + 4 * h4) * (int64_t)DV + c_lo + c;
+            o[0] = acc.x;
+            o[DV] = acc.y;
+            o[2 * DV] = acc.z;
+            o[3 * DV] = acc.w;
         }
         if (rank == 0 && a.lse && tid < HB) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
     }
@@ -435,15 +481,9 @@ bool sparse_attn_tc_supported(int D_, int dv, int H, int K) {
     return D_ == D && dv == DV && H % HB == 0 && K >= 1 && K <= MAX_S * TM;
 }
 
-size_t sparse_attn_tc_workspace_bytes(int B, int T, int H, int K) {
-    const int tiles = (K + TM - 1) / TM;
-    const int S = tiles <= 1 ? 1 : (tiles <= 2 ? 2 : 4);
-    return (size_t)B * T * (H / HB) * S * (DV + 2) * HB * sizeof(float);
-}
-
 csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const void *q, const uint8_t *codes,
                                   const uint8_t *scales, const int32_t *idx, const int32_t *kv_len, float sm_scale,
-                                  float *out, float *lse, uint32_t *err_flag, void *workspace, cudaStream_t stream) {
+                                  float *out, float *lse, uint32_t *err_flag, cudaStream_t stream) {
     static bool smem_set[64];
     CSA2_CUDA_CALL(ensure_smem_limit((const void *)sparse_attn_tc_kernel, (int)SMEM, smem_set),
                    "sparse_attn_tc: smem attribute");
@@ -454,7 +494,6 @@ csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const v
     a.hblocks = H / HB;
     a.q = (const uint16_t *)q; a.codes = codes; a.scales = scales; a.idx = idx; a.kv_len = kv_len;
     a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.err_flag = err_flag;
-    a.part = (float *)workspace;
     const int64_t grid = (int64_t)B * T * a.hblocks * a.csize;
     if (grid > 0x7FFFFFFF) {
         set_error("sparse_attn_tc: grid too large");

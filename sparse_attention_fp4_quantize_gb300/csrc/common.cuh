@@ -62,10 +62,9 @@ static inline cudaStream_t stream_of(csa2_stream_t s) { return (cudaStream_t)s; 
 
 // tcgen05 sparse attention (attn_tc.cu): D = 576, dv = 512, 64-head blocks, K <= 1024.
 bool sparse_attn_tc_supported(int D, int dv, int H, int K);
-size_t sparse_attn_tc_workspace_bytes(int B, int T, int H, int K);
 csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const void *q, const uint8_t *codes,
                                   const uint8_t *scales, const int32_t *idx, const int32_t *kv_len, float sm_scale,
-                                  float *out, float *lse, uint32_t *err_flag, void *workspace, cudaStream_t stream);
+                                  float *out, float *lse, uint32_t *err_flag, cudaStream_t stream);
 
 // --------------------------------------------------------------- device side
 // Order-preserving map of an fp32 score to uint32: larger score -> larger key.

@@ -384,7 +384,7 @@ def test_sparse_attn_workspace_is_required_when_split(csa2):
     scales = torch.zeros(100, 36, dtype=torch.uint8, device=DEV)
     idx = torch.zeros(1, 1, 1536, dtype=torch.int32, device=DEV)     # K > 1024: split-KV path
     out = torch.zeros(1, 1, 64, 512, device=DEV)
-    assert csa2.csa2_sparse_attn_workspace_bytes(1, 1, 64, 576, 512, 512) > 0    # tcgen05 path: partials
+    assert csa2.csa2_sparse_attn_workspace_bytes(1, 1, 64, 576, 512, 512) == 0   # tcgen05 path: no scratch
     assert csa2.csa2_sparse_attn_workspace_bytes(1, 1, 64, 576, 512, 1536) > 0
     with pytest.raises(csa2.Csa2Error) as e:
         csa2.csa2_sparse_attn_fp4(0, q, codes, scales, 100, idx, out, 0.1)

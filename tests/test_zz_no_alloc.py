@@ -6,8 +6,8 @@ cudaFree because they can synchronise the device).  For them the library
 offers a variant of the sparse attention whose split-KV scratch is an array
 built into the library.  This file checks, through the C ABI, that the variant
 gives the same output as the regular entry point (within the attention
-tolerance of the other tests) on calls in a row with different inputs, and
-that a shape needing more scratch than the array holds is rejected.
+tolerance of the other tests) on two calls in a row with different inputs, and
+that the array covers every supported shape on this GPU.
 
 It is collected last on purpose, and it needs no other test to have run.
 Marked gpu.
@@ -43,10 +43,9 @@ def _rel_err(a, b):
     return float((num / den).max())
 
 
-# shapes that need scratch: 576-channel entries (tensor-core path, partials
-# merged through the scratch), 128-channel entries and K > 512 (split path)
-CASES = [(11, 32, 3000, 512, 64, 576), (12, 3, 5000, 512, 32, 128), (13, 2, 4000, 1536, 64, 576),
-         (14, 8, 3000, 512, 16, 128)]
+# shapes that take the split-KV path (and so need scratch): 128-channel
+# entries, and 576-channel entries with more than 1024 selected
+CASES = [(11, 8, 3000, 512, 16, 128), (12, 3, 5000, 512, 32, 128), (13, 2, 4000, 1536, 64, 576)]
 
 
 def test_noalloc_matches_workspace_entry_point_twice():
@@ -75,20 +74,14 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert torch.allclose(lse, ref_lse, rtol=1e-5, atol=1e-5)
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch():
-    """64 decode tokens x 64 heads with K = 512 need 33.7 MB of partials: more
-    than the built-in array holds, so the call is refused before any launch."""
+def test_noalloc_scratch_covers_every_shape_on_this_gpu():
+    """The split policy keeps splits x tokens x head blocks <= the SM count, so
+    no supported shape needs more than SMs x 64 x 513 x 4 bytes (+256)."""
     import sparse_attention_fp4_quantize_gb300 as csa2
-    B = 64
-    need = csa2.csa2_sparse_attn_workspace_bytes(B, 1, 64, 576, 512, 512)
-    assert need > csa2.noalloc_max_scratch_bytes()
-    q = torch.zeros(B, 1, 64, 576, dtype=torch.int16, device=DEV)
-    codes = torch.zeros(100, 288, dtype=torch.uint8, device=DEV)
-    scales = torch.zeros(100, 36, dtype=torch.uint8, device=DEV)
-    idx = torch.zeros(B, 1, 512, dtype=torch.int32, device=DEV)
-    out = torch.full((B, 1, 64, 512), 5.0, device=DEV)
-    with pytest.raises(csa2.Csa2Error) as e:
-        csa2.csa2_sparse_attn_fp4_noalloc(0, q, codes, scales, 100, idx, out, 0.1)
-    assert e.value.status == 3 and "built-in array" in str(e.value)
-    torch.cuda.synchronize()
-    assert (out == 5.0).all()          # outputs untouched
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    worst = sms * 64 * 513 * 4 + 256
+    if worst > csa2.noalloc_max_scratch_bytes():
+        pytest.skip("larger GPU: some shapes are rejected by design")
+    for B, H, D, K in [(1, 64, 576, 2048), (2, 128, 576, 1100), (1, 16, 128, 512), (9, 64 * 16, 576, 2048),
+                       (1, 16 * 150, 128, 2048)]:
+        assert csa2.csa2_sparse_attn_workspace_bytes(B, 1, H, D, D - 64, K) <= csa2.noalloc_max_scratch_bytes()
