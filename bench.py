@@ -236,6 +236,108 @@ def _traffic_record(kernel):
     return rec.get("dram_bytes_per_launch")
 
 
+def _time_graph(fn, stream, reps, warm=3):
+    """Capture fn() as a CUDA graph on `stream`, replay it `warm` times, then
+    time `reps` replays with events; seconds per replay."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e-3 / reps
+
+
+def _extra_workloads(dev, stream, peak_gbs):
+    """The other synthetic workloads, each timed on the device: the 1M-row FP4
+    append, the 4096-query prefill scoring, the Reindex + 3 Reuse group at 1M
+    context, the pool build, and the tiny Full-layer chain."""
+    import torch
+    import gen
+    import sparse_attention_fp4_quantize_gb300 as csa2
+    res = {}
+    # append: quantise 1,048,576 x 576 rows (two output sets alternate; the 1.2 GB input exceeds L2)
+    w5 = gen.APPEND_POOL
+    R = w5.B * w5.N
+    rows = gen.kv_rows(w5.seed, 10, R, 576, rms=False, device=dev)
+    outs = [(torch.empty(R, 288, dtype=torch.uint8, device=dev), torch.empty(R, 36, dtype=torch.uint8, device=dev))
+            for _ in range(2)]
+    t = _time_graph(lambda: [csa2.csa2_quantize_kv_fp4(rows, c, s_, stream=stream) for c, s_ in outs], stream, 20) / 2
+    qbytes = R * 576 * 2 + R * (288 + 36)
+    res["append_quantize_1m_rows"] = {"us": t * 1e6, "bytes": qbytes, "gbs": qbytes / t / 1e9,
+                                     "hbm_frac": qbytes / t / 1e9 / peak_gbs}
+    del rows, outs
+    # pool for 16 x 65536 entries from Full scores
+    q5, w5w, k5 = gen.indexer_inputs(w5, device=dev)
+    kl5 = gen.kv_lengths(w5).to(dev)
+    sc5 = torch.empty(w5.B, 1, w5.N, device=dev)
+    csa2.csa2_index_score(0, q5, w5w, k5, kl5, sc5, stream=stream)
+    pool5 = torch.empty(w5.B, 1, 2048, dtype=torch.int32, device=dev)
+    t = _time_graph(lambda: csa2.csa2_build_pool(sc5, kl5, pool5, stream=stream), stream, 50)
+    res["pool_build_b16_n65536"] = {"us": t * 1e6, "score_bytes_read": w5.B * w5.N * 4}
+    t = _time_graph(lambda: csa2.csa2_index_score(0, q5, w5w, k5, kl5, sc5, stream=stream), stream, 20)
+    res["full_score_b16_n65536"] = {"us": t * 1e6, "key_gbs": w5.B * w5.N * 64 / t / 1e9,
+                                    "hbm_frac": w5.B * w5.N * 68 / t / 1e9 / peak_gbs}
+    del q5, w5w, k5, sc5
+    # prefill: 4096 causal queries x 32768 keys (FP8), scores materialised
+    w4 = gen.PREFILL_CHUNK
+    q4, ww4, k4 = gen.indexer_inputs(w4, device=dev)
+    kl4 = gen.kv_lengths(w4).to(dev)
+    sc4 = torch.empty(1, w4.T, w4.N, device=dev)
+    t = _time_graph(lambda: csa2.csa2_index_score(0, q4, ww4, k4, kl4, sc4, stream=stream), stream, 5)
+    flops = 2.0 * w4.T * 4 * 64 * w4.N
+    res["prefill_score_t4096_n32768"] = {"us": t * 1e6, "tflops": flops / t / 1e12,
+                                         "score_write_gbs": w4.T * w4.N * 4 / t / 1e9}
+    idx4 = torch.empty(1, w4.T, 512, dtype=torch.int32, device=dev)
+    t = _time_graph(lambda: csa2.csa2_topk(0, sc4, idx4, kv_len=kl4, stream=stream), stream, 5)
+    res["prefill_topk_t4096_n32768"] = {"us": t * 1e6, "score_read_gbs": w4.T * w4.N * 4 / t / 1e9}
+    del q4, ww4, k4, sc4, idx4
+    # Reindex + 3 Reuse group at 1M context, B = 8, each layer over its own FP4 KV
+    w3 = gen.REINDEX_REUSE_1M
+    q0, w0, k3 = gen.indexer_inputs(w3, layer=0, device=dev)
+    q1, w1, _ = gen.indexer_inputs(w3, layer=1, device=dev)
+    kl3 = gen.kv_lengths(w3).to(dev)
+    full3 = torch.empty(w3.B, 1, w3.N, device=dev)
+    csa2.csa2_index_score(0, q0, w0, k3, kl3, full3, stream=stream)
+    pool3 = torch.empty(w3.B, 1, 2048, dtype=torch.int32, device=dev)
+    csa2.csa2_build_pool(full3, kl3, pool3, stream=stream)
+    rs3 = torch.empty(w3.B, 1, 16384, device=dev)
+    idx3 = torch.empty(w3.B, 1, 512, dtype=torch.int32, device=dev)
+    planes = [gen.fp4_planes(w3.seed, 40 + l, w3.B * w3.N, 576, device=dev) for l in range(4)]
+    qs = [gen.normal_bf16(w3.seed, 200 + l, (w3.B, 1, 64, 576), device=dev) for l in range(4)]
+    outs3 = [torch.empty(w3.B, 1, 64, 512, device=dev) for _ in range(4)]
+    ws3 = csa2.workspace_for_attn(w3.B, 1, 64, 576, 512, 512, device=dev)
+
+    def group():
+        csa2.csa2_index_score(1, q1, w1, k3, kl3, rs3, pool_blocks=pool3, stream=stream)
+        csa2.csa2_topk(1, rs3, idx3, pool_blocks=pool3, stream=stream)
+        for l in range(4):
+            csa2.csa2_sparse_attn_fp4(1 if l == 0 else 2, qs[l], planes[l][0], planes[l][1], w3.N, idx3, outs3[l],
+                                      1 / 24.0, kv_len=kl3, workspace=ws3, stream=stream)
+    t = _time_graph(group, stream, 50)
+    gbytes = w3.B * 16384 * 64 + 4 * w3.B * 512 * 324 + 4 * w3.B * 64 * 512 * 4
+    res["reindex_reuse_group_b8_1m"] = {"us": t * 1e6, "token_layers_per_s": w3.B * 4 / t,
+                                        "algorithmic_bytes": gbytes, "gbs": gbytes / t / 1e9}
+    t = _time_graph(lambda: csa2.csa2_build_pool(full3, kl3, pool3, stream=stream), stream, 50)
+    res["pool_build_b8_n262144"] = {"us": t * 1e6, "score_bytes_read": w3.B * w3.N * 4}
+    del planes, qs, outs3, k3, full3
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args):
     import torch
     world, rank, local = _dist()
@@ -360,6 +462,10 @@ def run_gpu(args):
             "avg_launch_us": dom[1]["avg_s"] * 1e6}
     path_bytes = alg["keys"] + alg["gathered"] + alg["outputs"]
 
+    extras = None
+    if not args.no_extras:
+        extras = _extra_workloads(dev, stream, peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(budget_s=args.cpu_budget)
@@ -383,6 +489,7 @@ def run_gpu(args):
         "clocks": clocks.summary(t0, t1),
         "device_error_flags": errs,
         "cpu_baseline": cpu,
+        "workloads": extras,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -504,6 +611,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' timings")
     ap.add_argument("--profile-case", action="store_true", help="3 eager steps on one input set (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:

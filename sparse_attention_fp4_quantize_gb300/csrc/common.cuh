@@ -66,6 +66,12 @@ csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const v
                                   const uint8_t *scales, const int32_t *idx, const int32_t *kv_len, float sm_scale,
                                   float *out, float *lse, uint32_t *err_flag, cudaStream_t stream);
 
+// tcgen05 prefill scoring (index_score_tc.cu): FP8, Full mode, T >= 64.
+bool index_score_prefill_tc_supported(int T, csa2_dtype dt);
+csa2_status launch_index_score_prefill_tc(int B, int T, int64_t N, const void *q, const float *w, const void *k,
+                                          const int32_t *kv_len, float *scores, uint32_t *err_flag,
+                                          cudaStream_t stream);
+
 // --------------------------------------------------------------- device side
 // Order-preserving map of an fp32 score to uint32: larger score -> larger key.
 // -inf (and NaN bit patterns that would sort below it) map to 0, the

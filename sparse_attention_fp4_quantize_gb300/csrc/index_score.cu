@@ -331,6 +331,8 @@ extern "C" csa2_status csa2_index_score(csa2_mode mode, int B, int T, int64_t N,
     int64_t want = (a.tasks + (kThreads / 32) - 1) / (kThreads / 32);
     int64_t cap = (int64_t)num_sms() * 8;
     int blocks = (int)(want < cap ? want : cap);
+    if (mode == CSA2_MODE_FULL && index_score_prefill_tc_supported(T, q_dt))
+        return launch_index_score_prefill_tc(B, T, N, q_idx, w, k_idx, kv_len, scores, err_flag, stream_of(stream));
     const bool decode = (mode == CSA2_MODE_REINDEX) || T == 1;
     if (decode) {
         const int ch = (q_dt == CSA2_FP8_E4M3) ? 8 : 4;
