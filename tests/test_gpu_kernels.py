@@ -176,7 +176,8 @@ def test_index_score_tiny_bf16(csa2):
     check_scores(_score_gpu(csa2, 0, q, wt, k, kl), ref, mag)
 
 
-@pytest.mark.parametrize("B,T,N", [(3, 1, 1000), (2, 5, 777), (1, 2, 16), (4, 1, 1)])
+@pytest.mark.parametrize("B,T,N", [(3, 1, 1000), (2, 5, 777), (1, 2, 16), (4, 1, 1),
+                                   (2, 100, 1000), (1, 64, 130), (3, 200, 4100)])   # T >= 64: tensor-core path
 def test_index_score_full_ragged_fp8(csa2, B, T, N):
     q = gen.normal_e4m3(9, 1, (B, T, 4, 64))
     k = gen.normal_e4m3(9, 2, (B, N, 64))
