@@ -145,6 +145,7 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_remote, uint32_t src_local
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
 __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -178,6 +179,12 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     const uint32_t bar_o = bar_ld + 16;
     const uint32_t bar_rx = bar_ld + 24;
 
+    // the selected entry of this thread: its index load overlaps the set-up below
+    const int e = tid & (TM - 1);   // entry of this thread in the tile
+    const int half = tid >> 7;      // which 288 channels of the entry
+    const int sel = rank * TM + e;
+    const int64_t j = (sel < a.K) ? (int64_t)__ldg(a.idx + bt * a.K + sel) : -1;
+
     if (tid == 0) {
         tc::mbar_init(bar_ld, TM);   // one arrival per entry thread
         tc::mbar_init(bar_s, 1);
@@ -189,28 +196,24 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     __syncthreads();
 
     // ---- 1. gather: TMA bulk copies of Q rows and the selected code rows
-    const int e = tid & (TM - 1);   // entry of this thread in the tile
-    const int half = tid >> 7;      // which 288 channels of the entry
-    const int sel = rank * TM + e;
-    int64_t j = (sel < a.K) ? (int64_t)__ldg(a.idx + bt * a.K + sel) : -1;
+    if (half == 0 && e < HB) {      // Q rows do not depend on the indices: first
+        const uint16_t *qrow = a.q + ((bt * a.H) + h0 + e) * (int64_t)D;
+        mbar_expect_tx(bar_ld, D * 2);
+        bulk_g2s(tc::smem_u32(smem + OFF_QRAW + e * QRAW_STRIDE), qrow, D * 2, bar_ld);
+    }
     const bool valid = j >= 0 && j < len;
-    uint32_t sw[5];
+    if (half == 0) {
+        if (!valid && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
+        sValid[e] = valid ? 1 : 0;
+        mbar_arrive_expect_tx(bar_ld, valid ? D / 2 : 0);
+        if (valid)
+            bulk_g2s(tc::smem_u32(smem + OFF_CRAW + e * CRAW_STRIDE), a.codes + (b * a.N + j) * (D / 2), D / 2, bar_ld);
+    }
+    uint32_t sw[5];                 // scale words: plain loads, consumed by the dequantiser
     if (valid) {
         const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + (b * a.N + j) * (D / 16)) + 4 * half;
 #pragma unroll
         for (int i = 0; i < 5; ++i) sw[i] = __ldg(srow + i);
-    }
-    if (half == 0) {
-        if (!valid && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
-        sValid[e] = valid ? 1 : 0;
-        if (e < HB) {
-            const uint16_t *qrow = a.q + ((bt * a.H) + h0 + e) * (int64_t)D;
-            mbar_expect_tx(bar_ld, D * 2);
-            bulk_g2s(tc::smem_u32(smem + OFF_QRAW + e * QRAW_STRIDE), qrow, D * 2, bar_ld);
-        }
-        mbar_arrive_expect_tx(bar_ld, valid ? D / 2 : 0);
-        if (valid)
-            bulk_g2s(tc::smem_u32(smem + OFF_CRAW + e * CRAW_STRIDE), a.codes + (b * a.N + j) * (D / 2), D / 2, bar_ld);
     }
     bool ok = tc::mbar_wait(bar_ld, 0, MAX_POLLS);
 
@@ -377,15 +380,20 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     const uint32_t slice_floats = (uint32_t)W * RS + 2 * HB;
     const uint32_t slice_bytes = slice_floats * 4;
     float *stage = reinterpret_cast<float *>(smem + OFF_Q);   // free after P V
+    const int nbuf = (2 * slice_bytes <= Q_BYTES) ? 2 : 1;    // staging buffers (2 when S = 4)
+    int sent = 0;
     if (tid == 0) asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_rx),
                                "r"((uint32_t)(S - 1) * slice_bytes) : "memory");
     tc::fence_before();
     cluster.sync();                            // every CTA finished with its Khat tile
     for (int o = 0; o < S; ++o) {
         const int oo = (rank + 1 + o) % S;     // own slice last
-        float *dst = (oo == rank) ? sRecv + (size_t)rank * slice_floats : stage;
-        if (oo != rank && o > 0) {
-            if (tid == 0) bulk_wait_read0();   // the staging buffer is free again
+        float *dst = (oo == rank) ? sRecv + (size_t)rank * slice_floats : stage + (size_t)(sent % nbuf) * slice_floats;
+        if (oo != rank && sent >= nbuf) {
+            if (tid == 0) {                    // this staging buffer's previous copy has read it
+                if (nbuf == 2) bulk_wait_read1();
+                else bulk_wait_read0();
+            }
             __syncthreads();
         }
         for (int mb = oo * W / 128; mb < (oo + 1) * W / 128; ++mb) {
@@ -409,9 +417,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
                 const uint32_t ldst = tc::smem_u32(sRecv + (size_t)rank * slice_floats);
                 asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rdst) : "r"(ldst), "r"((uint32_t)oo));
                 asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar_rx), "r"((uint32_t)oo));
-                bulk_s2s(rdst, tc::smem_u32(stage), slice_bytes, rbar);
+                bulk_s2s(rdst, tc::smem_u32(dst), slice_bytes, rbar);
                 bulk_commit();
             }
+            ++sent;
         }
     }
     if (tid == 0) bulk_wait_read0();           // staging reads done before this CTA may exit
