@@ -5,16 +5,22 @@
 // "552B参数干掉1.6T：DeepSeek V4.1 Flash技术深度解析", DeepSelect paragraph (the
 // Top-K kernel of the sparse attention).
 //
-// Design.  Decode rows are few and long (32 x 16384 scores, 8 x 32768 block
-// maxima), so one row is split over a thread-block cluster of C CTAs.  Each
-// CTA loads its slice of the row ONCE from HBM into shared memory as
-// order-preserving uint32 keys and selects the slice's own Top-K with four
-// 8-bit radix passes that need only CTA barriers.  Ranked by (score desc,
-// position asc), every member of the row's Top-K is in its slice's Top-K, so
-// CTA 0 then gathers the C candidate lists through distributed shared memory
-// (one cluster exchange) and runs the same selection on them.  Ties at the
-// K-th value go to the lowest positions.  Only hardware barriers are used:
-// no flag spinning.
+// Design.  A row is split over a thread-block cluster of C CTAs (C = 1, 2, 4
+// or 8).  Each CTA reads its slice of the row from HBM once and keeps it in
+// shared memory as order-preserving uint32 keys.  The K-th largest key of the
+// row is then found by a radix select over the whole cluster: for each digit
+// (bits 31..21, 20..10, 9..0) every CTA histograms its slice into 2048 fine
+// and 64 coarse bins, one cluster barrier publishes the histograms, and every
+// warp of every CTA locates the boundary bin itself by reading the cluster's
+// coarse bins and then the 32 fine bins of the boundary coarse bin through
+// distributed shared memory, so nothing waits for another CTA's answer.  A
+// digit ends the search early when the boundary bin is taken whole (random
+// float scores need two digits).  The selection is then compacted in
+// position order across the cluster: every warp publishes its counts above
+// and at the threshold, one more barrier lets each warp sum the counts before
+// it, and each CTA writes its own ids straight to the output.  Ties at the
+// K-th value go to the lowest positions.  Only hardware barriers are used: no
+// flag spinning.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -26,8 +32,15 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 2048;    // widest digit: 11 bits
+constexpr int kCoarse = 64;    // coarse bin = 32 fine bins
+constexpr int kDigits = 3;     // bits 31..21, 20..10, 9..0
 constexpr int kMaxCluster = 8;
-constexpr int kMaxKeysPerCta = 32768;  // 128 KB of keys
+constexpr int kMaxKeysPerCta = 49152;  // 192 KB of keys
+constexpr int kSmemCap = 198 * 1024;   // dynamic shared memory ceiling (static use is ~26 KB)
+static_assert(kBins == 4 * kThreads, "each thread owns one uint4 of fine bins");
+static_assert(kCoarse == kThreads / 8, "eight threads make one coarse bin");
+static_assert(kWarps <= 32, "one lane per warp in the count exchange");
 
 enum Loader { LOAD_SCORES = 0, LOAD_REINDEX = 1, LOAD_BLOCKMAX = 2 };
 
@@ -41,189 +54,101 @@ struct TopkArgs {
     int P;
     int K;
     int32_t *out;            // [rows, K]
-    int chunk;               // keys per CTA
-    int csize;               // CTAs per row (cluster size)
-    int region;              // words of the key region (>= chunk, >= 2*C*K when C > 1)
+    int chunk;               // keys per CTA (multiple of 4)
 };
-
-__device__ __forceinline__ int64_t row_len(const TopkArgs &a, int64_t row) {
-    if (a.loader == LOAD_REINDEX) return a.M;
-    int64_t len = a.kv_len ? (int64_t)a.kv_len[row] : a.M;
-    len = len < a.M ? len : a.M;
-    len = len > 0 ? len : 0;
-    if (a.loader == LOAD_BLOCKMAX) return (len + 7) / 8;
-    return len;
-}
-
-// Radix select over keys[0, n) in shared memory: T = the K-th largest key and
-// kk = how many keys equal to T are taken (every key > T is taken).  With
-// fewer than K keys, or when the K-th largest is the invalid key 0, the result
-// is T = 0, kk = 0: take every valid key.
-__device__ void block_select(const uint32_t *keys, int n, int K, uint32_t *hist, uint32_t *wsum, uint32_t *bc,
-                             uint32_t &T_out, uint32_t &kk_out) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (n < K) {
-        T_out = 0;
-        kk_out = 0;
-        return;
-    }
-    uint32_t prefix = 0, pmask = 0, kk = (uint32_t)K;
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        if (tid < 256) hist[tid] = 0;
-        __syncthreads();
-        for (int base = 0; base < n; base += kThreads) {
-            const int i = base + tid;
-            uint32_t d = 0x100;  // not participating
-            if (i < n) {
-                const uint32_t k = keys[i];
-                if ((k & pmask) == prefix) d = (k >> shift) & 0xFF;
-            }
-            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d);
-            if (d != 0x100 && lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
-        }
-        __syncthreads();
-        if (tid < 256) {
-            // inclusive suffix sums S[b] = sum_{b' >= b} hist[b'] (warps 0..7 cover 32 bins each)
-            uint32_t sfx = hist[tid];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, sfx, off);
-                if (lane + off < 32) sfx += y;
-            }
-            if (lane == 0) wsum[warp] = sfx;
-        }
-        __syncthreads();
-        if (tid < 256) {
-            uint32_t hi = 0;
-            for (int w2 = warp + 1; w2 < 8; ++w2) hi += wsum[w2];
-            uint32_t sfx = hist[tid];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, sfx, off);
-                if (lane + off < 32) sfx += y;
-            }
-            sfx += hi;
-            uint32_t nxt = __shfl_down_sync(0xFFFFFFFFu, sfx, 1);
-            if (lane == 31) nxt = hi;
-            if (sfx >= kk && nxt < kk) {
-                bc[0] = (uint32_t)tid;
-                bc[1] = nxt;
-            }
-        }
-        __syncthreads();
-        const uint32_t d = bc[0];
-        kk -= bc[1];
-        prefix |= d << shift;
-        pmask |= 0xFFu << shift;
-        __syncthreads();   // bc and hist are rewritten in the next pass
-    }
-    T_out = prefix;
-    kk_out = prefix == 0 ? 0u : kk;
-}
-
-// Sum over the warps before this one of a per-warp value (lane 0 of each warp
-// provides it); also returns the total.  `scratch` holds kWarps words.
-__device__ __forceinline__ uint32_t warp_prefix(uint32_t v, uint32_t *scratch, uint32_t *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    uint32_t before = 0, all = 0;
-#pragma unroll
-    for (int w2 = 0; w2 < kWarps; ++w2) {
-        const uint32_t x = scratch[w2];
-        before += (w2 < warp) ? x : 0u;
-        all += x;
-    }
-    *total = all;
-    __syncthreads();  // scratch may be reused right after
-    return before;
-}
-
-// Position-ordered compaction of the selected keys of keys[0, n): a key is
-// selected if it is > T, or == T (T != 0) and among the first kk such keys.
-// Warp w owns a contiguous run of positions and its lanes read consecutive
-// words; ballots give the order inside a warp.  emit(i, slot) is called for
-// every selected position i with its output slot; returns the number selected.
-template <typename Emit>
-__device__ int block_compact(const uint32_t *keys, int n, uint32_t T, uint32_t kk, uint32_t *scratch, Emit emit) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t lt = (1u << lane) - 1u;
-    int R = (n + kWarps - 1) / kWarps;
-    R = (R + 31) & ~31;
-    const int w0 = min(n, warp * R), w1 = min(n, w0 + R);
-    uint32_t eq = 0;
-    if (T != 0)
-        for (int base = w0; base < w1; base += 32) {
-            const int i = base + lane;
-            eq += __popc(__ballot_sync(0xFFFFFFFFu, i < w1 && keys[i] == T));
-        }
-    uint32_t eq_total;
-    const uint32_t eq_before = warp_prefix(eq, scratch, &eq_total);
-    uint32_t sel = 0, tie = eq_before;
-    for (int base = w0; base < w1; base += 32) {
-        const int i = base + lane;
-        const uint32_t k = i < w1 ? keys[i] : 0u;
-        const bool is_eq = i < w1 && T != 0 && k == T;
-        const uint32_t be = __ballot_sync(0xFFFFFFFFu, is_eq);
-        const bool take = (i < w1 && k > T) || (is_eq && tie + __popc(be & lt) < kk);
-        sel += __popc(__ballot_sync(0xFFFFFFFFu, take));
-        tie += __popc(be);
-    }
-    uint32_t sel_total;
-    uint32_t slot = warp_prefix(sel, scratch, &sel_total);
-    tie = eq_before;
-    for (int base = w0; base < w1; base += 32) {
-        const int i = base + lane;
-        const uint32_t k = i < w1 ? keys[i] : 0u;
-        const bool is_eq = i < w1 && T != 0 && k == T;
-        const uint32_t be = __ballot_sync(0xFFFFFFFFu, is_eq);
-        const bool take = (i < w1 && k > T) || (is_eq && tie + __popc(be & lt) < kk);
-        const uint32_t bs = __ballot_sync(0xFFFFFFFFu, take);
-        if (take) emit(i, slot + __popc(bs & lt));
-        slot += __popc(bs);
-        tie += __popc(be);
-    }
-    return (int)sel_total;
-}
 
 __device__ __forceinline__ int32_t out_id(const TopkArgs &a, int64_t row, int64_t li) {
     if (a.loader == LOAD_REINDEX) return (int32_t)((int64_t)__ldg(a.pool + row * a.P + li / 8) * 8 + (li & 7));
     return (int32_t)li;
 }
 
+__device__ __forceinline__ uint32_t warp_suffix_sum(uint32_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, v, off);
+        if (lane + off < 32) v += y;
+    }
+    return v;
+}
+
+struct Boundary {
+    uint32_t bin, above, inbin;
+};
+
+// The bin b of the cluster-wide histogram with S(b) >= kk > S(b+1), where S(b)
+// counts the keys in bins >= b; computed by one warp on its own.
+template <int C>
+__device__ __forceinline__ Boundary find_boundary(cg::cluster_group &cluster, const uint32_t *fine,
+                                                  const uint32_t *coarse, uint32_t kk) {
+    const int lane = threadIdx.x & 31;
+    uint2 cs = make_uint2(0u, 0u);
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        const uint32_t *rc = C > 1 ? cluster.map_shared_rank(coarse, c) : coarse;
+        const uint2 v = reinterpret_cast<const uint2 *>(rc)[lane];
+        cs.x += v.x;
+        cs.y += v.y;
+    }
+    const uint32_t c0 = warp_suffix_sum(cs.x + cs.y);  // S over coarse bins >= 2 lane
+    const uint32_t c1 = c0 - cs.x, c2 = c1 - cs.y;
+    int sub = -1;
+    uint32_t cabove = 0u;
+    if (c1 >= kk && c2 < kk) { sub = 1; cabove = c2; }
+    else if (c0 >= kk && c1 < kk) { sub = 0; cabove = c1; }
+    const int cl = __ffs(__ballot_sync(0xFFFFFFFFu, sub >= 0)) - 1;
+    const uint32_t cb = 2u * cl + (uint32_t)__shfl_sync(0xFFFFFFFFu, sub, cl);
+    cabove = __shfl_sync(0xFFFFFFFFu, cabove, cl);
+    uint32_t f = 0u;
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        const uint32_t *rf = C > 1 ? cluster.map_shared_rank(fine, c) : fine;
+        f += rf[cb * 32u + lane];
+    }
+    const uint32_t f0 = warp_suffix_sum(f) + cabove;  // S(32 cb + lane)
+    const uint32_t f1 = f0 - f;
+    const int fl = __ffs(__ballot_sync(0xFFFFFFFFu, f0 >= kk && f1 < kk)) - 1;
+    Boundary r;
+    r.bin = cb * 32u + (uint32_t)fl;
+    r.above = __shfl_sync(0xFFFFFFFFu, f1, fl);
+    r.inbin = __shfl_sync(0xFFFFFFFFu, f, fl);
+    return r;
+}
+
+template <int C>
 __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
-    extern __shared__ uint32_t dyn[];
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t wsum[8];
-    __shared__ uint32_t bc[4];
-    __shared__ uint32_t scan[kWarps + 1];
-    __shared__ int lcount;
+    extern __shared__ __align__(16) uint32_t keys[];          // this CTA's slice (+ zero padding to 4)
+    __shared__ __align__(16) uint32_t fine[kDigits][kBins];   // this CTA's histogram of each digit
+    __shared__ __align__(16) uint32_t coarse[kDigits][kCoarse];
+    __shared__ uint32_t wcnt[2][32];                          // per-warp (greater, equal) counts
 
     cg::cluster_group cluster = cg::this_cluster();
-    const int cta = (int)cluster.block_rank();
-    const int C = a.csize;
+    const int cta = C > 1 ? (int)cluster.block_rank() : 0;
     const int64_t row = blockIdx.x / C;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = a.K;
-
-    // shared memory: [0, region) keys of this slice (later CTA 0's gathered
-    // candidates), then K local candidate keys and K local ids
-    uint32_t *keys = dyn;
-    uint32_t *lkey = dyn + a.region;
-    int32_t *lid = reinterpret_cast<int32_t *>(lkey + K);
-
-    const int64_t L = row_len(a, row);
     const int64_t beg = (int64_t)cta * a.chunk;
-    int n = 0;
-    if (beg < L) n = (int)((L - beg) < a.chunk ? (L - beg) : a.chunk);
+
+    // Issue the score loads before the row length is known: the slice is
+    // clipped to the row's M entries, positions at or past the length masked.
+    int64_t Mrow = a.M;
+    if (a.loader == LOAD_BLOCKMAX) Mrow = (a.M + 7) / 8;
+    int nm = 0;
+    if (beg < Mrow) nm = (int)((Mrow - beg) < a.chunk ? (Mrow - beg) : a.chunk);
+    const int nm4 = (nm + 3) >> 2;
+#pragma unroll
+    for (int d = 0; d < kDigits; ++d) reinterpret_cast<uint4 *>(fine[d])[tid] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < kDigits * kCoarse) (&coarse[0][0])[tid] = 0u;
 
     // ---------------------------------------------------------------- load
+    int64_t L;
     const float *srow = a.scores + row * a.M;
     if (a.loader == LOAD_BLOCKMAX) {
-        const int64_t len = a.kv_len ? min((int64_t)a.kv_len[row], a.M) : a.M;
+        const int64_t len = a.kv_len ? max((int64_t)0, min((int64_t)a.kv_len[row], a.M)) : a.M;
+        L = (len + 7) / 8;
         const bool vec = ((a.M & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15) == 0);
-        for (int i = tid; i < n; i += kThreads) {
+#pragma unroll 4
+        for (int i = tid; i < nm; i += kThreads) {
             const int64_t j0 = (beg + i) * 8;
             float m = __int_as_float(0xff800000);
             if (vec && j0 + 8 <= len) {
@@ -237,108 +162,193 @@ __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
         }
     } else {
         const bool vec = ((a.M & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15) == 0);
-        const int n4 = vec ? (n & ~3) : 0;
-        for (int i = 4 * tid; i < n4; i += 4 * kThreads) {
-            const float4 x = __ldg(reinterpret_cast<const float4 *>(srow + beg + i));
-            keys[i] = score_key(x.x);
-            keys[i + 1] = score_key(x.y);
-            keys[i + 2] = score_key(x.z);
-            keys[i + 3] = score_key(x.w);
-        }
-        for (int i = n4 + tid; i < n; i += kThreads) keys[i] = score_key(__ldg(srow + beg + i));
-        if (a.loader == LOAD_REINDEX) {
-            __syncthreads();
-            const int32_t *prow = a.pool + row * a.P;
-            for (int i = tid; i < n; i += kThreads)
-                if (__ldg(prow + (beg + i) / 8) < 0) keys[i] = 0;
-        }
-    }
-    __syncthreads();
-
-    // ---------------------------------------------------------------- this slice's Top-K
-    uint32_t T, kk;
-    block_select(keys, n, K, hist, wsum, bc, T, kk);
-    int32_t *orow = a.out + row * (int64_t)K;
-    if (C == 1) {
-        const int total = block_compact(keys, n, T, kk, scan, [&](int i, uint32_t slot) {
-            orow[slot] = out_id(a, row, beg + i);
-        });
-        for (int s2 = total + tid; s2 < K; s2 += kThreads) orow[s2] = -1;
-        return;
-    }
-    const int total = block_compact(keys, n, T, kk, scan, [&](int i, uint32_t slot) {
-        lkey[slot] = keys[i];
-        lid[slot] = (int32_t)(beg + i);
-    });
-    if (tid == 0) lcount = total;
-    cluster.sync();   // every CTA's candidate list is complete
-
-    // ---------------------------------------------------------------- CTA 0 merges the lists
-    int ncand = 0;
-    if (cta == 0) {
-        int off = 0;
-        for (int c = 0; c < C; ++c) {
-            const int cnt = *cluster.map_shared_rank(&lcount, c);
-            const uint32_t *rk = cluster.map_shared_rank(lkey, c);
-            const int32_t *ri = cluster.map_shared_rank(lid, c);
-            for (int i = tid; i < cnt; i += kThreads) {
-                keys[off + i] = rk[i];                                   // gathered keys
-                reinterpret_cast<int32_t *>(keys + a.region / 2)[off + i] = ri[i];  // gathered ids
+        const int32_t *prow = a.pool + row * a.P;
+        const int q4 = vec ? (nm >> 2) : 0;
+        const int64_t len = (a.loader == LOAD_SCORES && a.kv_len) ? (int64_t)a.kv_len[row] : a.M;
+        L = len < a.M ? (len > 0 ? len : 0) : a.M;
+        const int nv = (int)(L - beg < 0 ? 0 : (L - beg < nm ? L - beg : nm));  // valid positions of this slice
+#pragma unroll 4
+        for (int j = tid; j < q4; j += kThreads) {
+            const float4 x = __ldg(reinterpret_cast<const float4 *>(srow + beg) + j);
+            uint4 k = make_uint4(score_key(x.x), score_key(x.y), score_key(x.z), score_key(x.w));
+            // the four positions share one pool block (beg and 4j are multiples of 4)
+            if (a.loader == LOAD_REINDEX && __ldg(prow + (beg + 4 * j) / 8) < 0) k = make_uint4(0u, 0u, 0u, 0u);
+            if (4 * j + 3 >= nv) {
+                if (4 * j >= nv) k.x = 0u;
+                if (4 * j + 1 >= nv) k.y = 0u;
+                if (4 * j + 2 >= nv) k.z = 0u;
+                k.w = 0u;
             }
-            off += cnt;
+            reinterpret_cast<uint4 *>(keys)[j] = k;
         }
-        ncand = off;
+        for (int i = 4 * q4 + tid; i < nm; i += kThreads) {
+            uint32_t k = i < nv ? score_key(__ldg(srow + beg + i)) : 0u;
+            if (a.loader == LOAD_REINDEX && __ldg(prow + (beg + i) / 8) < 0) k = 0u;
+            keys[i] = k;
+        }
     }
-    cluster.sync();   // remote lists read; the other CTAs may leave
-    if (cta != 0) return;
+    if (tid < 4 * nm4 - nm) keys[nm + tid] = 0u;  // pad to a multiple of 4 with the invalid key
     __syncthreads();
-    uint32_t T2, kk2;
-    block_select(keys, ncand, K, hist, wsum, bc, T2, kk2);
-    const int32_t *gid = reinterpret_cast<const int32_t *>(keys + a.region / 2);
-    const int total2 = block_compact(keys, ncand, T2, kk2, scan, [&](int i, uint32_t slot) {
-        orow[slot] = out_id(a, row, gid[i]);
-    });
-    for (int s2 = total2 + tid; s2 < K; s2 += kThreads) orow[s2] = -1;
+
+    // ---------------------------------------------------------------- cluster-wide radix select
+    // Result: every key > T is selected, plus the first kk keys equal to T (T != 0).
+    uint32_t T = 0u, kk = 0u;
+    if (L > K) {  // otherwise every valid key is selected
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
+        uint32_t prefix = 0u, pmask = 0u;
+        kk = (uint32_t)K;
+#pragma unroll 1
+        for (int d = 0; d < kDigits; ++d) {
+            const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
+            const uint32_t dmask = d == 2 ? 0x3FFu : 0x7FFu;
+            uint32_t *h = fine[d];
+#pragma unroll 4
+            for (int j = tid; j < nm4; j += kThreads) {
+                const uint4 v = k4[j];
+                if (v.x != 0u && (v.x & pmask) == prefix) atomicAdd(&h[(v.x >> shift) & dmask], 1u);
+                if (v.y != 0u && (v.y & pmask) == prefix) atomicAdd(&h[(v.y >> shift) & dmask], 1u);
+                if (v.z != 0u && (v.z & pmask) == prefix) atomicAdd(&h[(v.z >> shift) & dmask], 1u);
+                if (v.w != 0u && (v.w & pmask) == prefix) atomicAdd(&h[(v.w >> shift) & dmask], 1u);
+            }
+            __syncthreads();
+            {   // coarse bins: eight threads' fine bins each
+                const uint4 q = reinterpret_cast<const uint4 *>(h)[tid];
+                uint32_t s = q.x + q.y + q.z + q.w;
+                s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+                s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+                s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
+                if ((tid & 7) == 0) coarse[d][tid >> 3] = s;
+            }
+            if (C > 1) cluster.sync(); else __syncthreads();  // every slice's histograms are complete
+            if (d == 0) {  // at most K valid keys: take them all
+                uint32_t tot = 0u;
+#pragma unroll
+                for (int c = 0; c < C; ++c) {
+                    const uint32_t *rc = C > 1 ? cluster.map_shared_rank(coarse[0], c) : coarse[0];
+                    const uint2 v = reinterpret_cast<const uint2 *>(rc)[lane];
+                    tot += v.x + v.y;
+                }
+                if (__reduce_add_sync(0xFFFFFFFFu, tot) <= (uint32_t)K) {
+                    kk = 0u;
+                    break;
+                }
+            }
+            const Boundary bd = find_boundary<C>(cluster, h, coarse[d], kk);
+            kk -= bd.above;
+            prefix |= bd.bin << shift;
+            pmask |= dmask << shift;
+            if (bd.inbin == kk) {  // the boundary bin is taken whole: every key >= prefix
+                T = prefix - 1u;   // prefix >= 2^21 here: a bin that holds valid keys is never 0
+                kk = 0u;
+                break;
+            }
+            if (d == kDigits - 1) T = prefix;
+        }
+    }
+
+    // ---------------------------------------------------------------- position-ordered compaction
+    // Warp w owns a contiguous run of this slice; ballots order its lanes.
+    int R = (nm + kWarps - 1) / kWarps;
+    R = (R + 31) & ~31;
+    const int w0 = min(nm, warp * R), w1 = min(nm, w0 + R);
+    uint32_t gt = 0, eq = 0;
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const uint32_t k = i < w1 ? keys[i] : 0u;
+        gt += __popc(__ballot_sync(0xFFFFFFFFu, k > T));
+        eq += __popc(__ballot_sync(0xFFFFFFFFu, T != 0u && k == T));
+    }
+    if (lane == 0) {
+        wcnt[0][warp] = gt;
+        wcnt[1][warp] = eq;
+    }
+    if (C > 1) cluster.sync(); else __syncthreads();  // every warp's counts are published
+    uint32_t bg = 0u, be_ = 0u, tg = 0u, te = 0u;     // (before this warp, in the row) counts
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        const uint32_t(*rc)[32] = C > 1 ? cluster.map_shared_rank(wcnt, c) : wcnt;
+        const uint32_t vg = lane < kWarps ? rc[0][lane] : 0u, ve = lane < kWarps ? rc[1][lane] : 0u;
+        const bool before = c < cta || (c == cta && lane < warp);
+        bg += before ? vg : 0u;
+        be_ += before ? ve : 0u;
+        tg += vg;
+        te += ve;
+    }
+    if (C > 1) cluster.barrier_arrive();  // this CTA's remote reads are done
+    const uint32_t gt_before = __reduce_add_sync(0xFFFFFFFFu, bg), eq_before = __reduce_add_sync(0xFFFFFFFFu, be_);
+    int32_t *orow = a.out + row * (int64_t)K;
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t tie = eq_before;
+    uint32_t slot = gt_before + min(kk, tie);
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const uint32_t k = i < w1 ? keys[i] : 0u;
+        const bool is_eq = T != 0u && k == T;
+        const uint32_t bq = __ballot_sync(0xFFFFFFFFu, is_eq);
+        const bool take = k > T || (is_eq && tie + __popc(bq & lt) < kk);
+        const uint32_t bs = __ballot_sync(0xFFFFFFFFu, take);
+        if (take) orow[slot + __popc(bs & lt)] = out_id(a, row, beg + i);
+        slot += __popc(bs);
+        tie += __popc(bq);
+    }
+    if (cta == C - 1) {
+        const uint32_t gt_total = __reduce_add_sync(0xFFFFFFFFu, tg), eq_total = __reduce_add_sync(0xFFFFFFFFu, te);
+        const int total = (int)(gt_total + min(kk, eq_total));
+        for (int s2 = total + tid; s2 < K; s2 += kThreads) orow[s2] = -1;
+    }
+    if (C > 1) cluster.barrier_wait();  // no CTA leaves while another may still read its counts
+}
+
+// Keys per CTA and dynamic shared memory for a split of the rows over C CTAs.
+struct TopkPlan {
+    int64_t chunk;
+    size_t smem;
+};
+
+TopkPlan plan_for(int64_t Lmax, int C) {
+    TopkPlan p;
+    p.chunk = ((Lmax + C - 1) / C + 3) & ~int64_t(3);
+    if (p.chunk < 4) p.chunk = 4;
+    p.smem = (size_t)p.chunk * sizeof(uint32_t);
+    return p;
+}
+
+// CTAs per row: enough that a slice fits shared memory, and for rows of more
+// than 4096 candidates up to 4 while the grid stays within one CTA per SM
+// (wider clusters than 4 measured slower on 152-SM parts).
+int cluster_for(int64_t rows, int64_t Lmax, int sms) {
+    int C = 1;
+    while (C < kMaxCluster && plan_for(Lmax, C).chunk > kMaxKeysPerCta) C *= 2;
+    while (C < 4 && plan_for(Lmax, C).chunk > 4096 && rows * C * 2 <= (int64_t)sms) C *= 2;
+    return C;
 }
 
 csa2_status launch_topk(const TopkArgs &in, int64_t Lmax, cudaStream_t stream) {
     TopkArgs a = in;
     if (a.rows == 0) return CSA2_OK;
-    const int sms = num_sms();
-    const size_t smem_cap = 220 * 1024;
-    auto chunk_for = [&](int c) { int64_t ch = (Lmax + c - 1) / c; return (ch + 3) & ~int64_t(3); };
-    auto smem_for = [&](int c) {
-        int64_t region = chunk_for(c);
-        if (c > 1 && region < 2 * (int64_t)c * a.K) region = 2 * (int64_t)c * a.K;
-        return (size_t)(region + 2 * (int64_t)a.K) * sizeof(uint32_t);
-    };
-    int C = 1;
-    while (C < kMaxCluster && a.rows * C * 2 <= sms) C *= 2;
-    while (C > 1 && chunk_for(C) < 1024) C /= 2;
-    while (C < kMaxCluster && (chunk_for(C) > kMaxKeysPerCta || smem_for(C) > smem_cap)) C *= 2;
-    if (chunk_for(C) > kMaxKeysPerCta || smem_for(C) > smem_cap) {
-        set_error("topk: a row of %lld candidates with K=%d does not fit %d CTAs", (long long)Lmax, a.K, kMaxCluster);
+    const int C = cluster_for(a.rows, Lmax, num_sms());
+    const TopkPlan pl = plan_for(Lmax, C);
+    if (pl.chunk > kMaxKeysPerCta || pl.smem > (size_t)kSmemCap) {
+        set_error("topk: a row of %lld candidates does not fit %d CTAs", (long long)Lmax, kMaxCluster);
         return CSA2_ERR_UNSUPPORTED;
     }
-    int64_t chunk = chunk_for(C);
-    if (chunk < 4) chunk = 4;
-    a.chunk = (int)chunk;
-    a.csize = C;
-    int64_t region = chunk;
-    if (C > 1 && region < 2 * (int64_t)C * a.K) region = 2 * (int64_t)C * a.K;
-    a.region = (int)((region + 1) & ~int64_t(1));
-    const size_t smem = (size_t)(a.region + 2 * (int64_t)a.K) * sizeof(uint32_t);
-    static bool smem_set[64];
-    CSA2_CUDA_CALL(ensure_smem_limit((const void *)topk_radix_kernel, (int)smem_cap, smem_set), "topk: smem attribute");
+    a.chunk = (int)pl.chunk;
     const int64_t grid = a.rows * C;
     if (grid > 0x7FFFFFFF) {
         set_error("topk: too many rows");
         return CSA2_ERR_UNSUPPORTED;
     }
+    const void *fn = C == 1 ? (const void *)topk_radix_kernel<1>
+                   : C == 2 ? (const void *)topk_radix_kernel<2>
+                   : C == 4 ? (const void *)topk_radix_kernel<4>
+                            : (const void *)topk_radix_kernel<8>;
+    static bool smem_set[4][64];
+    const int ci = C == 1 ? 0 : (C == 2 ? 1 : (C == 4 ? 2 : 3));
+    CSA2_CUDA_CALL(ensure_smem_limit(fn, kSmemCap, smem_set[ci]), "topk: smem attribute");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -347,7 +357,8 @@ csa2_status launch_topk(const TopkArgs &in, int64_t Lmax, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    CSA2_CUDA_CALL(cudaLaunchKernelEx(&cfg, topk_radix_kernel, a), "topk_radix_kernel launch");
+    void *args[] = {&a};
+    CSA2_CUDA_CALL(cudaLaunchKernelExC(&cfg, fn, args), "topk_radix_kernel launch");
     CSA2_LAUNCH_CHECK("topk_radix_kernel");
     return CSA2_OK;
 }
