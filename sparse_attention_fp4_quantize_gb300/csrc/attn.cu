@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(AttnCfg<D, DV, NG>::THREADS, 1) sparse_attn_ke
     int32_t *sValid = reinterpret_cast<int32_t *>(smem + C::OFF_V);  // [2][TE]
     float *sL = reinterpret_cast<float *>(smem + C::OFF_V + 2 * TE * 4);  // [2][HB]
 
+    pdl_wait();
+    pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int hg = warp >> 1;    // head group of 16
     const int half = warp & 1;   // entry half in S, dv half in P V
@@ -408,6 +410,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restri
                                                            const float *__restrict__ part_lse, int splits,
                                                            int64_t rows, int dv, float *__restrict__ out,
                                                            float *__restrict__ lse) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t row = blockIdx.x;
     __shared__ float wts[64];
     __shared__ float s_lse;
@@ -455,12 +459,14 @@ csa2_status launch_attn(AttnArgs a, cudaStream_t stream) {
     static bool smem_set[64];
     CSA2_CUDA_CALL(ensure_smem_limit((const void *)kern, (int)C::SMEM, smem_set), "sparse_attn: smem attribute");
     dim3 grid((unsigned)((int64_t)a.B * a.T), a.splits, a.H / C::HB);
-    kern<<<grid, C::THREADS, C::SMEM, stream>>>(a);
+    CSA2_CUDA_CALL(launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, stream, a), "sparse_attn_kernel launch");
     CSA2_LAUNCH_CHECK("sparse_attn_kernel");
     if (a.splits > 1) {
         const int64_t rows = (int64_t)a.B * a.T * a.H;
-        attn_combine_kernel<<<(unsigned)rows, 128, 0, stream>>>(a.part_o, a.part_lse, a.splits, rows, DV, a.out,
-                                                               a.lse);
+        CSA2_CUDA_CALL(launch_pdl(attn_combine_kernel, dim3((unsigned)rows), dim3(128), 0, stream,
+                                  (const float *)a.part_o, (const float *)a.part_lse, a.splits, rows, DV, a.out,
+                                  a.lse),
+                       "attn_combine_kernel launch");
         CSA2_LAUNCH_CHECK("attn_combine_kernel");
     }
     return CSA2_OK;

@@ -159,8 +159,6 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     const int hblk = (int)(group - bt * a.hblocks);
     const int64_t b = bt / a.T;
     const int h0 = hblk * HB;
-    int64_t len = a.kv_len ? (int64_t)a.kv_len[bt] : a.N;
-    len = len < a.N ? len : a.N;
 
     uint8_t *sK = smem + OFF_K;
     uint8_t *sQ = smem + OFF_Q;
@@ -179,11 +177,9 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     const uint32_t bar_o = bar_ld + 16;
     const uint32_t bar_rx = bar_ld + 24;
 
-    // the selected entry of this thread: its index load overlaps the set-up below
     const int e = tid & (TM - 1);   // entry of this thread in the tile
     const int half = tid >> 7;      // which 288 channels of the entry
     const int sel = rank * TM + e;
-    const int64_t j = (sel < a.K) ? (int64_t)__ldg(a.idx + bt * a.K + sel) : -1;
 
     if (tid == 0) {
         tc::mbar_init(bar_ld, TM);   // one arrival per entry thread
@@ -194,6 +190,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
     __syncthreads();
+    pdl_wait();   // the set-up above overlaps the previous kernel's tail
+    const int64_t j = (sel < a.K) ? (int64_t)__ldg(a.idx + bt * a.K + sel) : -1;   // this thread's entry
+    int64_t len = a.kv_len ? (int64_t)a.kv_len[bt] : a.N;
+    len = len < a.N ? len : a.N;
 
     // ---- 1. gather: TMA bulk copies of Q rows and the selected code rows
     if (half == 0 && e < HB) {      // Q rows do not depend on the indices: first
@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         tc::commit(bar_o);
     }
     ok = tc::mbar_wait(bar_o, 0, MAX_POLLS) && ok;
+    pdl_launch_dependents();   // the next kernel may launch during the merge
     tc::fence_after();
     if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
 
@@ -497,13 +498,14 @@ csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const v
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = a.csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     CSA2_CUDA_CALL(cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel, a), "sparse_attn_tc_kernel launch");
     CSA2_LAUNCH_CHECK("sparse_attn_tc_kernel");
     return CSA2_OK;

@@ -83,6 +83,39 @@ __device__ __forceinline__ uint32_t score_key(float f) {
     return (k <= 0x007FFFFFu) ? 0u : k;
 }
 
+// Programmatic dependent launch.  The library's kernels (all but the Top-K
+// kernel) are launched with programmatic stream serialization allowed, so
+// they may start while the previous kernel on the stream drains.  Before
+// pdl_wait() a kernel touches only its own shared memory, TMEM and barriers;
+// pdl_wait() returns once the previous grid has completed with its memory
+// writes visible (without the launch attribute it returns at once).
+// pdl_launch_dependents() lets the next kernel begin launching: at the start
+// of short kernels, before the final phase of the attention and Top-K.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+static inline cudaLaunchAttribute pdl_attribute() {
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    return at;
+}
+
+// Plain (non-cluster) launch with the programmatic-serialization attribute.
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 __device__ __forceinline__ void flag_error(uint32_t *err_flag, uint32_t bit) {
     if (err_flag) atomicOr(err_flag, bit);
 }

@@ -87,6 +87,8 @@ struct ScoreArgs {
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads) index_score_kernel(ScoreArgs a) {
     constexpr int ES = FP8 ? 1 : 2;      // element size
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
@@ -192,6 +194,8 @@ __global__ void __launch_bounds__(kThreads) index_score_kernel(ScoreArgs a) {
 // CH x 1 KB of keys in flight.
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 2) index_score_decode_kernel(ScoreArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int ES = FP8 ? 1 : 2;
     constexpr int NV = FP8 ? 1 : 2;          // 16-byte loads per 16 d-values
     constexpr int CH = FP8 ? 8 : 4;          // groups per warp chunk
@@ -342,13 +346,19 @@ extern "C" csa2_status csa2_index_score(csa2_mode mode, int B, int T, int64_t N,
         int64_t cap_d = (int64_t)num_sms() * 2;
         int blocks_d = (int)(want_d < cap_d ? want_d : cap_d);
         if (q_dt == CSA2_FP8_E4M3)
-            index_score_decode_kernel<true><<<blocks_d, kThreads, 0, stream_of(stream)>>>(a);
+            CSA2_CUDA_CALL(launch_pdl(index_score_decode_kernel<true>, dim3(blocks_d), dim3(kThreads), 0,
+                                      stream_of(stream), a),
+                           "index_score_decode_kernel launch");
         else
-            index_score_decode_kernel<false><<<blocks_d, kThreads, 0, stream_of(stream)>>>(a);
+            CSA2_CUDA_CALL(launch_pdl(index_score_decode_kernel<false>, dim3(blocks_d), dim3(kThreads), 0,
+                                      stream_of(stream), a),
+                           "index_score_decode_kernel launch");
     } else if (q_dt == CSA2_FP8_E4M3) {
-        index_score_kernel<true><<<blocks, kThreads, 0, stream_of(stream)>>>(a);
+        CSA2_CUDA_CALL(launch_pdl(index_score_kernel<true>, dim3(blocks), dim3(kThreads), 0, stream_of(stream), a),
+                       "index_score_kernel launch");
     } else {
-        index_score_kernel<false><<<blocks, kThreads, 0, stream_of(stream)>>>(a);
+        CSA2_CUDA_CALL(launch_pdl(index_score_kernel<false>, dim3(blocks), dim3(kThreads), 0, stream_of(stream), a),
+                       "index_score_kernel launch");
     }
     CSA2_LAUNCH_CHECK("index_score_kernel");
     return CSA2_OK;

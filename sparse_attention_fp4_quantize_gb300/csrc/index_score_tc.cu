@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(Pref
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+    pdl_launch_dependents();
     uint32_t uses0 = 0, uses1 = 0;   // completed phases of the two accumulator barriers
     bool ok = true;
 
@@ -236,7 +238,8 @@ csa2_status launch_index_score_prefill_tc(int B, int T, int64_t N, const void *q
     a.kranges = (a.ktiles + KTILES_PER_ITEM - 1) / KTILES_PER_ITEM;
     a.items = (int64_t)B * a.qtiles * a.kranges;
     int64_t grid = a.items < num_sms() ? a.items : num_sms();
-    index_score_prefill_tc_kernel<<<(unsigned)grid, THREADS, SMEM, stream>>>(a);
+    CSA2_CUDA_CALL(launch_pdl(index_score_prefill_tc_kernel, dim3((unsigned)grid), dim3(THREADS), SMEM, stream, a),
+                   "index_score_prefill_tc_kernel launch");
     CSA2_LAUNCH_CHECK("index_score_prefill_tc_kernel");
     return CSA2_OK;
 }

@@ -112,6 +112,8 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(
     const uint16_t *__restrict__ kv, uint32_t total_units, FastDiv upr_div, int D, int64_t stride,
     int64_t row0, const int64_t *__restrict__ dst_slot, int64_t n_slots, uint8_t *__restrict__ codes,
     uint8_t *__restrict__ scales, uint32_t *err_flag) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const uint32_t nthreads = gridDim.x * kThreads;
     const uint32_t upr = upr_div.d;
@@ -189,9 +191,10 @@ extern "C" csa2_status csa2_quantize_kv_fp4(const void *kv, int64_t rows, int D,
         int64_t want = ((int64_t)units + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
         int blocks = (int)(want < max_blocks ? want : max_blocks);
         if (blocks < 1) blocks = 1;
-        quantize_fp4_kernel<<<blocks, kThreads, 0, stream_of(stream)>>>(
-            (const uint16_t *)kv, units, fd, D, kv_row_stride, r0, dst_slot, n_slots, codes, scales,
-            err_flag);
+        CSA2_CUDA_CALL(launch_pdl(quantize_fp4_kernel, dim3(blocks), dim3(kThreads), 0, stream_of(stream),
+                                  (const uint16_t *)kv, units, fd, D, kv_row_stride, r0, dst_slot, n_slots, codes,
+                                  scales, err_flag),
+                       "quantize_fp4_kernel launch");
         CSA2_LAUNCH_CHECK("quantize_fp4_kernel");
     }
     return CSA2_OK;
