@@ -41,7 +41,7 @@ namespace {
 
 constexpr int TM = 128;                    // entries per CTA (MMA M)
 constexpr int D = 576, DV = 512, HB = 64;  // channels, value channels, heads per cluster
-constexpr int THREADS = 256;
+constexpr int THREADS = 512;               // 4 threads per entry, 8 per head
 constexpr int MAX_S = 4;                   // CTAs per cluster
 constexpr uint32_t KT_SBO = (D / 8) * 128;        // 9216: bytes per 8-entry group of the Khat tile
 constexpr uint32_t KT_BYTES = (TM / 8) * KT_SBO;  // 147456
@@ -51,30 +51,40 @@ constexpr uint32_t QRAW_STRIDE = D * 2 + 16;      // 1168: staged bf16 Q rows (p
 constexpr uint32_t CRAW_STRIDE = D / 2 + 16;      // 304: staged code rows (padded)
 constexpr uint32_t OFF_QRAW = 0;                  // staging lives in the Khat region before dequant
 constexpr uint32_t OFF_CRAW = HB * QRAW_STRIDE;   // 74752
-constexpr int ST_STRIDE = TM + 4;                 // fp32 row stride of the transposed S (132)
-constexpr uint32_t ST_BYTES = HB * ST_STRIDE * 4; // 33792
+constexpr int ST_STRIDE = TM + 8;                 // fp32 row stride of the transposed S (136)
+constexpr uint32_t ST_BYTES = HB * ST_STRIDE * 4; // 34816
 constexpr uint32_t P_SBO = (TM / 8) * 128;        // 2048: bytes per 8-head group of the P tile
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_Q = OFF_K + KT_BYTES;
 constexpr uint32_t OFF_ST = OFF_Q;                // reuses the Q tile after S is computed
-constexpr uint32_t OFF_P = OFF_Q + ST_BYTES;
+constexpr uint32_t OFF_P = OFF_Q + Q_BYTES - (HB / 8) * P_SBO;   // P at the end: staging fits below it
 constexpr uint32_t OFF_MISC = OFF_Q + Q_BYTES;
-constexpr uint32_t OFF_BAR = OFF_MISC;            // 4 mbarriers
-constexpr uint32_t OFF_TMEM = OFF_BAR + 32;
+constexpr uint32_t OFF_BAR = OFF_MISC;            // 5 mbarriers: Q, codes, S, O, received (64 bytes reserved)
+constexpr uint32_t OFF_TMEM = OFF_BAR + 64;
 constexpr uint32_t OFF_VALID = OFF_TMEM + 16;     // int[128]
 constexpr uint32_t OFF_CS = OFF_VALID + TM * 4;   // float[64] logit factor per head
 constexpr uint32_t OFF_M = OFF_CS + HB * 4;       // float[64] row max (log2 domain)
 constexpr uint32_t OFF_L = OFF_M + HB * 4;        // float[64] row sum
 constexpr uint32_t OFF_W = OFF_L + HB * 4;        // float[MAX_S][64] merge weights
 constexpr uint32_t OFF_LSE = OFF_W + MAX_S * HB * 4;      // float[64]
-constexpr uint32_t SMEM = OFF_LSE + HB * 4;
+constexpr uint32_t OFF_IL = OFF_LSE + HB * 4;             // float[64] 1 / row sum
+constexpr uint32_t OFF_STATS = OFF_IL + HB * 4;           // float[MAX_S][2][64] every CTA's (max, sum)
+constexpr uint32_t SMEM = OFF_STATS + MAX_S * 2 * HB * 4;
+// Merge payload: the normalised partial O (O / L) of W channels as f16 rows of
+// RSH halves (136 bytes: 8-byte accesses by consecutive channels are
+// conflict-free).
+constexpr int RSH = HB + 4;
+__host__ __device__ constexpr uint32_t slice_bytes_for(int W) { return (uint32_t)W * RSH * 2; }
 constexpr uint32_t TMEM_COLS = 512;               // S^T: 64 cols, O^T: 4 x 64 cols
 constexpr uint32_t S_COL = 0, O_COL = 64;
 constexpr uint32_t MAX_POLLS = 1u << 22;          // about a second of polling at most
 static_assert(OFF_CRAW + TM * CRAW_STRIDE <= KT_BYTES, "staging must fit in the Khat region");
-static_assert((DV * (HB + 4) + MAX_S * 2 * HB) * 4 <= KT_BYTES, "received partials must fit in the Khat region");
-static_assert(((DV / 2) * (HB + 4) + 2 * HB) * 4 <= Q_BYTES, "a staged slice must fit in the Q region");
+static_assert(MAX_S * slice_bytes_for(DV / MAX_S) <= KT_BYTES && 2 * slice_bytes_for(DV / 2) <= KT_BYTES,
+              "received partials must fit in the Khat region");
+static_assert(slice_bytes_for(DV / MAX_S) % 16 == 0 && slice_bytes_for(DV / 2) % 16 == 0, "bulk copy sizes");
 static_assert(ST_BYTES + (HB / 8) * P_SBO <= Q_BYTES, "S^T copy and P must fit in the Q region");
+static_assert((MAX_S - 1) * slice_bytes_for(DV / MAX_S) <= OFF_P - OFF_Q && slice_bytes_for(DV / 2) <= OFF_P - OFF_Q,
+              "the slices owed to other CTAs are staged below P while P V runs");
 static_assert(SMEM <= 227 * 1024, "shared memory");
 
 struct TcArgs {
@@ -172,61 +182,74 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     float *sL = reinterpret_cast<float *>(smem + OFF_L);
     float *sW = reinterpret_cast<float *>(smem + OFF_W);
     float *sLse = reinterpret_cast<float *>(smem + OFF_LSE);
-    const uint32_t bar_ld = tc::smem_u32(smem + OFF_BAR);
-    const uint32_t bar_s = bar_ld + 8;
-    const uint32_t bar_o = bar_ld + 16;
-    const uint32_t bar_rx = bar_ld + 24;
+    float *sIL = reinterpret_cast<float *>(smem + OFF_IL);
+    float *sStats = reinterpret_cast<float *>(smem + OFF_STATS);
+    const uint32_t bar_q = tc::smem_u32(smem + OFF_BAR);   // Q rows landed
+    const uint32_t bar_ld = bar_q + 8;                       // code rows landed
+    const uint32_t bar_s = bar_q + 16;                       // S MMA done
+    const uint32_t bar_o = bar_q + 24;                       // P V done
+    const uint32_t bar_rx = bar_q + 32;                      // other CTAs' slices landed
 
     const int e = tid & (TM - 1);   // entry of this thread in the tile
-    const int half = tid >> 7;      // which 288 channels of the entry
+    const int qt = tid >> 7;        // which 144 channels of the entry (0..3)
     const int sel = rank * TM + e;
 
     if (tid == 0) {
-        tc::mbar_init(bar_ld, TM);   // one arrival per entry thread
+        tc::mbar_init(bar_q, HB);    // one arrival per head row
+        tc::mbar_init(bar_ld, TM);   // one arrival per entry
         tc::mbar_init(bar_s, 1);
         tc::mbar_init(bar_o, 1);
         tc::mbar_init(bar_rx, 1);
         tc::mbar_init_fence();
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
+    if (tid < HB) reinterpret_cast<uint32_t *>(sM)[tid] = 0u;   // per-head max |q| (bits), used by 2a
     __syncthreads();
+    // cluster barrier, first half: this CTA runs; the wait comes before the first remote store
+    if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     pdl_wait();   // the set-up above overlaps the previous kernel's tail
     const int64_t j = (sel < a.K) ? (int64_t)__ldg(a.idx + bt * a.K + sel) : -1;   // this thread's entry
     int64_t len = a.kv_len ? (int64_t)a.kv_len[bt] : a.N;
     len = len < a.N ? len : a.N;
 
     // ---- 1. gather: TMA bulk copies of Q rows and the selected code rows
-    if (half == 0 && e < HB) {      // Q rows do not depend on the indices: first
+    if (qt == 0 && e < HB) {        // Q rows do not depend on the indices: first
         const uint16_t *qrow = a.q + ((bt * a.H) + h0 + e) * (int64_t)D;
-        mbar_expect_tx(bar_ld, D * 2);
-        bulk_g2s(tc::smem_u32(smem + OFF_QRAW + e * QRAW_STRIDE), qrow, D * 2, bar_ld);
+        mbar_arrive_expect_tx(bar_q, D * 2);
+        bulk_g2s(tc::smem_u32(smem + OFF_QRAW + e * QRAW_STRIDE), qrow, D * 2, bar_q);
     }
     const bool valid = j >= 0 && j < len;
-    if (half == 0) {
+    if (qt == 0) {
         if (!valid && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
         sValid[e] = valid ? 1 : 0;
         mbar_arrive_expect_tx(bar_ld, valid ? D / 2 : 0);
         if (valid)
             bulk_g2s(tc::smem_u32(smem + OFF_CRAW + e * CRAW_STRIDE), a.codes + (b * a.N + j) * (D / 2), D / 2, bar_ld);
     }
-    uint32_t sw[5];                 // scale words: plain loads, consumed by the dequantiser
+    // scale bytes 9 qt .. 9 qt + 8 of the entry's 36: words 2 qt .. 2 qt + 2, shifted by qt bytes
+    // (consumed only by the dequantiser, so their latency overlaps the Q conversion)
+    uint32_t sw0 = 0, sw1 = 0, sw2 = 0;
     if (valid) {
-        const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + (b * a.N + j) * (D / 16)) + 4 * half;
-#pragma unroll
-        for (int i = 0; i < 5; ++i) sw[i] = __ldg(srow + i);
+        const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + (b * a.N + j) * (D / 16)) + 2 * qt;
+        sw0 = __ldg(srow);
+        sw1 = __ldg(srow + 1);
+        sw2 = __ldg(srow + 2);
     }
-    bool ok = tc::mbar_wait(bar_ld, 0, MAX_POLLS);
+    bool ok = tc::mbar_wait(bar_q, 0, MAX_POLLS);   // Q first: its conversion overlaps the code copies
 
     // ---- 2a. staged Q -> registers, per-head power-of-two scale, f16 core-matrix tile [head][channel]
     {
-        const int hq = warp * 8 + (lane & 7);
-        const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE;
-        uint4 qv[18];
+        // lanes: 8 heads x 4 chunk positions, so both the staged-row reads and the
+        // tile stores touch every bank once per 128 bytes; a warp pair covers the
+        // 72 chunks of its 8 heads (36 each, 9 per thread)
+        const int hq = 8 * (warp & 7) + (lane & 7), cpos = lane >> 3, c0 = 36 * (warp >> 3);
+        const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE + (c0 + cpos) * 16;
+        uint4 qv[9];
 #pragma unroll
-        for (int i = 0; i < 18; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + ((lane >> 3) + 4 * i) * 16);
+        for (int i = 0; i < 9; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + i * 64);
         float mx = 0.f;
 #pragma unroll
-        for (int i = 0; i < 18; ++i) {
+        for (int i = 0; i < 9; ++i) {
             const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -234,56 +257,54 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+        uint32_t *hmax = reinterpret_cast<uint32_t *>(sM);
+        if (cpos == 0) atomicMax(hmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
+        __syncthreads();
+        mx = __uint_as_float(hmax[hq]);
         int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
         int sh = 14 - e2;  // max |q| * 2^sh in [2^14, 2^15)
         sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
         const float up = ldexpf(1.0f, sh);
-        uint8_t *qdst = sQ + warp * Q_SBO + (lane & 7) * 16;
+        uint8_t *qdst = sQ + (hq >> 3) * Q_SBO + (hq & 7) * 16 + (c0 + cpos) * 128;
 #pragma unroll
-        for (int i = 0; i < 18; ++i) {
+        for (int i = 0; i < 9; ++i) {
             const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
             uint32_t o[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
-            *reinterpret_cast<uint4 *>(qdst + ((lane >> 3) + 4 * i) * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(qdst + i * 512) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        if ((lane >> 3) == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
+        if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
     }
     // ---- 2b. staged codes -> registers (the Khat tile overwrites the staging area)
-    uint4 cw[9];
+    ok = tc::mbar_wait(bar_ld, 0, MAX_POLLS) && ok;
+    uint2 cw[9];   // chunk pairs: 8 channels per word, one 16-channel scale group per pair
     {
-        const uint8_t *craw = smem + OFF_CRAW + e * CRAW_STRIDE + half * 144;
+        const uint8_t *craw = smem + OFF_CRAW + e * CRAW_STRIDE + qt * 72;
 #pragma unroll
-        for (int i = 0; i < 9; ++i) cw[i] = valid ? *reinterpret_cast<const uint4 *>(craw + 16 * i) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 9; ++i) cw[i] = valid ? *reinterpret_cast<const uint2 *>(craw + 8 * i) : make_uint2(0, 0);
     }
     __syncthreads();
-    // ---- 2c. dequantise this thread's 288 channels of its entry into the Khat tile
+    // ---- 2c. dequantise this thread's 144 channels of its entry into the Khat tile
     {
-        uint8_t *kdst = sK + (e >> 3) * KT_SBO + (e & 7) * 16;
+        uint8_t *kdst = sK + (e >> 3) * KT_SBO + (e & 7) * 16 + qt * 18 * 128;
+        const uint32_t s0 = __funnelshift_r(sw0, sw1, 8 * qt), s1 = __funnelshift_r(sw1, sw2, 8 * qt);
+        const uint32_t s2 = sw2 >> (8 * qt);
 #pragma unroll
         for (int i = 0; i < 9; ++i) {
-            const uint32_t w4[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+            uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (valid) {
+                const uint32_t sb = ((i < 4 ? s0 : (i < 8 ? s1 : s2)) >> (8 * (i & 3))) & 0xFFu;
+                const uint32_t sc = e4m3_to_f16x2_bcast(sb);
 #pragma unroll
-            for (int gg = 0; gg < 2; ++gg) {           // the two 16-channel groups of this chunk
-                const int lb = 2 * i + gg;            // group index within this half (0..17)
-                uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                if (valid) {
-                    // scale byte lb + 2*half of the loaded words, compile-time indices only
-                    const uint32_t s_lo = (sw[lb >> 2] >> (8 * (lb & 3))) & 0xFFu;
-                    const uint32_t s_hi = (sw[(lb + 2) >> 2] >> (8 * ((lb + 2) & 3))) & 0xFFu;
-                    const uint32_t sc = e4m3_to_f16x2_bcast(half ? s_hi : s_lo);
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const uint32_t wd = w4[2 * gg + k];
-#pragma unroll
-                        for (int bb = 0; bb < 4; ++bb) r[4 * k + bb] = hmul2(e2m1x2_to_f16x2((wd >> (8 * bb)) & 0xFF), sc);
-                    }
+                for (int bb = 0; bb < 4; ++bb) {
+                    r[bb] = hmul2(e2m1x2_to_f16x2((cw[i].x >> (8 * bb)) & 0xFF), sc);
+                    r[4 + bb] = hmul2(e2m1x2_to_f16x2((cw[i].y >> (8 * bb)) & 0xFF), sc);
                 }
-                const int c8 = half * 36 + 4 * i + 2 * gg;
-                *reinterpret_cast<uint4 *>(kdst + c8 * 128) = make_uint4(r[0], r[1], r[2], r[3]);
-                *reinterpret_cast<uint4 *>(kdst + (c8 + 1) * 128) = make_uint4(r[4], r[5], r[6], r[7]);
             }
+            *reinterpret_cast<uint4 *>(kdst + (2 * i) * 128) = make_uint4(r[0], r[1], r[2], r[3]);
+            *reinterpret_cast<uint4 *>(kdst + (2 * i + 1) * 128) = make_uint4(r[4], r[5], r[6], r[7]);
         }
     }
     tc::fence_async_smem();
@@ -306,16 +327,16 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     tc::fence_after();
 
     // ---- 4a. S^T -> shared memory, transposed to [head][entry] (the Q tile is free now)
-    const int quarter = warp & 3, hh = warp >> 2;
+    const int quarter = warp & 3, hh = warp >> 2;   // TMEM lane quarter, 16-column group
     {
-        uint32_t r[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + S_COL + 32 * hh, r);
+        uint32_t r[16];
+        tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + S_COL + 16 * hh, r);
         tc::tmem_ld_wait();
         const int ee = 32 * quarter + lane;
         const bool v = ok && sValid[ee];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int h = 32 * hh + jj;
+        for (int jj = 0; jj < 16; ++jj) {
+            const int h = 16 * hh + jj;
             sT[h * ST_STRIDE + ee] = v ? __uint_as_float(r[jj]) * sCs[h] : -INFINITY;
         }
     }
@@ -323,31 +344,33 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
 
     // ---- 4b. softmax per head over this CTA's entries; P -> f16 core-matrix tile [head][entry]
     {
-        const int h = tid >> 2, part = tid & 3;
-        float z[32];
+        const int h = tid >> 3, part = tid & 7;   // 8 threads per head, entries 8 i + part
+        float z[16];
         float mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            z[i] = sT[h * ST_STRIDE + 4 * i + part];
+        for (int i = 0; i < 16; ++i) {
+            z[i] = sT[h * ST_STRIDE + 8 * i + part];
             mx = fmaxf(mx, z[i]);
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
         float sum = 0.f;
-        uint8_t *pdst = sP + (h >> 3) * P_SBO + (h & 7) * 16;
+        uint8_t *pdst = sP + (h >> 3) * P_SBO + (h & 7) * 16 + part * 2;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int ee = 4 * i + part;
+        for (int i = 0; i < 16; ++i) {
             const float p = (mx == -INFINITY || z[i] == -INFINITY) ? 0.f : ex2(z[i] - mx);
             const __half ph = __float2half_rn(p);
             sum += __half2float(ph);
-            *reinterpret_cast<__half *>(pdst + (ee >> 3) * 128 + (ee & 7) * 2) = ph;
+            *reinterpret_cast<__half *>(pdst + i * 128) = ph;   // entry 8 i + part
         }
         sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
         sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
         if (part == 0) {
             sM[h] = mx;
             sL[h] = sum;
+            sIL[h] = sum > 0.f ? 1.f / sum : 0.f;
         }
     }
     tc::fence_async_smem();
@@ -355,7 +378,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     __syncthreads();
     tc::fence_after();
 
-    // ---- 5. O^T = Vhat^T . P^T  (4 blocks of M = 128 channels, N = 64 heads, K = 128 entries)
+    // ---- 5. O^T = Vhat^T . P^T  (4 blocks of M = 128 channels, N = 64 heads, K = 128 entries),
+    // one commit for all (a commit per block measured slower: it held back the next block)
+    const int W = DV / S;                      // channels per owner
+    const int bpo = W / 128;                   // blocks per owner
     if (tid == 0) {
         const uint32_t a0 = tc::smem_u32(sK), b0 = tc::smem_u32(sP);
         constexpr uint32_t idesc = tc::idesc_f16_f32(TM, HB, true, false);
@@ -366,62 +392,103 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
                             tc::desc_noswizzle(b0 + ks * 256, 128, P_SBO), idesc, ks > 0);
         tc::commit(bar_o);
     }
+    if (S > 1) {   // every CTA runs: publish this CTA's (max, sum) per head in every CTA of the cluster
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+        if (tid < HB)
+            for (int c = 0; c < S; ++c) {
+                float *st = cluster.map_shared_rank(sStats, c) + rank * 2 * HB;
+                st[tid] = sM[tid];
+                st[HB + tid] = sL[tid];
+            }
+    } else if (tid < HB) {
+        sStats[tid] = sM[tid];
+        sStats[HB + tid] = sL[tid];
+    }
     ok = tc::mbar_wait(bar_o, 0, MAX_POLLS) && ok;
-    pdl_launch_dependents();   // the next kernel may launch during the merge
+    pdl_launch_dependents();   // the next kernel may launch during the exchange
     tc::fence_after();
-    if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
 
-    // ---- 6. send raw O slices and (max, sum) to the owners of the channel slices
-    // Payload for owner o: [W channels][RS floats: 64 heads + pad] then 64 max + 64 sum.
-    // Slices for other CTAs are staged in this CTA's Q region and moved by the
-    // TMA engine (bulk shared -> remote shared copies completing on the owner's
-    // mbarrier); the own slice is written in place.
-    const int W = DV / S;                      // channels per owner
-    constexpr int RS = HB + 4;                 // floats per received channel row
-    const uint32_t slice_floats = (uint32_t)W * RS + 2 * HB;
-    const uint32_t slice_bytes = slice_floats * 4;
-    float *stage = reinterpret_cast<float *>(smem + OFF_Q);   // free after P V
-    const int nbuf = (2 * slice_bytes <= Q_BYTES) ? 2 : 1;    // staging buffers (2 when S = 4)
-    int sent = 0;
+    // ---- 6. stage normalised O slices (f16) and (max, sum) for the owners of the channel slices
+    // Payload for owner o: [W channels][RSH halves: 64 heads + pad] of O / L, then
+    // 64 max + 64 sum (fp32).  A slice owed to another CTA is staged in the Q
+    // region below P before the cluster barrier (overlapping the wait for the
+    // slowest CTA); after it the TMA engine copies the slices into the owners'
+    // shared memory (bulk shared -> remote shared, completing on the owner's
+    // mbarrier).  The own slice is written in place (the Khat tile is free).
+    const uint32_t slice_bytes = slice_bytes_for(W);
+    uint8_t *stage = smem + OFF_Q;             // sT is dead; P stays above the staging
+    uint8_t *recv = smem + OFF_K;              // received slices, by source rank
     if (tid == 0) asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_rx),
                                "r"((uint32_t)(S - 1) * slice_bytes) : "memory");
-    tc::fence_before();
-    cluster.sync();                            // every CTA finished with its Khat tile
-    for (int o = 0; o < S; ++o) {
-        const int oo = (rank + 1 + o) % S;     // own slice last
-        float *dst = (oo == rank) ? sRecv + (size_t)rank * slice_floats : stage + (size_t)(sent % nbuf) * slice_floats;
-        if (oo != rank && sent >= nbuf) {
-            if (tid == 0) {                    // this staging buffer's previous copy has read it
-                if (nbuf == 2) bulk_wait_read1();
-                else bulk_wait_read0();
-            }
-            __syncthreads();
-        }
-        for (int mb = oo * W / 128; mb < (oo + 1) * W / 128; ++mb) {
-            uint32_t r[32];
-            tc::tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * HB + 32 * hh, r);
-            tc::tmem_ld_wait();
-            float *row = dst + (size_t)(mb * 128 - oo * W + 32 * quarter + lane) * RS + 32 * hh;
+    float il[16];                               // 1 / L of this thread's 16 heads
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-                *reinterpret_cast<uint4 *>(row + 4 * q4) = make_uint4(r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
+    for (int jj = 0; jj < 16; ++jj) il[jj] = sIL[16 * hh + jj];
+    // slice o of the sending order (own slice last): stage it, and for another
+    // CTA's slice copy it once the cluster barrier has passed
+    auto stage_slice = [&](int o) {
+        const int oo = (rank + 1 + o) % S;
+        uint8_t *dst = (oo == rank) ? recv + (size_t)rank * slice_bytes : stage + (size_t)o * slice_bytes;
+        for (int bi = 0; bi < bpo; ++bi) {
+            const int mb = oo * bpo + bi;
+            uint32_t r[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * HB + 16 * hh, r);
+            tc::tmem_ld_wait();
+            uint8_t *row = dst + (size_t)(bi * 128 + 32 * quarter + lane) * (RSH * 2) + 32 * hh;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                *reinterpret_cast<uint2 *>(row + 8 * q4) =
+                    make_uint2(pack_f16x2(__uint_as_float(r[4 * q4]) * il[4 * q4], __uint_as_float(r[4 * q4 + 1]) * il[4 * q4 + 1]),
+                               pack_f16x2(__uint_as_float(r[4 * q4 + 2]) * il[4 * q4 + 2], __uint_as_float(r[4 * q4 + 3]) * il[4 * q4 + 3]));
         }
-        if (tid < HB) {
-            dst[(size_t)W * RS + tid] = sM[tid];
-            dst[(size_t)W * RS + HB + tid] = sL[tid];
+    };
+    auto send_slice = [&](int o) {   // one thread; the slice's staging writes are fenced and synced
+        const int oo = (rank + 1 + o) % S;
+        uint32_t rdst, rbar;
+        const uint32_t ldst = tc::smem_u32(recv + (size_t)rank * slice_bytes);
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rdst) : "r"(ldst), "r"((uint32_t)oo));
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar_rx), "r"((uint32_t)oo));
+        bulk_s2s(rdst, tc::smem_u32(stage + (size_t)o * slice_bytes), slice_bytes, rbar);
+        bulk_commit();
+    };
+    if (S > 1) stage_slice(0);                 // overlaps the wait for the slowest CTA
+    if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
+    tc::fence_async_smem();
+    tc::fence_before();
+    cluster.sync();                            // every CTA's P V is done: its Khat region may be written
+    if (S > 1 && tid == 0) send_slice(0);
+    // combine weights L_c 2^(m_c - M) / sum_c' L_c' 2^(m_c' - M) from every CTA's (max, sum)
+    if (tid < HB) {
+        float mc[MAX_S], lc[MAX_S];
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < MAX_S; ++c) {
+            if (c < S) {
+                mc[c] = sStats[c * 2 * HB + tid];
+                lc[c] = sStats[c * 2 * HB + HB + tid];
+                M = fmaxf(M, mc[c]);
+            }
         }
-        if (oo != rank) {
+        float L = 0.f;
+#pragma unroll
+        for (int c = 0; c < MAX_S; ++c) {
+            if (c < S) {
+                const float wc = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : lc[c] * ex2(mc[c] - M);
+                sW[c * HB + tid] = wc;
+                L += wc;
+            }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int c = 0; c < MAX_S; ++c)
+            if (c < S) sW[c * HB + tid] *= inv;
+        sLse[tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
+    for (int o = (S > 1 ? 1 : 0); o < S; ++o) {
+        stage_slice(o);
+        if (o + 1 < S) {
             tc::fence_async_smem();
             __syncthreads();
-            if (tid == 0) {
-                uint32_t rdst, rbar;
-                const uint32_t ldst = tc::smem_u32(sRecv + (size_t)rank * slice_floats);
-                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rdst) : "r"(ldst), "r"((uint32_t)oo));
-                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar_rx), "r"((uint32_t)oo));
-                bulk_s2s(rdst, tc::smem_u32(dst), slice_bytes, rbar);
-                bulk_commit();
-            }
-            ++sent;
+            if (tid == 0) send_slice(o);
         }
     }
     if (tid == 0) bulk_wait_read0();           // staging reads done before this CTA may exit
@@ -429,39 +496,35 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     __syncthreads();
     if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
 
-    // ---- 7. combine this CTA's channel slice: weights 2^(m_c - M) / L per head
-    if (tid < HB) {
-        float M = -INFINITY;
-        for (int c = 0; c < S; ++c) M = fmaxf(M, sRecv[(size_t)c * slice_floats + W * RS + tid]);
-        float L = 0.f;
-        for (int c = 0; c < S; ++c) {
-            const float mc = sRecv[(size_t)c * slice_floats + W * RS + tid];
-            const float wc = (M == -INFINITY || mc == -INFINITY) ? 0.f : ex2(mc - M);
-            sW[c * HB + tid] = wc;
-            L += wc * sRecv[(size_t)c * slice_floats + W * RS + HB + tid];
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        for (int c = 0; c < S; ++c) sW[c * HB + tid] *= inv;
-        sLse[tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
-    }
-    __syncthreads();
+    // ---- 7. combine this CTA's channel slice with the weights
     {
-        // thread -> (4 heads, channel): lanes take consecutive channels, so each
-        // output store of a warp covers 32 consecutive channels of one head
+        // thread -> (8 heads, channel): lanes take consecutive channels (conflict-free
+        // 8-byte reads of the 136-byte rows; every output store of a warp covers 32
+        // consecutive channels of one head)
         const int c_lo = rank * W;
-        for (int t = tid; t < (HB / 4) * W; t += THREADS) {
-            const int h4 = t / W, c = t - h4 * W;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int src = 0; src < S; ++src) {
-                const float4 v = *reinterpret_cast<const float4 *>(sRecv + (size_t)src * slice_floats + (size_t)c * RS + 4 * h4);
-                const float *w = sW + src * HB + 4 * h4;
-                acc.x += w[0] * v.x; acc.y += w[1] * v.y; acc.z += w[2] * v.z; acc.w += w[3] * v.w;
+        const int wshift = S == 1 ? 9 : (S == 2 ? 8 : 7);   // log2 W
+        for (int t = tid; t < (HB / 8) * W; t += THREADS) {
+            const int h8 = t >> wshift, c = t & (W - 1);
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int src = 0; src < MAX_S; ++src) {
+                if (src < S) {
+                    const uint8_t *rp = recv + (size_t)src * slice_bytes + (size_t)c * (RSH * 2) + 16 * h8;
+                    const uint2 v0 = *reinterpret_cast<const uint2 *>(rp);
+                    const uint2 v1 = *reinterpret_cast<const uint2 *>(rp + 8);
+                    const float4 w0 = *reinterpret_cast<const float4 *>(sW + src * HB + 8 * h8);
+                    const float4 w1 = *reinterpret_cast<const float4 *>(sW + src * HB + 8 * h8 + 4);
+                    const float2 a01 = __half22float2(*reinterpret_cast<const __half2 *>(&v0.x));
+                    const float2 a23 = __half22float2(*reinterpret_cast<const __half2 *>(&v0.y));
+                    const float2 a45 = __half22float2(*reinterpret_cast<const __half2 *>(&v1.x));
+                    const float2 a67 = __half22float2(*reinterpret_cast<const __half2 *>(&v1.y));
+                    acc[0] += w0.x * a01.x; acc[1] += w0.y * a01.y; acc[2] += w0.z * a23.x; acc[3] += w0.w * a23.y;
+                    acc[4] += w1.x * a45.x; acc[5] += w1.y * a45.y; acc[6] += w1.z * a67.x; acc[7] += w1.w * a67.y;
+                }
             }
-            float *o = a.out + ((bt * a.H) + h0 + 4 * h4) * (int64_t)DV + c_lo + c;
-            o[0] = acc.x;
-            o[DV] = acc.y;
-            o[2 * DV] = acc.z;
-            o[3 * DV] = acc.w;
+            float *o = a.out + ((bt * a.H) + h0 + 8 * h8) * (int64_t)DV + c_lo + c;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i * DV] = acc[i];
         }
         if (rank == 0 && a.lse && tid < HB) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
     }
