@@ -45,6 +45,17 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
     }
 }
 
+// FP8 x FP8 -> fp32 tensor-core product, 16 keys x 8 columns x 32 d-values.
+// A registers: {row g, k 4t..4t+3}, {row g+8, same k}, {row g, k 16+4t..}, {row g+8, ...};
+// B registers: {k 4t..4t+3}, {k 16+4t..} of column g (g = lane / 4, t = lane % 4).
+__device__ __forceinline__ void mma_e4m3_16832(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // 16 consecutive d-values of one 64-wide row (FP8: 16 B; bf16: 32 B) ->
 // 8 packed 2-element registers: reg 2s = d(4s, 4s+1), reg 2s+1 = d(4s+2, 4s+3).
 template <bool FP8>
@@ -247,38 +258,40 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_decode_kernel(ScoreAr
                 for (int u = 0; u < NV; ++u) raw[c][r][u] = v[c][r] ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
             }
         }
+        // FP8: the raw 16 bytes of d-values 16 t4 .. 16 t4 + 15 (head g < 4; columns 4-7 zero)
+        // feed two k32 MMAs directly, the same d-permutation on keys and query;
+        // bf16: converted fragments for four k16 MMAs
         uint32_t qf[8];
-        load_row16<FP8>(a.q + ((row * 4 + (g & 3)) * 64 + 16 * t4) * ES, (g >> 2) == 0, qf);
+        uint4 q8 = make_uint4(0, 0, 0, 0);
+        if constexpr (FP8) {
+            if ((g >> 2) == 0) q8 = __ldg(reinterpret_cast<const uint4 *>(a.q + (row * 4 + g) * 64 + 16 * t4));
+        } else {
+            load_row16<FP8>(a.q + ((row * 4 + (g & 3)) * 64 + 16 * t4) * ES, (g >> 2) == 0, qf);
+        }
         const float w0 = (t4 < 2) ? a.w[row * 4 + 2 * t4] : 0.f;
         const float w1 = (t4 < 2) ? a.w[row * 4 + 2 * t4 + 1] : 0.f;
         float *out = a.scores + row * M;
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
-            uint32_t ka[8], kb[8];
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (FP8) {
-                const uint32_t wa[4] = {raw[c][0][0].x, raw[c][0][0].y, raw[c][0][0].z, raw[c][0][0].w};
-                const uint32_t wb[4] = {raw[c][1][0].x, raw[c][1][0].y, raw[c][1][0].z, raw[c][1][0].w};
-#pragma unroll
-                for (int s2 = 0; s2 < 4; ++s2) {
-                    ka[2 * s2] = e4m3x2_to_f16x2(wa[s2] & 0xFFFFu);
-                    ka[2 * s2 + 1] = e4m3x2_to_f16x2(wa[s2] >> 16);
-                    kb[2 * s2] = e4m3x2_to_f16x2(wb[s2] & 0xFFFFu);
-                    kb[2 * s2 + 1] = e4m3x2_to_f16x2(wb[s2] >> 16);
-                }
+                const uint4 ra = raw[c][0][0], rb = raw[c][1][0];   // keys g and g + 8
+                mma_e4m3_16832(acc, ra.x, rb.x, ra.y, rb.y, q8.x, q8.y);
+                mma_e4m3_16832(acc, ra.z, rb.z, ra.w, rb.w, q8.z, q8.w);
             } else {
+                uint32_t ka[8], kb[8];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     uint32_t *d = r ? kb : ka;
                     d[0] = raw[c][r][0].x; d[1] = raw[c][r][0].y; d[2] = raw[c][r][0].z; d[3] = raw[c][r][0].w;
                     d[4] = raw[c][r][NV - 1].x; d[5] = raw[c][r][NV - 1].y; d[6] = raw[c][r][NV - 1].z; d[7] = raw[c][r][NV - 1].w;
                 }
-            }
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int s2 = 0; s2 < 4; ++s2) {
-                const uint32_t af[4] = {ka[2 * s2], kb[2 * s2], ka[2 * s2 + 1], kb[2 * s2 + 1]};
-                const uint32_t bf[2] = {qf[2 * s2], qf[2 * s2 + 1]};
-                mma16816<FP8>(acc, af, bf);
+                for (int s2 = 0; s2 < 4; ++s2) {
+                    const uint32_t af[4] = {ka[2 * s2], kb[2 * s2], ka[2 * s2 + 1], kb[2 * s2 + 1]};
+                    const uint32_t bf[2] = {qf[2 * s2], qf[2 * s2 + 1]};
+                    mma16816<FP8>(acc, af, bf);
+                }
             }
             float s0 = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);
             float s1 = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);
