@@ -66,6 +66,31 @@ def _dist():
     return world, rank, local
 
 
+def _rank_seed(rank, r):
+    """Seed of input set r on `rank`: every rank serves its own sequences, so
+    the work per GPU is fixed as ranks are added (weak scaling)."""
+    return 1 + 1000 * rank + 17 * r
+
+
+def _max_over_ranks(sec, device=None):
+    """The slowest rank's seconds, on every rank (the job ends with it); the
+    value itself with one rank or no process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(sec)
+    dev = device if (device is not None and dist.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([float(sec)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_rate(units_per_rank_step, steps, world, sec):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time."""
+    return units_per_rank_step * steps * world / sec
+
+
 class ClockSampler:
     """nvidia-smi clocks/throttle sampling in the background (100 ms)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -352,7 +377,7 @@ def run_gpu(args):
     steps = []
     for r in range(ROTATE):
         st = DecoderStep(StepShape(B=B, N=NCAP, D=D, dv=DV, H=H, K=K, P=P), device=dev)
-        _fill_instance(st, seed=1 + 1000 * rank + 17 * r)
+        _fill_instance(st, seed=_rank_seed(rank, r))
         steps.append(st)
     stream = torch.cuda.Stream(device=dev)
     # warm the library (attributes, module load) eagerly, then capture one graph per input set
@@ -396,15 +421,10 @@ def run_gpu(args):
     barrier()
     time.sleep(0.15)
     clocks.stop()
-    sec = e0.elapsed_time(e1) * 1e-3
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([sec], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        sec = float(tt.item())
+    sec = _max_over_ranks(e0.elapsed_time(e1) * 1e-3, dev)
     st0 = steps[0]
     tl = st0.token_layers
-    value = tl * args.steps * world / sec
+    value = _job_rate(tl, args.steps, world, sec)
     errs = [int(s.err.item()) for s in steps]
 
     # ---- end to end through the public API with pinned host buffers
@@ -431,13 +451,8 @@ def run_gpu(args):
             host_lse.copy_(st.lse[-1], non_blocking=True)
         f1.record(stream)
     torch.cuda.synchronize()
-    e2e_sec = f0.elapsed_time(f1) * 1e-3
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_sec], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_sec = float(tt.item())
-    e2e_value = tl * e2e_steps * world / e2e_sec
+    e2e_sec = _max_over_ranks(f0.elapsed_time(f1) * 1e-3, dev)
+    e2e_value = _job_rate(tl, e2e_steps, world, e2e_sec)
 
     # ---- per-kernel durations (events around each call, eager steps on the same stream)
     brk = _kernel_breakdown(steps, stream, rounds=max(40, min(args.steps, 400)))

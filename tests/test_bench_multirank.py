@@ -1,0 +1,86 @@
+"""Host logic of the benchmark's multi-rank mode, on CPU with gloo.
+
+bench.py under torchrun runs one replica per GPU (the decode path shards by
+sequence and has no exchange step): every rank draws its own sequences, times
+its own steps, and the job's time is the slowest rank's.  These tests run
+that logic with two gloo ranks on the CPU; no GPU and no CUDA call is made.
+"""
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, secs, out_dir):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port),
+                       "RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w, r, _ = bench._dist()
+        assert (w, r) == (world, rank)
+        dist.barrier()
+        slowest = bench._max_over_ranks(secs[rank])
+        rate = bench._job_rate(640, 10, w, slowest)
+        # the second reduction must see the same answer on every rank
+        again = bench._max_over_ranks(slowest)
+        with open(os.path.join(out_dir, "rank%d.txt" % rank), "w") as f:
+            f.write("%r %r %r\n" % (slowest, rate, again))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_rate_gloo_two_ranks(tmp_path):
+    world = 2
+    secs = [0.25, 0.4]   # rank 1 is slower: the job takes its time
+    mp.start_processes(_rank_main, args=(world, _free_port(), secs, str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    got = []
+    for r in range(world):
+        slowest, rate, again = (float(x) for x in open(tmp_path / ("rank%d.txt" % r)).read().split())
+        got.append((slowest, rate, again))
+    for slowest, rate, again in got:
+        assert slowest == pytest.approx(0.4)
+        assert again == pytest.approx(0.4)
+        # 640 token-layers per rank-step, 10 steps, both ranks' work over the slowest time
+        assert rate == pytest.approx(640 * 10 * world / 0.4)
+
+
+def test_single_process_is_identity():
+    assert not dist.is_initialized()
+    assert bench._max_over_ranks(0.123) == pytest.approx(0.123)
+    assert bench._job_rate(640, 10, 1, 0.5) == pytest.approx(12800.0)
+
+
+def test_rank_seeds_are_disjoint():
+    seeds = {(rank, r): bench._rank_seed(rank, r) for rank in range(8) for r in range(bench.ROTATE)}
+    assert len(set(seeds.values())) == len(seeds)
+    assert bench._rank_seed(0, 0) == 1   # rank 0's first input set is the single-GPU workload's seed
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+
+    class Args:
+        steps, warmup = 1, 3
+
+    # must return at once: no oracle build, no output
+    assert bench.run_reference(Args()) is None
+    assert capsys.readouterr().out == ""
