@@ -10,23 +10,25 @@
 //
 // Layout of the work.  A thread-block cluster of S in {1, 2, 4} CTAs serves
 // one query token and 64 heads; CTA c owns selected entries [128c, 128c+128).
+// 512 threads: four per entry (144 channels each) and eight per head.
 //  1. The TMA engine gathers the operands: one bulk copy per Q head row
-//     (1152 B) and one per selected entry's code row (288 B), completing on
-//     one mbarrier; the 36-byte scale rows (not 16-byte sized) are plain loads.
+//     (1152 B, on its own mbarrier) and one per selected entry's code row
+//     (288 B); the 36-byte scale rows (not 16-byte sized) are plain loads.
 //  2. Q (bf16) is scaled per head by a power of two into f16 (exact; the scale
-//     is folded into the logit factor); the entries are dequantised once
-//     (E2M1 x E4M3 -> exact f16) into a no-swizzle core-matrix tile.
+//     is folded into the logit factor) while the code rows are in flight; the
+//     entries are dequantised once (E2M1 x E4M3 -> exact f16) into a
+//     no-swizzle core-matrix tile.
 //  3. S^T [128 entries x 64 heads] = Khat . Q^T  (36 tcgen05.mma, M128 N64 K16)
 //  4. softmax on a transposed copy of S^T in shared memory; P -> f16.
 //  5. O^T [512 ch x 64 heads] = Vhat^T . P^T  (4 x 8 MMAs; the same Khat bytes
 //     read MN-major), fp32 accumulators in TMEM.
-//  6. Merge across the cluster: every CTA stages the raw O slice and the
-//     per-head (max, sum) owed to each other CTA in its own shared memory and
-//     the TMA engine copies it into the owner's shared memory (bulk
-//     shared -> remote shared copies completing on the owner's mbarrier; this
-//     measured ~2x faster than per-thread remote stores and than a merge
-//     through L2); each owner then combines its channel slice with weights
-//     2^(m_c - M) / L and writes it out.
+//  6. Merge across the cluster: every CTA pushes its per-head (max, sum) into
+//     every CTA's shared memory, normalises its partial O by the sum and
+//     stages each other CTA's 128-channel slice as f16 below the P tile; after
+//     one cluster barrier the TMA engine copies the slices into the owners'
+//     shared memory (bulk shared -> remote shared copies completing on the
+//     owner's mbarrier).  Each owner combines its slice with the weights
+//     L_c 2^(m_c - M) / sum_c' L_c' 2^(m_c' - M) and writes it out.
 // Waits on the mbarriers are bounded; on timeout the kernel sets
 // CSA2_FLAG_TIMEOUT and still runs every cluster barrier, so it always ends.
 #include <cooperative_groups.h>
