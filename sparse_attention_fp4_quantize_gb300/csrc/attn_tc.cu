@@ -228,14 +228,15 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         if (valid)
             bulk_g2s(tc::smem_u32(smem + OFF_CRAW + e * CRAW_STRIDE), a.codes + (b * a.N + j) * (D / 2), D / 2, bar_ld);
     }
-    // scale bytes 9 qt .. 9 qt + 8 of the entry's 36: words 2 qt .. 2 qt + 2, shifted by qt bytes
-    // (consumed only by the dequantiser, so their latency overlaps the Q conversion)
-    uint32_t sw0 = 0, sw1 = 0, sw2 = 0;
+    // the entry's 36 scale bytes as 9 words (consumed only by the dequantiser, so
+    // their latency overlaps the Q conversion)
+    uint32_t sw[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) sw[i] = 0u;
     if (valid) {
-        const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + (b * a.N + j) * (D / 16)) + 2 * qt;
-        sw0 = __ldg(srow);
-        sw1 = __ldg(srow + 1);
-        sw2 = __ldg(srow + 2);
+        const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + (b * a.N + j) * (D / 16));
+#pragma unroll
+        for (int i = 0; i < 9; ++i) sw[i] = __ldg(srow + i);
     }
     bool ok = tc::mbar_wait(bar_q, 0, MAX_POLLS);   // Q first: its conversion overlaps the code copies
 
@@ -280,49 +281,74 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
     }
     // ---- 2b. staged codes -> registers (the Khat tile overwrites the staging area)
+    // The 36 16-channel groups of an entry are dequantised in two halves (groups
+    // 0-17, then 18-35) so that the S MMAs of the first half run while the
+    // second half is dequantised.  In half h the thread takes local groups
+    // qh, qh + 4, ... (< 18) with qh = (qt + 2h) mod 4: nine groups in all.
     ok = tc::mbar_wait(bar_ld, 0, MAX_POLLS) && ok;
-    uint2 cw[9];   // chunk pairs: 8 channels per word, one 16-channel scale group per pair
+    uint2 cw[2][5];   // per half: up to five groups, 8 code bytes (16 channels) each
     {
-        const uint8_t *craw = smem + OFF_CRAW + e * CRAW_STRIDE + qt * 72;
+        const uint8_t *craw = smem + OFF_CRAW + e * CRAW_STRIDE;
 #pragma unroll
-        for (int i = 0; i < 9; ++i) cw[i] = valid ? *reinterpret_cast<const uint2 *>(craw + 8 * i) : make_uint2(0, 0);
-    }
-    __syncthreads();
-    // ---- 2c. dequantise this thread's 144 channels of its entry into the Khat tile
-    {
-        uint8_t *kdst = sK + (e >> 3) * KT_SBO + (e & 7) * 16 + qt * 18 * 128;
-        const uint32_t s0 = __funnelshift_r(sw0, sw1, 8 * qt), s1 = __funnelshift_r(sw1, sw2, 8 * qt);
-        const uint32_t s2 = sw2 >> (8 * qt);
+        for (int h = 0; h < 2; ++h) {
+            const int qh = (qt + 2 * h) & 3, nh = qh < 2 ? 5 : 4;
 #pragma unroll
-        for (int i = 0; i < 9; ++i) {
-            uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (valid) {
-                const uint32_t sb = ((i < 4 ? s0 : (i < 8 ? s1 : s2)) >> (8 * (i & 3))) & 0xFFu;
-                const uint32_t sc = e4m3_to_f16x2_bcast(sb);
-#pragma unroll
-                for (int bb = 0; bb < 4; ++bb) {
-                    r[bb] = hmul2(e2m1x2_to_f16x2((cw[i].x >> (8 * bb)) & 0xFF), sc);
-                    r[4 + bb] = hmul2(e2m1x2_to_f16x2((cw[i].y >> (8 * bb)) & 0xFF), sc);
-                }
-            }
-            *reinterpret_cast<uint4 *>(kdst + (2 * i) * 128) = make_uint4(r[0], r[1], r[2], r[3]);
-            *reinterpret_cast<uint4 *>(kdst + (2 * i + 1) * 128) = make_uint4(r[4], r[5], r[6], r[7]);
+            for (int i = 0; i < 5; ++i)
+                cw[h][i] = (valid && i < nh) ? *reinterpret_cast<const uint2 *>(craw + 8 * (18 * h + qh + 4 * i))
+                                              : make_uint2(0, 0);
         }
     }
+    __syncthreads();
+    // ---- 2c. dequantise one half of this thread's groups into the Khat tile
+    auto dequant_half = [&](const int h) {
+        const int qh = (qt + 2 * h) & 3, nh = qh < 2 ? 5 : 4;
+        uint8_t *kbase = sK + (e >> 3) * KT_SBO + (e & 7) * 16;
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            if (i < nh) {
+                const int g = 18 * h + qh + 4 * i;   // group of the entry
+                // scale byte g: word g / 4, byte g % 4 (compile-time word choice by a select)
+                const uint32_t word = h == 0 ? sw[i] : ((qh >> 1) ? sw[i < 4 ? 5 + i : 8] : sw[4 + i]);
+                const int byte = h == 0 ? qh : ((2 + qh) & 3);
+                uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                if (valid) {
+                    const uint32_t sc = e4m3_to_f16x2_bcast((word >> (8 * byte)) & 0xFFu);
+#pragma unroll
+                    for (int bb = 0; bb < 4; ++bb) {
+                        r[bb] = hmul2(e2m1x2_to_f16x2((cw[h][i].x >> (8 * bb)) & 0xFF), sc);
+                        r[4 + bb] = hmul2(e2m1x2_to_f16x2((cw[h][i].y >> (8 * bb)) & 0xFF), sc);
+                    }
+                }
+                *reinterpret_cast<uint4 *>(kbase + (2 * g) * 128) = make_uint4(r[0], r[1], r[2], r[3]);
+                *reinterpret_cast<uint4 *>(kbase + (2 * g + 1) * 128) = make_uint4(r[4], r[5], r[6], r[7]);
+            }
+        }
+    };
+    // ---- 3. S^T = Khat . Q^T  (M = 128 entries, N = 64 heads, K = 576): 18 k-steps per half
+    const uint32_t a0s = tc::smem_u32(sK), b0s = tc::smem_u32(sQ);
+    constexpr uint32_t idesc_s = tc::idesc_f16_f32(TM, HB, false, false);
+    dequant_half(0);
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    // ---- 3. S^T = Khat . Q^T  (M = 128 entries, N = 64 heads, K = 576)
     if (tid == 0) {
-        const uint32_t a0 = tc::smem_u32(sK), b0 = tc::smem_u32(sQ);
-        constexpr uint32_t idesc = tc::idesc_f16_f32(TM, HB, false, false);
-#pragma unroll 4
-        for (int ks = 0; ks < D / 16; ++ks)
-            tc::mma_f16(tmem + S_COL, tc::desc_noswizzle(a0 + ks * 256, 128, KT_SBO),
-                        tc::desc_noswizzle(b0 + ks * 256, 128, Q_SBO), idesc, ks > 0);
+#pragma unroll 2
+        for (int ks = 0; ks < D / 32; ++ks)
+            tc::mma_f16(tmem + S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
+                        tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, ks > 0);
+    }
+    dequant_half(1);
+    tc::fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (tid == 0) {
+#pragma unroll 2
+        for (int ks = D / 32; ks < D / 16; ++ks)
+            tc::mma_f16(tmem + S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
+                        tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, true);
         tc::commit(bar_s);
     }
     ok = tc::mbar_wait(bar_s, 0, MAX_POLLS) && ok;
