@@ -360,6 +360,28 @@ def _extra_workloads(dev, stream, peak_gbs):
     res["pool_build_b8_n262144"] = {"us": t * 1e6, "score_bytes_read": w3.B * w3.N * 4}
     del planes, qs, outs3, k3, full3
     torch.cuda.empty_cache()
+    # attention alone at larger token counts (T=1 decode tokens, H=64, Top-512 of 16384 entries):
+    # the same kernel once the launch holds more than one token per SM group; two
+    # rotating input sets whose gathered rows exceed L2
+    for nb in (128, 512):
+        wa = gen.scaled(gen.FULL_BATCHED_DECODE, B=nb)
+        kla = torch.full((nb,), 16384, dtype=torch.int32, device=dev)
+        sets = []
+        for r_ in range(2):
+            codes, scales = gen.fp4_planes(wa.seed, 60 + r_, nb * 16384, 576, device=dev)
+            qa = gen.normal_bf16(wa.seed, 70 + r_, (nb, 1, 64, 576), device=dev)
+            ia = torch.randint(0, 16384, (nb, 1, 512), generator=torch.Generator(device=dev).manual_seed(80 + r_),
+                               device=dev, dtype=torch.int32)
+            oa = torch.empty(nb, 1, 64, 512, device=dev)
+            sets.append((codes, scales, qa, ia, oa))
+        t = _time_graph(lambda: [csa2.csa2_sparse_attn_fp4(2, qa_, c_, s_, 16384, ia_, oa_, 1 / 24.0, kv_len=kla,
+                                                           stream=stream)
+                                 for c_, s_, qa_, ia_, oa_ in sets], stream, 20) / 2
+        ab = nb * 512 * 324 + nb * 64 * 512 * 4
+        res["attention_b%d" % nb] = {"us": t * 1e6, "algorithmic_bytes": ab, "gbs": ab / t / 1e9,
+                                     "hbm_frac": ab / t / 1e9 / peak_gbs}
+        del sets
+        torch.cuda.empty_cache()
     return res
 
 

@@ -37,7 +37,7 @@ constexpr int kCoarse = 64;    // coarse bin = 32 fine bins
 constexpr int kDigits = 3;     // bits 31..21, 20..10, 9..0
 constexpr int kMaxCluster = 8;
 constexpr int kMaxKeysPerCta = 49152;  // 192 KB of keys
-constexpr int kSmemCap = 198 * 1024;   // dynamic shared memory ceiling (static use is ~26 KB)
+constexpr int kSmemCap = 192 * 1024;   // dynamic shared memory ceiling (static use is ~33 KB)
 static_assert(kBins == 4 * kThreads, "each thread owns one uint4 of fine bins");
 static_assert(kCoarse == kThreads / 8, "eight threads make one coarse bin");
 static_assert(kWarps <= 32, "one lane per warp in the count exchange");
@@ -78,15 +78,16 @@ struct Boundary {
 
 // The bin b of the cluster-wide histogram with S(b) >= kk > S(b+1), where S(b)
 // counts the keys in bins >= b; computed by one warp on its own.
+// `coarse` holds every CTA's coarse bins ([C][64], pushed here before the
+// cluster barrier); the fine bins are read from each CTA.
 template <int C>
 __device__ __forceinline__ Boundary find_boundary(cg::cluster_group &cluster, const uint32_t *fine,
-                                                  const uint32_t *coarse, uint32_t kk) {
+                                                  const uint32_t (*coarse)[kCoarse], uint32_t kk) {
     const int lane = threadIdx.x & 31;
     uint2 cs = make_uint2(0u, 0u);
 #pragma unroll
     for (int c = 0; c < C; ++c) {
-        const uint32_t *rc = C > 1 ? cluster.map_shared_rank(coarse, c) : coarse;
-        const uint2 v = reinterpret_cast<const uint2 *>(rc)[lane];
+        const uint2 v = reinterpret_cast<const uint2 *>(coarse[c])[lane];
         cs.x += v.x;
         cs.y += v.y;
     }
@@ -119,8 +120,8 @@ template <int C>
 __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
     extern __shared__ __align__(16) uint32_t keys[];          // this CTA's slice (+ zero padding to 4)
     __shared__ __align__(16) uint32_t fine[kDigits][kBins];   // this CTA's histogram of each digit
-    __shared__ __align__(16) uint32_t coarse[kDigits][kCoarse];
-    __shared__ uint32_t wcnt[2][32];                          // per-warp (greater, equal) counts
+    __shared__ __align__(16) uint32_t coarse[kDigits][C][kCoarse];   // every CTA's coarse bins, pushed
+    __shared__ uint32_t wcnt[C][2][kWarps];                   // every CTA's per-warp (greater, equal) counts
 
     cg::cluster_group cluster = cg::this_cluster();
     const int cta = C > 1 ? (int)cluster.block_rank() : 0;
@@ -138,7 +139,9 @@ __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
     const int nm4 = (nm + 3) >> 2;
 #pragma unroll
     for (int d = 0; d < kDigits; ++d) reinterpret_cast<uint4 *>(fine[d])[tid] = make_uint4(0u, 0u, 0u, 0u);
-    if (tid < kDigits * kCoarse) (&coarse[0][0])[tid] = 0u;
+    // cluster barrier, first half: this CTA runs (its shared memory may be written once
+    // every CTA has arrived: the wait follows the load)
+    if (C > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     pdl_wait();   // the set-up above overlaps the previous kernel's tail
 
     // ---------------------------------------------------------------- load
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
     }
     if (tid < 4 * nm4 - nm) keys[nm + tid] = 0u;  // pad to a multiple of 4 with the invalid key
     __syncthreads();
+    if (C > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
     // ---------------------------------------------------------------- cluster-wide radix select
     // Result: every key > T is selected, plus the first kk keys equal to T (T != 0).
@@ -212,21 +216,24 @@ __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
                 if (v.w != 0u && (v.w & pmask) == prefix) atomicAdd(&h[(v.w >> shift) & dmask], 1u);
             }
             __syncthreads();
-            {   // coarse bins: eight threads' fine bins each
+            {   // coarse bins (eight threads' fine bins each), pushed into every CTA
                 const uint4 q = reinterpret_cast<const uint4 *>(h)[tid];
                 uint32_t s = q.x + q.y + q.z + q.w;
                 s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
                 s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
                 s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
-                if ((tid & 7) == 0) coarse[d][tid >> 3] = s;
+                if ((tid & 7) == 0) {
+#pragma unroll
+                    for (int c = 0; c < C; ++c)
+                        *(C > 1 ? cluster.map_shared_rank(&coarse[d][cta][tid >> 3], c) : &coarse[d][cta][tid >> 3]) = s;
+                }
             }
             if (C > 1) cluster.sync(); else __syncthreads();  // every slice's histograms are complete
             if (d == 0) {  // at most K valid keys: take them all
                 uint32_t tot = 0u;
 #pragma unroll
                 for (int c = 0; c < C; ++c) {
-                    const uint32_t *rc = C > 1 ? cluster.map_shared_rank(coarse[0], c) : coarse[0];
-                    const uint2 v = reinterpret_cast<const uint2 *>(rc)[lane];
+                    const uint2 v = reinterpret_cast<const uint2 *>(coarse[0][c])[lane];
                     tot += v.x + v.y;
                 }
                 if (__reduce_add_sync(0xFFFFFFFFu, tot) <= (uint32_t)K) {
@@ -260,23 +267,27 @@ __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
         gt += __popc(__ballot_sync(0xFFFFFFFFu, k > T));
         eq += __popc(__ballot_sync(0xFFFFFFFFu, T != 0u && k == T));
     }
-    if (lane == 0) {
-        wcnt[0][warp] = gt;
-        wcnt[1][warp] = eq;
+    if (lane == 0) {   // publish this warp's counts in every CTA
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            uint32_t *dst = C > 1 ? cluster.map_shared_rank(&wcnt[cta][0][warp], c) : &wcnt[cta][0][warp];
+            dst[0] = gt;
+            dst[kWarps] = eq;
+        }
     }
-    if (C > 1) cluster.sync(); else __syncthreads();  // every warp's counts are published
+    // every warp's counts are in place; and after this barrier no CTA reads another's
+    // shared memory, so each may leave when done
+    if (C > 1) cluster.sync(); else __syncthreads();
     uint32_t bg = 0u, be_ = 0u, tg = 0u, te = 0u;     // (before this warp, in the row) counts
 #pragma unroll
     for (int c = 0; c < C; ++c) {
-        const uint32_t(*rc)[32] = C > 1 ? cluster.map_shared_rank(wcnt, c) : wcnt;
-        const uint32_t vg = lane < kWarps ? rc[0][lane] : 0u, ve = lane < kWarps ? rc[1][lane] : 0u;
+        const uint32_t vg = lane < kWarps ? wcnt[c][0][lane] : 0u, ve = lane < kWarps ? wcnt[c][1][lane] : 0u;
         const bool before = c < cta || (c == cta && lane < warp);
         bg += before ? vg : 0u;
         be_ += before ? ve : 0u;
         tg += vg;
         te += ve;
     }
-    if (C > 1) cluster.barrier_arrive();  // this CTA's remote reads are done
     const uint32_t gt_before = __reduce_add_sync(0xFFFFFFFFu, bg), eq_before = __reduce_add_sync(0xFFFFFFFFu, be_);
     int32_t *orow = a.out + row * (int64_t)K;
     const uint32_t lt = (1u << lane) - 1u;
@@ -298,7 +309,6 @@ __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
         const int total = (int)(gt_total + min(kk, eq_total));
         for (int s2 = total + tid; s2 < K; s2 += kThreads) orow[s2] = -1;
     }
-    if (C > 1) cluster.barrier_wait();  // no CTA leaves while another may still read its counts
 }
 
 // Keys per CTA and dynamic shared memory for a split of the rows over C CTAs.
