@@ -44,7 +44,7 @@ def _workload_config(extra=None):
     cfg = {"workload": "csa2_decoder_step_b32_ctx32k-64k_n16384_d576_h64_top512_pool2048x8_20layers",
            "batch": B, "entries_cap": NCAP, "D": D, "dv": DV, "heads": H, "topk": K, "pool_blocks": P,
            "layers": LAYERS, "schedule": "1Full+3Reuse, 4x(1Reindex+3Reuse)", "kv": "FP4 E2M1 + E4M3/16, per layer",
-           "indexer": "FP8 E4M3 4x64", "l2": "4 rotating disjoint input sets, each step's working set > L2"}
+           "indexer": "FP8 E4M3 4x64, fused score->pool->Top-512 (scores stay on chip)", "l2": "4 rotating disjoint input sets, each step's working set > L2"}
     if extra:
         cfg.update(extra)
     return cfg
@@ -196,7 +196,7 @@ def _kernel_breakdown(steps, stream, rounds):
     import sparse_attention_fp4_quantize_gb300 as csa2
     import sparse_attention_fp4_quantize_gb300.decode as dec
     kinds = {"quantize": "csa2_quantize_kv_fp4", "index_score": "csa2_index_score", "build_pool": "csa2_build_pool",
-             "topk": "csa2_topk", "sparse_attn": "csa2_sparse_attn_fp4"}
+             "topk": "csa2_topk", "index_topk": "csa2_index_topk", "sparse_attn": "csa2_sparse_attn_fp4"}
     orig = {fn: getattr(dec, fn) for fn in kinds.values()}
     out = {}
     for kind, keep in kinds.items():
@@ -206,7 +206,7 @@ def _kernel_breakdown(steps, stream, rounds):
             def inner(*a, **kw):
                 if fn_name != keep:
                     return None
-                if fn_name in ("csa2_index_score", "csa2_topk") and a[0] == csa2.MODE_REUSE:
+                if fn_name in ("csa2_index_score", "csa2_topk", "csa2_index_topk") and a[0] == csa2.MODE_REUSE:
                     return fn(*a, **kw)          # no launch
                 count[0] += 1
                 return fn(*a, **kw)

@@ -161,13 +161,34 @@ size_t csa2_build_pool_workspace_bytes(int B, int T, int64_t N, int P);
  *        a selected l = 8p + i is written as 8*pool_blocks[b,t,p] + i.
  *        REUSE: returns CSA2_OK, idx untouched (the layer consumes its source
  *        layer's idx buffer).
- * idx    int32 [B, T, K], 1 <= K <= 2048.  M <= 524288.
+ * idx    int32 [B, T, K], 1 <= K <= 2048.  M <= 393216 (larger rows:
+ *        CSA2_ERR_UNSUPPORTED).
  * workspace: csa2_topk_workspace_bytes() bytes (currently 0; NULL ok).
  */
 csa2_status csa2_topk(csa2_mode mode, int B, int T, int64_t M, const float *scores,
                       const int32_t *kv_len, const int32_t *pool_blocks, int P, int K, int32_t *idx,
                       void *workspace, size_t ws_bytes, csa2_stream_t stream);
 size_t csa2_topk_workspace_bytes(int B, int T, int64_t M, int K);
+
+/*
+ * csa2_index_topk -- fused decode indexer: the result of csa2_index_score
+ * (same mode, FP8 E4M3 q_idx and k_idx only) followed by csa2_topk, and for
+ * FULL with pool_out also by csa2_build_pool (G = 8), without writing the
+ * scores out.  [ENG] Hierarchical Sparse Indexer and CSA2 section (score,
+ * pool, Top-512 per layer); the fusion itself is not on the pages.
+ *
+ * Arguments as in csa2_index_score and csa2_topk: q_idx [B, T, 4, 64],
+ * w fp32 [B, T, 4], k_idx [B, N, 64], kv_len int32 [B*T], REINDEX pool_blocks
+ * int32 [B, T, P]; idx int32 [B, T, K], 1 <= K <= 2048; FULL pool_out int32
+ * [B, T, P_out] or NULL, 1 <= P_out <= 2048.  Candidates per row (N for
+ * FULL, 8P for REINDEX) <= 349184 (larger rows: CSA2_ERR_UNSUPPORTED).  Selection rules, ties, -1 padding and the
+ * err_flag bits are those of the unfused calls.  bf16 indexer tensors:
+ * CSA2_ERR_INVALID_ARG (use the unfused calls).  REUSE: returns CSA2_OK.
+ */
+csa2_status csa2_index_topk(csa2_mode mode, int B, int T, int64_t N, const void *q_idx, csa2_dtype q_dt,
+                            const float *w, const void *k_idx, csa2_dtype k_dt, const int32_t *kv_len,
+                            const int32_t *pool_blocks, int P, int K, int32_t *idx, int32_t *pool_out,
+                            int P_out, uint32_t *err_flag, csa2_stream_t stream);
 
 /*
  * csa2_sparse_attn_fp4 -- attention of each query head over its selected FP4

@@ -7,7 +7,8 @@ pointers, shapes and the current CUDA stream to the C ABI declared in
 CPU fallback: if the shared library is missing the import fails loudly.
 
 Names follow the C ABI: ``csa2_quantize_kv_fp4``, ``csa2_index_score``,
-``csa2_build_pool``, ``csa2_topk``, ``csa2_sparse_attn_fp4`` and the
+``csa2_build_pool``, ``csa2_topk``, ``csa2_index_topk`` (fused decode indexer),
+``csa2_sparse_attn_fp4`` and the
 ``*_workspace_bytes`` helpers.
 """
 from __future__ import annotations
@@ -48,6 +49,7 @@ def _load() -> ctypes.CDLL:
         "csa2_build_pool_workspace_bytes": ([i32, i32, i64, i32], u64),
         "csa2_topk": ([i32, i32, i32, i64, P, P, P, i32, i32, P, P, u64, P], i32),
         "csa2_topk_workspace_bytes": ([i32, i32, i64, i32], u64),
+        "csa2_index_topk": ([i32, i32, i32, i64, P, i32, P, P, i32, P, P, i32, i32, P, P, i32, P, P], i32),
         "csa2_sparse_attn_fp4": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P, P,
                                   P, u64, P], i32),
         "csa2_sparse_attn_workspace_bytes": ([i32, i32, i32, i32, i32, i32], u64),
@@ -70,7 +72,7 @@ _lib = _load()
 
 def exported_symbols():
     return ["csa2_quantize_kv_fp4", "csa2_index_score", "csa2_build_pool", "csa2_build_pool_workspace_bytes",
-            "csa2_topk", "csa2_topk_workspace_bytes", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes",
+            "csa2_topk", "csa2_topk_workspace_bytes", "csa2_index_topk", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes",
             "csa2_sparse_attn_fp4_noalloc", "csa2_sparse_attn_noalloc_max_scratch_bytes",
             "csa2_status_string", "csa2_last_error", "csa2_version"]
 
@@ -150,6 +152,23 @@ def csa2_topk(mode, scores, idx, kv_len=None, pool_blocks=None, workspace=None, 
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.csa2_topk(int(mode), B, T, M, _ptr(scores), _ptr(kv_len), _ptr(pool_blocks), P, K, _ptr(idx),
                           _ptr(workspace), ws, _stream(stream)))
+
+
+def csa2_index_topk(mode, q_idx, w, k_idx, kv_len, idx, pool_blocks=None, pool_out=None, err_flag=None,
+                    stream=None):
+    """Fused decode indexer (FP8): the scores of csa2_index_score feed the
+    Top-K of csa2_topk (and, for FULL with pool_out, the pool of
+    csa2_build_pool) without being written out.  q_idx [B,T,4,64], w fp32
+    [B,T,4], k_idx [B,N,64], kv_len int32 [B*T] -> idx int32 [B,T,K]
+    (+ pool_out int32 [B,T,P_out])."""
+    _cuda(q_idx, w, k_idx, kv_len, idx, pool_blocks, pool_out, err_flag)
+    B, T = q_idx.shape[0], q_idx.shape[1]
+    N = k_idx.shape[1]
+    P = 0 if pool_blocks is None else pool_blocks.shape[-1]
+    P_out = 0 if pool_out is None else pool_out.shape[-1]
+    _check(_lib.csa2_index_topk(int(mode), B, T, N, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), _ptr(k_idx),
+                                _dtype_code(k_idx), _ptr(kv_len), _ptr(pool_blocks), P, idx.shape[-1], _ptr(idx),
+                                _ptr(pool_out), P_out, _ptr(err_flag), _stream(stream)))
 
 
 def csa2_sparse_attn_workspace_bytes(B, T, H, D, dv, K) -> int:

@@ -45,17 +45,6 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
     }
 }
 
-// FP8 x FP8 -> fp32 tensor-core product, 16 keys x 8 columns x 32 d-values.
-// A registers: {row g, k 4t..4t+3}, {row g+8, same k}, {row g, k 16+4t..}, {row g+8, ...};
-// B registers: {k 4t..4t+3}, {k 16+4t..} of column g (g = lane / 4, t = lane % 4).
-__device__ __forceinline__ void mma_e4m3_16832(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // 16 consecutive d-values of one 64-wide row (FP8: 16 B; bf16: 32 B) ->
 // 8 packed 2-element registers: reg 2s = d(4s, 4s+1), reg 2s+1 = d(4s+2, 4s+3).
 template <bool FP8>

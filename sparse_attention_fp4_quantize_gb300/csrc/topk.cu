@@ -116,17 +116,164 @@ __device__ __forceinline__ Boundary find_boundary(cg::cluster_group &cluster, co
     return r;
 }
 
+// Shared memory of the cluster-wide selection.
+template <int C>
+struct SelSmem {
+    uint32_t (*fine)[kBins];            // [kDigits][kBins] this CTA's histogram of each digit
+    uint32_t (*coarse)[C][kCoarse];     // [kDigits][C][kCoarse] every CTA's coarse bins, pushed
+    uint32_t (*wcnt)[2][kWarps];        // [C][2][kWarps] every CTA's per-warp (greater, equal) counts
+};
+
+// Cluster-wide radix select over every CTA's keys[0, 4 nm4) (zero-padded).  L
+// is the row's candidate count: with at most K of them every valid key is
+// taken.  Result: every key > T is selected, plus the first kk keys equal to
+// T (T != 0).  The fine histograms must be zero on entry; they are left
+// dirty (reset_fine before another selection).  Contains cluster barriers:
+// every thread of every CTA of the cluster calls it.
+template <int C>
+__device__ void cluster_select(cg::cluster_group &cluster, int cta, const SelSmem<C> &sm, const uint32_t *keys,
+                               int nm4, int64_t L, int K, uint32_t &T_out, uint32_t &kk_out) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    uint32_t T = 0u, kk = 0u;
+    if (L > K) {
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
+        uint32_t prefix = 0u, pmask = 0u;
+        kk = (uint32_t)K;
+#pragma unroll 1
+        for (int d = 0; d < kDigits; ++d) {
+            const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
+            const uint32_t dmask = d == 2 ? 0x3FFu : 0x7FFu;
+            uint32_t *h = sm.fine[d];
+#pragma unroll 4
+            for (int j = tid; j < nm4; j += kThreads) {
+                const uint4 v = k4[j];
+                if (v.x != 0u && (v.x & pmask) == prefix) atomicAdd(&h[(v.x >> shift) & dmask], 1u);
+                if (v.y != 0u && (v.y & pmask) == prefix) atomicAdd(&h[(v.y >> shift) & dmask], 1u);
+                if (v.z != 0u && (v.z & pmask) == prefix) atomicAdd(&h[(v.z >> shift) & dmask], 1u);
+                if (v.w != 0u && (v.w & pmask) == prefix) atomicAdd(&h[(v.w >> shift) & dmask], 1u);
+            }
+            __syncthreads();
+            {   // coarse bins (eight threads' fine bins each), pushed into every CTA
+                const uint4 q = reinterpret_cast<const uint4 *>(h)[tid];
+                uint32_t s = q.x + q.y + q.z + q.w;
+                s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+                s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+                s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
+                if ((tid & 7) == 0) {
+#pragma unroll
+                    for (int c = 0; c < C; ++c)
+                        *(C > 1 ? cluster.map_shared_rank(&sm.coarse[d][cta][tid >> 3], c) : &sm.coarse[d][cta][tid >> 3]) = s;
+                }
+            }
+            if (C > 1) cluster.sync(); else __syncthreads();  // every slice's histograms are complete
+            if (d == 0) {  // at most K valid keys: take them all
+                uint32_t tot = 0u;
+#pragma unroll
+                for (int c = 0; c < C; ++c) {
+                    const uint2 v = reinterpret_cast<const uint2 *>(sm.coarse[0][c])[lane];
+                    tot += v.x + v.y;
+                }
+                if (__reduce_add_sync(0xFFFFFFFFu, tot) <= (uint32_t)K) {
+                    kk = 0u;
+                    break;
+                }
+            }
+            const Boundary bd = find_boundary<C>(cluster, h, sm.coarse[d], kk);
+            kk -= bd.above;
+            prefix |= bd.bin << shift;
+            pmask |= dmask << shift;
+            if (bd.inbin == kk) {  // the boundary bin is taken whole: every key >= prefix
+                T = prefix - 1u;   // prefix >= 2^21 here: a bin that holds valid keys is never 0
+                kk = 0u;
+                break;
+            }
+            if (d == kDigits - 1) T = prefix;
+        }
+    }
+    T_out = T;
+    kk_out = kk;
+}
+
+// Zero the fine histograms for another selection (after a cluster barrier
+// that follows every CTA's last read of them); the caller syncs the CTA.
+template <int C>
+__device__ __forceinline__ void reset_fine(const SelSmem<C> &sm) {
+#pragma unroll
+    for (int d = 0; d < kDigits; ++d) reinterpret_cast<uint4 *>(sm.fine[d])[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Position-ordered compaction of the selection (T, kk) across the cluster:
+// orow[slot] = id(i) for every selected slice position i, slots in row
+// position order; the last CTA pads the row to K with -1.  Warp w owns a
+// contiguous run of the slice; ballots order its lanes.  One cluster barrier
+// (after it no CTA reads another's shared memory).
+template <int C, typename IdFn>
+__device__ void cluster_compact(cg::cluster_group &cluster, int cta, const SelSmem<C> &sm, const uint32_t *keys,
+                                int nm, uint32_t T, uint32_t kk, int K, int32_t *orow, IdFn id) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int R = (nm + kWarps - 1) / kWarps;
+    R = (R + 31) & ~31;
+    const int w0 = min(nm, warp * R), w1 = min(nm, w0 + R);
+    uint32_t gt = 0, eq = 0;
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const uint32_t k = i < w1 ? keys[i] : 0u;
+        gt += __popc(__ballot_sync(0xFFFFFFFFu, k > T));
+        eq += __popc(__ballot_sync(0xFFFFFFFFu, T != 0u && k == T));
+    }
+    if (lane == 0) {   // publish this warp's counts in every CTA
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            uint32_t *dst = C > 1 ? cluster.map_shared_rank(&sm.wcnt[cta][0][warp], c) : &sm.wcnt[cta][0][warp];
+            dst[0] = gt;
+            dst[kWarps] = eq;
+        }
+    }
+    if (C > 1) cluster.sync(); else __syncthreads();
+    uint32_t bg = 0u, be_ = 0u, tg = 0u, te = 0u;     // (before this warp, in the row) counts
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        const uint32_t vg = lane < kWarps ? sm.wcnt[c][0][lane] : 0u, ve = lane < kWarps ? sm.wcnt[c][1][lane] : 0u;
+        const bool before = c < cta || (c == cta && lane < warp);
+        bg += before ? vg : 0u;
+        be_ += before ? ve : 0u;
+        tg += vg;
+        te += ve;
+    }
+    const uint32_t gt_before = __reduce_add_sync(0xFFFFFFFFu, bg), eq_before = __reduce_add_sync(0xFFFFFFFFu, be_);
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t tie = eq_before;
+    uint32_t slot = gt_before + min(kk, tie);
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const uint32_t k = i < w1 ? keys[i] : 0u;
+        const bool is_eq = T != 0u && k == T;
+        const uint32_t bq = __ballot_sync(0xFFFFFFFFu, is_eq);
+        const bool take = k > T || (is_eq && tie + __popc(bq & lt) < kk);
+        const uint32_t bs = __ballot_sync(0xFFFFFFFFu, take);
+        if (take) orow[slot + __popc(bs & lt)] = id(i);
+        slot += __popc(bs);
+        tie += __popc(bq);
+    }
+    if (cta == C - 1) {
+        const uint32_t gt_total = __reduce_add_sync(0xFFFFFFFFu, tg), eq_total = __reduce_add_sync(0xFFFFFFFFu, te);
+        const int total = (int)(gt_total + min(kk, eq_total));
+        for (int s2 = total + tid; s2 < K; s2 += kThreads) orow[s2] = -1;
+    }
+}
+
 template <int C>
 __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
     extern __shared__ __align__(16) uint32_t keys[];          // this CTA's slice (+ zero padding to 4)
-    __shared__ __align__(16) uint32_t fine[kDigits][kBins];   // this CTA's histogram of each digit
-    __shared__ __align__(16) uint32_t coarse[kDigits][C][kCoarse];   // every CTA's coarse bins, pushed
-    __shared__ uint32_t wcnt[C][2][kWarps];                   // every CTA's per-warp (greater, equal) counts
+    __shared__ __align__(16) uint32_t fine[kDigits][kBins];
+    __shared__ __align__(16) uint32_t coarse[kDigits][C][kCoarse];
+    __shared__ uint32_t wcnt[C][2][kWarps];
+    const SelSmem<C> sm = {fine, coarse, wcnt};
 
     cg::cluster_group cluster = cg::this_cluster();
     const int cta = C > 1 ? (int)cluster.block_rank() : 0;
     const int64_t row = blockIdx.x / C;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int K = a.K;
     const int64_t beg = (int64_t)cta * a.chunk;
 
@@ -137,8 +284,7 @@ __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
     int nm = 0;
     if (beg < Mrow) nm = (int)((Mrow - beg) < a.chunk ? (Mrow - beg) : a.chunk);
     const int nm4 = (nm + 3) >> 2;
-#pragma unroll
-    for (int d = 0; d < kDigits; ++d) reinterpret_cast<uint4 *>(fine[d])[tid] = make_uint4(0u, 0u, 0u, 0u);
+    reset_fine(sm);
     // cluster barrier, first half: this CTA runs (its shared memory may be written once
     // every CTA has arrived: the wait follows the load)
     if (C > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -195,120 +341,154 @@ __global__ void __launch_bounds__(kThreads) topk_radix_kernel(TopkArgs a) {
     __syncthreads();
     if (C > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
-    // ---------------------------------------------------------------- cluster-wide radix select
-    // Result: every key > T is selected, plus the first kk keys equal to T (T != 0).
-    uint32_t T = 0u, kk = 0u;
-    if (L > K) {  // otherwise every valid key is selected
-        const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
-        uint32_t prefix = 0u, pmask = 0u;
-        kk = (uint32_t)K;
-#pragma unroll 1
-        for (int d = 0; d < kDigits; ++d) {
-            const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
-            const uint32_t dmask = d == 2 ? 0x3FFu : 0x7FFu;
-            uint32_t *h = fine[d];
-#pragma unroll 4
-            for (int j = tid; j < nm4; j += kThreads) {
-                const uint4 v = k4[j];
-                if (v.x != 0u && (v.x & pmask) == prefix) atomicAdd(&h[(v.x >> shift) & dmask], 1u);
-                if (v.y != 0u && (v.y & pmask) == prefix) atomicAdd(&h[(v.y >> shift) & dmask], 1u);
-                if (v.z != 0u && (v.z & pmask) == prefix) atomicAdd(&h[(v.z >> shift) & dmask], 1u);
-                if (v.w != 0u && (v.w & pmask) == prefix) atomicAdd(&h[(v.w >> shift) & dmask], 1u);
-            }
-            __syncthreads();
-            {   // coarse bins (eight threads' fine bins each), pushed into every CTA
-                const uint4 q = reinterpret_cast<const uint4 *>(h)[tid];
-                uint32_t s = q.x + q.y + q.z + q.w;
-                s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
-                s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
-                s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
-                if ((tid & 7) == 0) {
-#pragma unroll
-                    for (int c = 0; c < C; ++c)
-                        *(C > 1 ? cluster.map_shared_rank(&coarse[d][cta][tid >> 3], c) : &coarse[d][cta][tid >> 3]) = s;
+    uint32_t T, kk;
+    cluster_select<C>(cluster, cta, sm, keys, nm4, L, K, T, kk);
+    pdl_launch_dependents();   // the next kernel may launch during the compaction
+    cluster_compact<C>(cluster, cta, sm, keys, nm, T, kk, K, a.out + row * (int64_t)K,
+                       [&](int i) { return out_id(a, row, beg + i); });
+}
+
+// ---------------------------------------------------------------------------
+// Fused decode indexer: scores (FP8 keys and query, the same MMA tiling as the
+// decode scorer of csa2_index_score) go straight into the cluster's shared
+// memory as order-preserving keys, and the same cluster selection picks the
+// Top-K -- and for a Full layer optionally the pool of Top-P_out 8-position
+// blocks from the block maxima -- without writing the scores to HBM.
+struct FusedArgs {
+    int mode;
+    int64_t rows;             // B * T query rows
+    int T;
+    int64_t N;                // entries per sequence
+    int64_t M;                // candidates per row: N (Full) or 8 P (Reindex)
+    const uint8_t *q;         // FP8 [rows, 4, 64]
+    const float *w;           // [rows, 4]
+    const uint8_t *k;         // FP8 [B, N, 64]
+    const int32_t *kv_len;    // [rows]
+    const int32_t *pool_in;   // Reindex [rows, P]
+    int P;
+    int K;
+    int32_t *idx;             // [rows, K]
+    int32_t *pool_out;        // Full, optional [rows, P_out]
+    int P_out;
+    uint32_t *err_flag;
+    int chunk;                // candidates per CTA (multiple of 128)
+};
+
+template <int C>
+__global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
+    extern __shared__ __align__(16) uint32_t keys[];          // [chunk] scores as keys, then [chunk/8] block keys
+    __shared__ __align__(16) uint32_t fine[kDigits][kBins];
+    __shared__ __align__(16) uint32_t coarse[kDigits][C][kCoarse];
+    __shared__ uint32_t wcnt[C][2][kWarps];
+    const SelSmem<C> sm = {fine, coarse, wcnt};
+    uint32_t *bkeys = keys + a.chunk;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int cta = C > 1 ? (int)cluster.block_rank() : 0;
+    const int64_t row = blockIdx.x / C;
+    const int64_t b = row / a.T;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t4 = lane & 3;
+    const bool full = a.mode == CSA2_MODE_FULL;
+    const int64_t beg = (int64_t)cta * a.chunk;
+    int nm = 0;
+    if (beg < a.M) nm = (int)((a.M - beg) < a.chunk ? (a.M - beg) : a.chunk);
+    reset_fine(sm);
+    if (C > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    pdl_wait();
+
+    // ---------------------------------------------------------------- score this slice
+    int64_t len = a.kv_len[row];
+    len = len < a.N ? (len > 0 ? len : 0) : a.N;
+    const int64_t nblocks_n = (a.N + 7) / 8;
+    const uint4 q8 = (g < 4) ? __ldg(reinterpret_cast<const uint4 *>(a.q + (row * 4 + g) * 64 + 16 * t4))
+                             : make_uint4(0, 0, 0, 0);
+    const float w0 = (t4 < 2) ? a.w[row * 4 + 2 * t4] : 0.f;
+    const float w1 = (t4 < 2) ? a.w[row * 4 + 2 * t4 + 1] : 0.f;
+    const int nchunks = (nm + 127) / 128;
+    for (int cb = warp; cb < nchunks; cb += kWarps) {   // 8 groups of 16 candidates per warp chunk
+        const int i0 = cb * 128;
+        int32_t myblk = -1;
+        if (!full && lane < 16) {
+            const int64_t pidx = (beg + i0) / 8 + lane;
+            if (pidx < a.P) {
+                int64_t blk = a.pool_in[row * a.P + pidx];
+                if (blk < -1 || blk >= nblocks_n) {
+                    flag_error(a.err_flag, CSA2_FLAG_BAD_POOL);
+                    blk = -1;
                 }
+                myblk = (int32_t)blk;
             }
-            if (C > 1) cluster.sync(); else __syncthreads();  // every slice's histograms are complete
-            if (d == 0) {  // at most K valid keys: take them all
-                uint32_t tot = 0u;
-#pragma unroll
-                for (int c = 0; c < C; ++c) {
-                    const uint2 v = reinterpret_cast<const uint2 *>(coarse[0][c])[lane];
-                    tot += v.x + v.y;
-                }
-                if (__reduce_add_sync(0xFFFFFFFFu, tot) <= (uint32_t)K) {
-                    kk = 0u;
-                    break;
-                }
-            }
-            const Boundary bd = find_boundary<C>(cluster, h, coarse[d], kk);
-            kk -= bd.above;
-            prefix |= bd.bin << shift;
-            pmask |= dmask << shift;
-            if (bd.inbin == kk) {  // the boundary bin is taken whole: every key >= prefix
-                T = prefix - 1u;   // prefix >= 2^21 here: a bin that holds valid keys is never 0
-                kk = 0u;
-                break;
-            }
-            if (d == kDigits - 1) T = prefix;
         }
+        uint4 raw[8][2];
+        bool v[8][2];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int i = i0 + 16 * c + g + 8 * r;
+                int64_t j;
+                if (full) {
+                    j = beg + i;
+                } else {
+                    const int32_t blk = __shfl_sync(0xFFFFFFFFu, myblk, 2 * c + r);
+                    j = blk >= 0 ? (int64_t)blk * 8 + g : -1;
+                }
+                v[c][r] = i < nm && j >= 0 && j < len;
+                raw[c][r] = v[c][r] ? __ldg(reinterpret_cast<const uint4 *>(a.k + (b * a.N + j) * 64 + 16 * t4))
+                                    : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_e4m3_16832(acc, raw[c][0].x, raw[c][1].x, raw[c][0].y, raw[c][1].y, q8.x, q8.y);
+            mma_e4m3_16832(acc, raw[c][0].z, raw[c][1].z, raw[c][0].w, raw[c][1].w, q8.z, q8.w);
+            float s0 = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);
+            float s1 = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);
+            s0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
+            s1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
+            if (t4 == 0) {
+                keys[i0 + 16 * c + g] = v[c][0] ? score_key(s0) : 0u;
+                keys[i0 + 16 * c + g + 8] = v[c][1] ? score_key(s1) : 0u;
+            }
+        }
+    }
+    __syncthreads();   // keys [0, 128 nchunks) written; the rest of [0, 4 nm4) is never read
+    if (C > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    const int nm4 = (nm + 3) >> 2;
+
+    // ---------------------------------------------------------------- pool (Full, optional)
+    if (a.pool_out) {
+        const int nb = (nm + 7) / 8, nb4 = (nb + 3) >> 2;
+        for (int ib = tid; ib < 4 * nb4; ib += kThreads) {
+            uint32_t m = 0u;
+            if (ib < nb) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) m = max(m, keys[8 * ib + u]);   // order-preserving keys
+            }
+            bkeys[ib] = m;
+        }
+        __syncthreads();
+        uint32_t T, kk;
+        cluster_select<C>(cluster, cta, sm, bkeys, nb4, (len + 7) / 8, a.P_out, T, kk);
+        const int64_t b0 = beg / 8;
+        cluster_compact<C>(cluster, cta, sm, bkeys, nb, T, kk, a.P_out, a.pool_out + row * (int64_t)a.P_out,
+                           [&](int ib) { return (int32_t)(b0 + ib); });
+        reset_fine(sm);
+        // no CTA starts the next selection (its pushes) before every CTA is done with this one
+        if (C > 1) cluster.sync(); else __syncthreads();
     }
 
-    // ---------------------------------------------------------------- position-ordered compaction
-    pdl_launch_dependents();   // the next kernel may launch during the compaction
-    // Warp w owns a contiguous run of this slice; ballots order its lanes.
-    int R = (nm + kWarps - 1) / kWarps;
-    R = (R + 31) & ~31;
-    const int w0 = min(nm, warp * R), w1 = min(nm, w0 + R);
-    uint32_t gt = 0, eq = 0;
-    for (int base = w0; base < w1; base += 32) {
-        const int i = base + lane;
-        const uint32_t k = i < w1 ? keys[i] : 0u;
-        gt += __popc(__ballot_sync(0xFFFFFFFFu, k > T));
-        eq += __popc(__ballot_sync(0xFFFFFFFFu, T != 0u && k == T));
-    }
-    if (lane == 0) {   // publish this warp's counts in every CTA
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-            uint32_t *dst = C > 1 ? cluster.map_shared_rank(&wcnt[cta][0][warp], c) : &wcnt[cta][0][warp];
-            dst[0] = gt;
-            dst[kWarps] = eq;
-        }
-    }
-    // every warp's counts are in place; and after this barrier no CTA reads another's
-    // shared memory, so each may leave when done
-    if (C > 1) cluster.sync(); else __syncthreads();
-    uint32_t bg = 0u, be_ = 0u, tg = 0u, te = 0u;     // (before this warp, in the row) counts
-#pragma unroll
-    for (int c = 0; c < C; ++c) {
-        const uint32_t vg = lane < kWarps ? wcnt[c][0][lane] : 0u, ve = lane < kWarps ? wcnt[c][1][lane] : 0u;
-        const bool before = c < cta || (c == cta && lane < warp);
-        bg += before ? vg : 0u;
-        be_ += before ? ve : 0u;
-        tg += vg;
-        te += ve;
-    }
-    const uint32_t gt_before = __reduce_add_sync(0xFFFFFFFFu, bg), eq_before = __reduce_add_sync(0xFFFFFFFFu, be_);
-    int32_t *orow = a.out + row * (int64_t)K;
-    const uint32_t lt = (1u << lane) - 1u;
-    uint32_t tie = eq_before;
-    uint32_t slot = gt_before + min(kk, tie);
-    for (int base = w0; base < w1; base += 32) {
-        const int i = base + lane;
-        const uint32_t k = i < w1 ? keys[i] : 0u;
-        const bool is_eq = T != 0u && k == T;
-        const uint32_t bq = __ballot_sync(0xFFFFFFFFu, is_eq);
-        const bool take = k > T || (is_eq && tie + __popc(bq & lt) < kk);
-        const uint32_t bs = __ballot_sync(0xFFFFFFFFu, take);
-        if (take) orow[slot + __popc(bs & lt)] = out_id(a, row, beg + i);
-        slot += __popc(bs);
-        tie += __popc(bq);
-    }
-    if (cta == C - 1) {
-        const uint32_t gt_total = __reduce_add_sync(0xFFFFFFFFu, tg), eq_total = __reduce_add_sync(0xFFFFFFFFu, te);
-        const int total = (int)(gt_total + min(kk, eq_total));
-        for (int s2 = total + tid; s2 < K; s2 += kThreads) orow[s2] = -1;
-    }
+    // ---------------------------------------------------------------- Top-K
+    uint32_t T, kk;
+    cluster_select<C>(cluster, cta, sm, keys, nm4, full ? len : a.M, a.K, T, kk);
+    pdl_launch_dependents();
+    cluster_compact<C>(cluster, cta, sm, keys, nm, T, kk, a.K, a.idx + row * (int64_t)a.K, [&](int i) {
+        const int64_t li = beg + i;
+        if (full) return (int32_t)li;
+        return (int32_t)((int64_t)__ldg(a.pool_in + row * a.P + li / 8) * 8 + (li & 7));
+    });
 }
 
 // Keys per CTA and dynamic shared memory for a split of the rows over C CTAs.
@@ -378,6 +558,55 @@ csa2_status launch_topk(const TopkArgs &in, int64_t Lmax, cudaStream_t stream) {
     return CSA2_OK;
 }
 
+csa2_status launch_index_topk(const FusedArgs &in, cudaStream_t stream) {
+    FusedArgs a = in;
+    if (a.rows == 0) return CSA2_OK;
+    // keys and block keys of a slice: (chunk + chunk/8 + 4) words, chunk a multiple of 128
+    auto chunk_for = [&](int c) {
+        int64_t ch = ((a.M + c - 1) / c + 127) & ~int64_t(127);
+        return ch < 128 ? (int64_t)128 : ch;
+    };
+    auto smem_for = [&](int c) { return (size_t)(chunk_for(c) + chunk_for(c) / 8 + 4) * sizeof(uint32_t); };
+    int C = 1;
+    while (C < kMaxCluster && smem_for(C) > (size_t)kSmemCap) C *= 2;
+    while (C < 4 && chunk_for(C) > 4096 && a.rows * C * 2 <= (int64_t)num_sms()) C *= 2;
+    const int64_t chunk = chunk_for(C);
+    const size_t smem = smem_for(C);
+    if (smem > (size_t)kSmemCap) {
+        set_error("index_topk: a row of %lld candidates does not fit %d CTAs", (long long)a.M, kMaxCluster);
+        return CSA2_ERR_UNSUPPORTED;
+    }
+    a.chunk = (int)chunk;
+    const int64_t grid = a.rows * C;
+    if (grid > 0x7FFFFFFF) {
+        set_error("index_topk: too many rows");
+        return CSA2_ERR_UNSUPPORTED;
+    }
+    const void *fn = C == 1 ? (const void *)index_topk_kernel<1>
+                   : C == 2 ? (const void *)index_topk_kernel<2>
+                   : C == 4 ? (const void *)index_topk_kernel<4>
+                            : (const void *)index_topk_kernel<8>;
+    static bool smem_set[4][64];
+    const int ci = C == 1 ? 0 : (C == 2 ? 1 : (C == 4 ? 2 : 3));
+    CSA2_CUDA_CALL(ensure_smem_limit(fn, kSmemCap, smem_set[ci]), "index_topk: smem attribute");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];   // no programmatic serialization: see launch_topk
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {&a};
+    CSA2_CUDA_CALL(cudaLaunchKernelExC(&cfg, fn, args), "index_topk_kernel launch");
+    CSA2_LAUNCH_CHECK("index_topk_kernel");
+    return CSA2_OK;
+}
+
 }  // namespace
 }  // namespace csa2
 
@@ -440,4 +669,50 @@ extern "C" csa2_status csa2_build_pool(int B, int T, int64_t N, const float *sco
     a.K = P;
     a.out = pool_blocks;
     return launch_topk(a, (N + 7) / 8, stream_of(stream));
+}
+
+extern "C" csa2_status csa2_index_topk(csa2_mode mode, int B, int T, int64_t N, const void *q_idx, csa2_dtype q_dt,
+                                       const float *w, const void *k_idx, csa2_dtype k_dt, const int32_t *kv_len,
+                                       const int32_t *pool_blocks, int P, int K, int32_t *idx, int32_t *pool_out,
+                                       int P_out, uint32_t *err_flag, csa2_stream_t stream) {
+    clear_error();
+    CSA2_REQUIRE(mode == CSA2_MODE_FULL || mode == CSA2_MODE_REINDEX || mode == CSA2_MODE_REUSE,
+                 "index_topk: bad mode %d", (int)mode);
+    if (mode == CSA2_MODE_REUSE) return CSA2_OK;
+    CSA2_REQUIRE(B >= 0 && T >= 0 && N >= 0, "index_topk: negative shape");
+    CSA2_REQUIRE(q_dt == CSA2_FP8_E4M3 && k_dt == CSA2_FP8_E4M3,
+                 "index_topk: FP8 E4M3 indexer only (use csa2_index_score + csa2_topk for bf16)");
+    CSA2_REQUIRE(K >= 1 && K <= CSA2_MAX_K, "index_topk: K=%d not in [1,2048]", K);
+    if (mode == CSA2_MODE_REINDEX) {
+        CSA2_REQUIRE(pool_blocks != nullptr, "index_topk: REINDEX needs pool_blocks");
+        CSA2_REQUIRE(P >= 1 && P <= CSA2_MAX_POOL, "index_topk: P=%d not in [1,2048]", P);
+        CSA2_REQUIRE(pool_out == nullptr, "index_topk: pool_out is for FULL only");
+    } else {
+        CSA2_REQUIRE(pool_blocks == nullptr, "index_topk: FULL takes no pool_blocks");
+        if (pool_out) CSA2_REQUIRE(P_out >= 1 && P_out <= CSA2_MAX_POOL, "index_topk: P_out=%d not in [1,2048]", P_out);
+    }
+    if ((int64_t)B * T == 0) return CSA2_OK;
+    CSA2_REQUIRE(q_idx && w && k_idx && kv_len && idx, "index_topk: null pointer");
+    CSA2_REQUIRE(aligned(q_idx, 16) && aligned(k_idx, 16), "index_topk: q_idx/k_idx must be 16-byte aligned");
+    CSA2_REQUIRE(aligned(w, 4) && aligned(kv_len, 4) && aligned(idx, 4) && aligned(pool_out, 4) &&
+                     aligned(pool_blocks, 4),
+                 "index_topk: misaligned pointer");
+    FusedArgs a = {};
+    a.mode = (int)mode;
+    a.rows = (int64_t)B * T;
+    a.T = T;
+    a.N = N;
+    a.M = (mode == CSA2_MODE_FULL) ? N : (int64_t)P * 8;
+    a.q = (const uint8_t *)q_idx;
+    a.w = w;
+    a.k = (const uint8_t *)k_idx;
+    a.kv_len = kv_len;
+    a.pool_in = pool_blocks;
+    a.P = P;
+    a.K = K;
+    a.idx = idx;
+    a.pool_out = pool_out;
+    a.P_out = pool_out ? P_out : 0;
+    a.err_flag = err_flag;
+    return launch_index_topk(a, stream_of(stream));
 }

@@ -13,7 +13,10 @@ whole step can be captured in a CUDA graph.  Per step:
      every sequence (one launch for all layers);
   2. per group: the Full layer scores all entries, builds the pool and takes
      its Top-512; a Reindex layer scores the pool with its own indexer query
-     against the Full layer's index keys and takes its Top-512;
+     against the Full layer's index keys and takes its Top-512 (with FP8
+     indexer tensors each of these is one fused csa2_index_topk call, the
+     scores staying on chip; otherwise csa2_index_score, csa2_build_pool and
+     csa2_topk);
   3. every layer attends over its FP4 KV with its group's indices (Reuse
      layers consume the group's index buffer unchanged).
 """
@@ -23,8 +26,8 @@ from dataclasses import dataclass
 
 import torch
 
-from . import (MODE_FULL, MODE_REINDEX, MODE_REUSE, csa2_build_pool, csa2_index_score, csa2_quantize_kv_fp4,
-               csa2_sparse_attn_fp4, csa2_topk, workspace_for_attn)
+from . import (MODE_FULL, MODE_REINDEX, MODE_REUSE, csa2_build_pool, csa2_index_score, csa2_index_topk,
+               csa2_quantize_kv_fp4, csa2_sparse_attn_fp4, csa2_topk, workspace_for_attn)
 
 DECODER_SCHEDULE = ("full", "reuse", "reuse", "reuse") + ("reindex", "reuse", "reuse", "reuse") * 4
 
@@ -40,6 +43,7 @@ class StepShape:
     P: int = 2048
     idx_fp8: bool = True
     kv_per_layer: bool = True        # each layer attends over its own FP4 KV
+    fused_indexer: bool = True       # FP8 only: csa2_index_topk instead of score + pool + topk
     schedule: tuple = DECODER_SCHEDULE
 
 
@@ -105,8 +109,17 @@ class DecoderStep:
         csa2_quantize_kv_fp4(x["new_rows"], self.codes, self.scales, dst_slot=x["new_slots"], err_flag=self.err,
                              stream=stream)
         gi = -1
+        fused = s.fused_indexer and s.idx_fp8
         for layer, mode in enumerate(s.schedule):
-            if mode != "reuse":
+            if mode != "reuse" and fused:
+                gi += 1
+                if mode == "full":
+                    csa2_index_topk(MODE_FULL, x["q_idx"][gi], x["w_idx"][gi], self.k_idx, self.kv_len, self.idx[gi],
+                                    pool_out=self.pool if layer == 0 else None, err_flag=self.err, stream=stream)
+                else:
+                    csa2_index_topk(MODE_REINDEX, x["q_idx"][gi], x["w_idx"][gi], self.k_idx, self.kv_len,
+                                    self.idx[gi], pool_blocks=self.pool, err_flag=self.err, stream=stream)
+            elif mode != "reuse":
                 gi += 1
                 if mode == "full":
                     csa2_index_score(MODE_FULL, x["q_idx"][gi], x["w_idx"][gi], self.k_idx, self.kv_len,
@@ -132,8 +145,11 @@ class DecoderStep:
         s = self.shape
         split = self.ws is not None
         n = 1                                              # quantise
+        fused = s.fused_indexer and s.idx_fp8
         for layer, mode in enumerate(s.schedule):
-            if mode == "full":
+            if mode != "reuse" and fused:
+                n += 1                                     # fused score + (pool) + topk
+            elif mode == "full":
                 n += 2 + (1 if layer == 0 else 0)         # score, topk (+ pool)
             elif mode == "reindex":
                 n += 2

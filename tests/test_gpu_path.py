@@ -271,12 +271,13 @@ def test_append_and_pool_b16(csa2):
         assert (blk >= 0).sum() * 8 <= 16384
 
 
-def test_decoder_step_schedule_runs_and_reuses_indices(csa2):
-    """The 20-layer decoder step driver: every Reuse layer's output equals a
-    direct attention call with its group's indices, and Reindex selections lie
-    inside the pool."""
+@pytest.mark.parametrize("fused", [True, False])
+def test_decoder_step_schedule_runs_and_reuses_indices(csa2, fused):
+    """The 20-layer decoder step driver (fused indexer calls, or score + pool
+    + Top-K): every Reuse layer's output equals a direct attention call with
+    its group's indices, and Reindex selections lie inside the pool."""
     from sparse_attention_fp4_quantize_gb300.decode import DecoderStep, StepShape
-    st = DecoderStep(StepShape(B=4, N=3000), device=DEV)
+    st = DecoderStep(StepShape(B=4, N=3000, fused_indexer=fused), device=DEV)
     w = gen.scaled(gen.FULL_BATCHED_DECODE, B=4, N=3000)
     st.kv_len.copy_(gen.kv_lengths(w).clamp(max=3000).to(DEV))
     for kv in range(st.n_kv):
