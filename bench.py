@@ -304,7 +304,16 @@ def _extra_workloads(dev, stream, peak_gbs):
     qbytes = R * 576 * 2 + R * (288 + 36)
     res["append_quantize_1m_rows"] = {"us": t * 1e6, "bytes": qbytes, "gbs": qbytes / t / 1e9,
                                      "hbm_frac": qbytes / t / 1e9 / peak_gbs}
-    del rows, outs
+    # the same append from pre-RoPE rows: RoPE (fp32 table of 131072 positions) fused ahead of the quantiser
+    tab = gen.rope_table(131072, device=dev)
+    pos = torch.randint(0, 131072, (R,), generator=torch.Generator(device=dev).manual_seed(7), device=dev,
+                        dtype=torch.int32)
+    t = _time_graph(lambda: [csa2.csa2_rope_quantize_kv_fp4(rows, pos, tab, c, s_, stream=stream)
+                             for c, s_ in outs], stream, 20) / 2
+    rbytes = qbytes + R * 4
+    res["append_rope_quantize_1m_rows"] = {"us": t * 1e6, "bytes": rbytes, "gbs": rbytes / t / 1e9,
+                                          "hbm_frac": rbytes / t / 1e9 / peak_gbs}
+    del rows, outs, tab, pos
     # pool for 16 x 65536 entries from Full scores
     q5, w5w, k5 = gen.indexer_inputs(w5, device=dev)
     kl5 = gen.kv_lengths(w5).to(dev)

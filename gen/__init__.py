@@ -59,6 +59,16 @@ def rope_interleaved(x: torch.Tensor, pos: torch.Tensor) -> torch.Tensor:
     return torch.cat((x[..., : d - ROPE_DIMS], rot), dim=-1)
 
 
+def rope_table(n_pos, rope_dim=None, theta=None, device="cpu") -> torch.Tensor:
+    """fp32 [n_pos, rope_dim/2, 2] table of (cos, sin) of position * theta^(-2i/rope_dim),
+    evaluated in fp64 and rounded to fp32 (an input of the fused RoPE + quantise call)."""
+    rope_dim = ROPE_DIMS if rope_dim is None else rope_dim
+    theta = ROPE_THETA if theta is None else theta
+    inv = theta ** (-torch.arange(0, rope_dim, 2, dtype=torch.float64) / rope_dim)
+    ang = torch.arange(n_pos, dtype=torch.float64)[:, None] * inv
+    return torch.stack((torch.cos(ang), torch.sin(ang)), dim=-1).to(torch.float32).to(device)
+
+
 def kv_rows(seed, stream, rows, D, *, rms=True, rope_pos=None, outlier_p=1e-3, outlier_mul=8.0,
             device="cpu") -> torch.Tensor:
     """bf16 bit patterns [rows, D] of post-RoPE KV rows: N(0,1) with each

@@ -102,6 +102,28 @@ csa2_status csa2_quantize_kv_fp4(const void *kv, int64_t rows, int D, int64_t kv
                                  uint8_t *scales, uint32_t *err_flag, csa2_stream_t stream);
 
 /*
+ * csa2_rope_quantize_kv_fp4 -- RoPE, then csa2_quantize_kv_fp4, in one pass
+ * over pre-RoPE rows.  [ENG] section "效率组件四件", item 4 (the FP4 main KV
+ * is quantised after RoPE); the pages fix neither the rotation layout nor how
+ * the angles are evaluated.  Rotation: interleaved pairs (2i, 2i+1) of the
+ * last rope_dim channels, with the caller's fp32 table
+ *     cos_sin[pos][i] = (cos, sin),  float [n_pos, rope_dim/2, 2], 8-byte aligned:
+ *     a' = (a*c) - (b*s),  b' = (a*s) + (b*c)
+ * in fp32, every product and sum rounded (no fused multiply-add), then rounded
+ * to bf16 (nearest even) before the quantiser sees it: the stored bytes equal
+ * csa2_quantize_kv_fp4 of the rows an unfused RoPE in those steps writes.
+ *
+ * pos       int32 [rows]: row r uses table row pos[r]; a position outside
+ *           [0, n_pos) skips the row's rotated groups and sets CSA2_FLAG_BAD_INDEX.
+ * rope_dim  multiple of 16, 16..D (64 for the 576-channel entries).
+ * Other arguments and rules as csa2_quantize_kv_fp4.
+ */
+csa2_status csa2_rope_quantize_kv_fp4(const void *kv, int64_t rows, int D, int64_t kv_row_stride,
+                                      const int32_t *pos, const float *cos_sin, int64_t n_pos, int rope_dim,
+                                      const int64_t *dst_slot, int64_t n_slots, uint8_t *codes, uint8_t *scales,
+                                      uint32_t *err_flag, csa2_stream_t stream);
+
+/*
  * csa2_index_score -- indexer scores of query tokens against compressed
  * entries.  [ENG] section "Hierarchical Sparse Indexer——索引成本变常数": Full
  * layers score every entry (cost linear in context); later Reindex layers

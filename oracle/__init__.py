@@ -129,6 +129,25 @@ def quantize_kv_fp4(kv_bf16_bits: np.ndarray, dst_slot=None, n_slots=None):
     return codes, scales
 
 
+def rope_bf16(kv_bf16_bits: np.ndarray, pos, cos_sin, rope_dim=64):
+    """RoPE (interleaved pairs of the last rope_dim channels, fp32 table
+    cos_sin [n_pos, rope_dim/2, 2], fp32 arithmetic without FMA) -> bf16 bits."""
+    kv = _c(kv_bf16_bits, np.uint16)
+    R, D = kv.shape
+    ps = _c(pos, np.int32)
+    cs = _c(cos_sin, np.float32)
+    out = np.zeros((R, D), np.uint16)
+    rc = _load().orc_rope_bf16(_p(kv), R, D, D, _p(ps), _p(cs), cs.shape[0], rope_dim, _p(out))
+    if rc != 0:
+        raise ValueError("oracle rope: bad shape or position")
+    return out
+
+
+def rope_quantize_kv_fp4(kv_bf16_bits, pos, cos_sin, rope_dim=64, dst_slot=None, n_slots=None):
+    """Pre-RoPE bf16 rows -> RoPE (rope_bf16) -> quantize_kv_fp4."""
+    return quantize_kv_fp4(rope_bf16(kv_bf16_bits, pos, cos_sin, rope_dim), dst_slot=dst_slot, n_slots=n_slots)
+
+
 def dequant_fp4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     codes = _c(codes, np.uint8)
     scales = _c(scales, np.uint8)

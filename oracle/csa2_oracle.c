@@ -195,6 +195,60 @@ ORC_EXPORT int orc_quantize_kv_fp4(const uint16_t *kv, int64_t rows, int D, int6
     return 0;
 }
 
+/*
+ * RoPE on the append path, then the quantiser ("DeepSeek-V4.1-Flash：把 KV
+ * Cache 压缩到极限的百万上下文 MoE", 效率组件四件 item 4: the FP4 main KV is
+ * quantised after RoPE).  The pages fix neither the rotation layout nor how
+ * the angles are evaluated; READING: interleaved pairs (2i, 2i+1) of the last
+ * rope_dim channels, rotated by a caller-supplied fp32 table cos_sin[pos][i] =
+ * (cos, sin), evaluated in fp32 without fused multiply-add:
+ *     a' = (a*c) - (b*s),  b' = (a*s) + (b*c)   (every product and sum rounded to fp32)
+ * then rounded to bf16 (nearest, ties to even).  Other channels pass through.
+ * out_bits may alias nothing; returns 0, or -1 on a bad shape or position.
+ */
+static uint16_t f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u) return (uint16_t)(u >> 16);   /* inf / NaN: truncate */
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+static float bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+ORC_EXPORT int orc_rope_bf16(const uint16_t *kv, int64_t rows, int D, int64_t row_stride, const int32_t *pos,
+                             const float *cos_sin, int64_t n_pos, int rope_dim, uint16_t *out)
+{
+    int64_t r;
+    if (D <= 0 || rope_dim <= 0 || rope_dim > D || rope_dim % 2 != 0) return -1;
+    for (r = 0; r < rows; ++r) {
+        const uint16_t *x = kv + r * row_stride;
+        uint16_t *y = out + r * (int64_t)D;
+        const int64_t p = pos[r];
+        int c, i;
+        if (p < 0 || p >= n_pos) return -1;
+        for (c = 0; c < D - rope_dim; ++c) y[c] = x[c];
+        for (i = 0; i < rope_dim / 2; ++i) {
+            const float cs = cos_sin[(p * (rope_dim / 2) + i) * 2];
+            const float sn = cos_sin[(p * (rope_dim / 2) + i) * 2 + 1];
+            const float a = bf16_to_f32(x[D - rope_dim + 2 * i]);
+            const float b = bf16_to_f32(x[D - rope_dim + 2 * i + 1]);
+            const float ac = a * cs, bs = b * sn, as = a * sn, bc = b * cs;
+            const float ra = ac - bs, rb = as + bc;
+            y[D - rope_dim + 2 * i] = f32_to_bf16_rne(ra);
+            y[D - rope_dim + 2 * i + 1] = f32_to_bf16_rne(rb);
+        }
+    }
+    return 0;
+}
+
 /* Dequantised value of channel c of a stored entry (codes row, scales row). */
 static double fp4_value(const uint8_t *crow, const uint8_t *srow, int c)
 {

@@ -44,6 +44,7 @@ def _load() -> ctypes.CDLL:
     P, i32, i64, u64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
     sig = {
         "csa2_quantize_kv_fp4": ([P, i64, i32, i64, P, i64, P, P, P, P], i32),
+        "csa2_rope_quantize_kv_fp4": ([P, i64, i32, i64, P, P, i64, i32, P, i64, P, P, P, P], i32),
         "csa2_index_score": ([i32, i32, i32, i64, P, i32, P, P, i32, P, P, i32, P, P, P], i32),
         "csa2_build_pool": ([i32, i32, i64, P, P, i32, i32, P, P, u64, P], i32),
         "csa2_build_pool_workspace_bytes": ([i32, i32, i64, i32], u64),
@@ -71,7 +72,7 @@ _lib = _load()
 
 
 def exported_symbols():
-    return ["csa2_quantize_kv_fp4", "csa2_index_score", "csa2_build_pool", "csa2_build_pool_workspace_bytes",
+    return ["csa2_quantize_kv_fp4", "csa2_rope_quantize_kv_fp4", "csa2_index_score", "csa2_build_pool", "csa2_build_pool_workspace_bytes",
             "csa2_topk", "csa2_topk_workspace_bytes", "csa2_index_topk", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes",
             "csa2_sparse_attn_fp4_noalloc", "csa2_sparse_attn_noalloc_max_scratch_bytes",
             "csa2_status_string", "csa2_last_error", "csa2_version"]
@@ -119,6 +120,17 @@ def csa2_quantize_kv_fp4(kv, codes, scales, dst_slot=None, err_flag=None, stream
     n_slots = codes.shape[0]
     _check(_lib.csa2_quantize_kv_fp4(_ptr(kv), R, D, kv.stride(0), _ptr(dst_slot), n_slots, _ptr(codes),
                                      _ptr(scales), _ptr(err_flag), _stream(stream)))
+
+
+def csa2_rope_quantize_kv_fp4(kv, pos, cos_sin, codes, scales, dst_slot=None, err_flag=None, stream=None):
+    """Pre-RoPE kv bf16 [R, D] (or int16 bits), pos int32 [R], cos_sin fp32
+    [n_pos, rope_dim/2, 2] -> codes uint8 [S, D/2], scales uint8 [S, D/16]."""
+    _cuda(kv, pos, cos_sin, codes, scales, dst_slot, err_flag)
+    R, D = kv.shape
+    n_pos, half = cos_sin.shape[0], cos_sin.shape[1]
+    _check(_lib.csa2_rope_quantize_kv_fp4(_ptr(kv), R, D, D, _ptr(pos), _ptr(cos_sin), n_pos, 2 * half,
+                                          _ptr(dst_slot), codes.shape[0], _ptr(codes), _ptr(scales),
+                                          _ptr(err_flag), _stream(stream)))
 
 
 def csa2_index_score(mode, q_idx, w, k_idx, kv_len, scores, pool_blocks=None, err_flag=None, stream=None):

@@ -108,10 +108,30 @@ __device__ __forceinline__ uint32_t encode_word(uint32_t w, float inv) {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
+// RoPE of the append path, fused ahead of the quantiser: interleaved pairs
+// (2i, 2i+1) of the last rope_dim channels rotated by a caller-supplied fp32
+// table cos_sin[pos][i] = (cos, sin), in fp32 without fused multiply-add, then
+// rounded to bf16 (nearest even) -- the rows the unfused path would store.
+struct RopeArgs {
+    const int32_t *pos;      // [rows] token position of each row
+    const float2 *cos_sin;   // [n_pos, rope_dim / 2]
+    int64_t n_pos;
+    int rope_dim;
+};
+
+__device__ __forceinline__ uint32_t rope_word(uint32_t w, float2 cs) {
+    const float a = __uint_as_float(w << 16), b = __uint_as_float(w & 0xFFFF0000u);
+    const float ra = __fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, cs.y));
+    const float rb = __fadd_rn(__fmul_rn(a, cs.y), __fmul_rn(b, cs.x));
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ra)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(rb)) << 16);
+}
+
+template <bool ROPE>
 __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(
     const uint16_t *__restrict__ kv, uint32_t total_units, FastDiv upr_div, int D, int64_t stride,
     int64_t row0, const int64_t *__restrict__ dst_slot, int64_t n_slots, uint8_t *__restrict__ codes,
-    uint8_t *__restrict__ scales, uint32_t *err_flag) {
+    uint8_t *__restrict__ scales, uint32_t *err_flag, RopeArgs rope) {
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -132,6 +152,22 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(
             ur[k] = (ok[k] ? u : 0u) - r * upr;
             v[k] = make_uint4(0, 0, 0, 0);
             if (ok[k]) v[k] = ld_stream_v4(kv + (row0 + r) * stride + (int64_t)ur[k] * 8);
+        }
+        if constexpr (ROPE) {
+            const uint32_t u0 = (uint32_t)(D - rope.rope_dim) / 8;   // first unit of the rotated channels
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                if (!ok[k] || ur[k] < u0) continue;
+                const int64_t p = rope.pos[row0 + rr[k]];
+                if (p < 0 || p >= rope.n_pos) {   // both units of the group see the same row: skipped together
+                    flag_error(err_flag, CSA2_FLAG_BAD_INDEX);
+                    ok[k] = false;
+                    continue;
+                }
+                const float2 *t = rope.cos_sin + p * (rope.rope_dim / 2) + (ur[k] - u0) * 4;
+                v[k] = make_uint4(rope_word(v[k].x, t[0]), rope_word(v[k].y, t[1]), rope_word(v[k].z, t[2]),
+                                  rope_word(v[k].w, t[3]));
+            }
         }
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {
@@ -163,25 +199,13 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(
 
 using namespace csa2;
 
-extern "C" csa2_status csa2_quantize_kv_fp4(const void *kv, int64_t rows, int D,
-                                            int64_t kv_row_stride, const int64_t *dst_slot,
-                                            int64_t n_slots, uint8_t *codes, uint8_t *scales,
-                                            uint32_t *err_flag, csa2_stream_t stream) {
-    clear_error();
-    CSA2_REQUIRE(rows >= 0, "quantize: rows < 0");
-    CSA2_REQUIRE(D >= 16 && D <= 4096 && D % 16 == 0, "quantize: D=%d must be a multiple of 16 in [16,4096]", D);
-    CSA2_REQUIRE(kv_row_stride >= D && kv_row_stride % 8 == 0,
-                 "quantize: kv_row_stride=%lld must be >= D and a multiple of 8", (long long)kv_row_stride);
-    CSA2_REQUIRE(n_slots >= 0, "quantize: n_slots < 0");
-    CSA2_REQUIRE(dst_slot || rows <= n_slots, "quantize: rows > n_slots without dst_slot");
-    if (rows == 0) return CSA2_OK;
-    CSA2_REQUIRE(kv && codes && scales, "quantize: null pointer");
-    CSA2_REQUIRE(aligned(kv, 16), "quantize: kv must be 16-byte aligned");
-    CSA2_REQUIRE(aligned(codes, 4), "quantize: codes must be 4-byte aligned");
-    CSA2_REQUIRE(!dst_slot || aligned(dst_slot, 8), "quantize: dst_slot must be 8-byte aligned");
+static csa2_status launch_quantize(const void *kv, int64_t rows, int D, int64_t kv_row_stride,
+                                   const int64_t *dst_slot, int64_t n_slots, uint8_t *codes, uint8_t *scales,
+                                   uint32_t *err_flag, const RopeArgs *rope, csa2_stream_t stream) {
     const uint32_t upr = (uint32_t)(D / 8);
     FastDiv fd;
     fd.init(upr);
+    const RopeArgs ra = rope ? *rope : RopeArgs{nullptr, nullptr, 0, 0};
     // Launch in chunks whose unit count fits comfortably in 32 bits.
     const int64_t max_rows = (int64_t)(0x7FFFFFFFu / upr);
     const int max_blocks = num_sms() * 8;
@@ -191,11 +215,60 @@ extern "C" csa2_status csa2_quantize_kv_fp4(const void *kv, int64_t rows, int D,
         int64_t want = ((int64_t)units + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
         int blocks = (int)(want < max_blocks ? want : max_blocks);
         if (blocks < 1) blocks = 1;
-        CSA2_CUDA_CALL(launch_pdl(quantize_fp4_kernel, dim3(blocks), dim3(kThreads), 0, stream_of(stream),
-                                  (const uint16_t *)kv, units, fd, D, kv_row_stride, r0, dst_slot, n_slots, codes,
-                                  scales, err_flag),
-                       "quantize_fp4_kernel launch");
+        if (rope)
+            CSA2_CUDA_CALL(launch_pdl(quantize_fp4_kernel<true>, dim3(blocks), dim3(kThreads), 0, stream_of(stream),
+                                      (const uint16_t *)kv, units, fd, D, kv_row_stride, r0, dst_slot, n_slots,
+                                      codes, scales, err_flag, ra),
+                           "quantize_fp4_kernel launch");
+        else
+            CSA2_CUDA_CALL(launch_pdl(quantize_fp4_kernel<false>, dim3(blocks), dim3(kThreads), 0, stream_of(stream),
+                                      (const uint16_t *)kv, units, fd, D, kv_row_stride, r0, dst_slot, n_slots,
+                                      codes, scales, err_flag, ra),
+                           "quantize_fp4_kernel launch");
         CSA2_LAUNCH_CHECK("quantize_fp4_kernel");
     }
     return CSA2_OK;
+}
+
+#define CSA2_QUANT_CHECKS()                                                                                    \
+    CSA2_REQUIRE(rows >= 0, "quantize: rows < 0");                                                            \
+    CSA2_REQUIRE(D >= 16 && D <= 4096 && D % 16 == 0, "quantize: D=%d must be a multiple of 16 in [16,4096]", \
+                 D);                                                                                           \
+    CSA2_REQUIRE(kv_row_stride >= D && kv_row_stride % 8 == 0,                                                 \
+                 "quantize: kv_row_stride=%lld must be >= D and a multiple of 8", (long long)kv_row_stride);   \
+    CSA2_REQUIRE(n_slots >= 0, "quantize: n_slots < 0");                                                      \
+    CSA2_REQUIRE(dst_slot || rows <= n_slots, "quantize: rows > n_slots without dst_slot")
+
+extern "C" csa2_status csa2_quantize_kv_fp4(const void *kv, int64_t rows, int D,
+                                            int64_t kv_row_stride, const int64_t *dst_slot,
+                                            int64_t n_slots, uint8_t *codes, uint8_t *scales,
+                                            uint32_t *err_flag, csa2_stream_t stream) {
+    clear_error();
+    CSA2_QUANT_CHECKS();
+    if (rows == 0) return CSA2_OK;
+    CSA2_REQUIRE(kv && codes && scales, "quantize: null pointer");
+    CSA2_REQUIRE(aligned(kv, 16), "quantize: kv must be 16-byte aligned");
+    CSA2_REQUIRE(aligned(codes, 4), "quantize: codes must be 4-byte aligned");
+    CSA2_REQUIRE(!dst_slot || aligned(dst_slot, 8), "quantize: dst_slot must be 8-byte aligned");
+    return launch_quantize(kv, rows, D, kv_row_stride, dst_slot, n_slots, codes, scales, err_flag, nullptr, stream);
+}
+
+extern "C" csa2_status csa2_rope_quantize_kv_fp4(const void *kv, int64_t rows, int D, int64_t kv_row_stride,
+                                                 const int32_t *pos, const float *cos_sin, int64_t n_pos,
+                                                 int rope_dim, const int64_t *dst_slot, int64_t n_slots,
+                                                 uint8_t *codes, uint8_t *scales, uint32_t *err_flag,
+                                                 csa2_stream_t stream) {
+    clear_error();
+    CSA2_QUANT_CHECKS();
+    CSA2_REQUIRE(rope_dim >= 16 && rope_dim <= D && rope_dim % 16 == 0,
+                 "rope_quantize: rope_dim=%d must be a multiple of 16 in [16, D]", rope_dim);
+    CSA2_REQUIRE(n_pos >= 1, "rope_quantize: n_pos < 1");
+    if (rows == 0) return CSA2_OK;
+    CSA2_REQUIRE(kv && codes && scales && pos && cos_sin, "rope_quantize: null pointer");
+    CSA2_REQUIRE(aligned(kv, 16), "quantize: kv must be 16-byte aligned");
+    CSA2_REQUIRE(aligned(codes, 4), "quantize: codes must be 4-byte aligned");
+    CSA2_REQUIRE(!dst_slot || aligned(dst_slot, 8), "quantize: dst_slot must be 8-byte aligned");
+    CSA2_REQUIRE(aligned(pos, 4) && aligned(cos_sin, 8), "rope_quantize: misaligned pos / cos_sin");
+    const RopeArgs ra = {pos, reinterpret_cast<const float2 *>(cos_sin), n_pos, rope_dim};
+    return launch_quantize(kv, rows, D, kv_row_stride, dst_slot, n_slots, codes, scales, err_flag, &ra, stream);
 }
