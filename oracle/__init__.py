@@ -79,6 +79,10 @@ def _load():
         lib.orc_topk.restype = i32
         lib.orc_sparse_attn.argtypes = [i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, dbl, P, P]
         lib.orc_sparse_attn.restype = i64
+        lib.orc_rope_bf16.argtypes = [P, i64, i32, i64, P, P, i64, i32, P]
+        lib.orc_rope_bf16.restype = i32
+        lib.orc_swa_attn_merge.argtypes = [i32, i32, i32, i32, i32, P, P, i32, P, dbl, P, P, P, P]
+        lib.orc_swa_attn_merge.restype = i32
         if not lib.orc_rounding_mode_ok():
             raise RuntimeError("oracle needs the round-to-nearest-even FP mode")
         _lib = lib
@@ -222,3 +226,23 @@ def sparse_attn(q_bf16_bits, codes, scales, N, idx, kv_len, sm_scale, dv):
     if bad < 0:
         raise MemoryError("oracle sparse_attn")
     return out, lse, int(bad)
+
+
+def swa_attn_merge(q_bf16_bits, kv_e4m3, swa_len, sm_scale, dv, o_sparse=None, lse_sparse=None):
+    """q uint16 [B,T,H,D]; kv uint8 E4M3 [B,W,D]; swa_len int32 [B*T]; optional
+    fp64/fp32 o_sparse [B,T,H,dv] and lse_sparse [B,T,H] -> (out fp64 [B,T,H,dv],
+    lse fp64 [B,T,H]): the window branch merged with the sparse branch."""
+    qa = _c(q_bf16_bits, np.uint16)
+    B, T, H, D = qa.shape
+    ka = _c(kv_e4m3, np.uint8)
+    W = ka.shape[1]
+    sl = _c(swa_len, np.int32)
+    os_ = None if o_sparse is None else _c(o_sparse, np.float64)
+    ls = None if lse_sparse is None else _c(lse_sparse, np.float64)
+    out = np.zeros((B, T, H, dv), np.float64)
+    lse = np.zeros((B, T, H), np.float64)
+    rc = _load().orc_swa_attn_merge(B, T, H, D, dv, _p(qa), _p(ka), W, _p(sl), ctypes.c_double(sm_scale),
+                                    _p(os_), _p(ls), _p(out), _p(lse))
+    if rc != 0:
+        raise MemoryError("oracle swa_attn_merge")
+    return out, lse

@@ -536,3 +536,74 @@ ORC_EXPORT int64_t orc_sparse_attn(int B, int T, int H, int D, int dv, const uin
     free(z);
     return bad;
 }
+
+/*
+ * Sliding-window branch with FP8 KV, merged with the sparse branch by
+ * log-sum-exp.  "DeepSeek-V4.1-Flash：把 KV Cache 压缩到极限的百万上下文 MoE",
+ * 效率组件四件 item 4 (SWA KV stays FP8) and "DeepSeek-V4.1-Flash: Pushing the
+ * Limits of KV Cache Compression" (every layer also has a sliding window).
+ * READINGS (the pages give neither the window size nor the FP8 layout): the
+ * window KV is E4M3 rows [B, W, D] without a scale (like the indexer keys),
+ * K = all D channels and V = the first dv (MLA-style, as the sparse branch);
+ * query row (b, t) attends to the first swa_len[b*T+t] (<= W) rows of b's
+ * window, all visible; the two branches cover disjoint entries, so the merge
+ * is the softmax over their union:
+ *     M = max(lse_w, lse_s),  a = e^(lse_w - M),  c = e^(lse_s - M),
+ *     out = (a o_w + c o_s) / (a + c),  lse = M + log(a + c).
+ * o_sparse / lse_sparse NULL: the window branch alone.  Empty window and
+ * lse_s = -inf both: out = 0, lse = -inf.
+ */
+ORC_EXPORT int orc_swa_attn_merge(int B, int T, int H, int D, int dv, const uint16_t *q, const uint8_t *kv, int W,
+                                  const int32_t *swa_len, double sm_scale, const double *o_sparse,
+                                  const double *lse_sparse, double *out, double *lse)
+{
+    double *z = (double *)malloc((size_t)(W > 0 ? W : 1) * sizeof(double));
+    double *ow = (double *)malloc((size_t)(dv > 0 ? dv : 1) * sizeof(double));
+    int64_t bt;
+    if (!z || !ow) { free(z); free(ow); return -1; }
+    for (bt = 0; bt < (int64_t)B * T; ++bt) {
+        const int64_t b = bt / T;
+        int n = swa_len[bt] < W ? swa_len[bt] : W, h, c, i;
+        if (n < 0) n = 0;
+        for (h = 0; h < H; ++h) {
+            const uint16_t *qr = q + (bt * H + h) * (int64_t)D;
+            double *o = out + (bt * H + h) * (int64_t)dv;
+            double m = -INFINITY, sum = 0.0, lw = -INFINITY, ls, M;
+            for (c = 0; c < dv; ++c) ow[c] = 0.0;
+            for (i = 0; i < n; ++i) {
+                const uint8_t *kr = kv + (b * W + i) * (int64_t)D;
+                double acc = 0.0;
+                for (c = 0; c < D; ++c) acc += bf16_value(qr[c]) * orc_e4m3_value(kr[c]);
+                z[i] = sm_scale * acc;
+                if (z[i] > m) m = z[i];
+            }
+            if (n > 0) {
+                for (i = 0; i < n; ++i) sum += exp(z[i] - m);
+                lw = m + log(sum);
+                for (i = 0; i < n; ++i) {
+                    const uint8_t *kr = kv + (b * W + i) * (int64_t)D;
+                    const double p = exp(z[i] - lw);
+                    for (c = 0; c < dv; ++c) ow[c] += p * orc_e4m3_value(kr[c]);
+                }
+            }
+            ls = lse_sparse ? lse_sparse[bt * H + h] : -INFINITY;
+            M = lw > ls ? lw : ls;
+            if (M == -INFINITY) {
+                for (c = 0; c < dv; ++c) o[c] = 0.0;
+                if (lse) lse[bt * H + h] = -INFINITY;
+                continue;
+            }
+            {
+                const double a = exp(lw - M), cs = exp(ls - M);
+                for (c = 0; c < dv; ++c) {
+                    const double os = o_sparse ? o_sparse[(bt * H + h) * (int64_t)dv + c] : 0.0;
+                    o[c] = (a * ow[c] + cs * os) / (a + cs);
+                }
+                if (lse) lse[bt * H + h] = M + log(a + cs);
+            }
+        }
+    }
+    free(z);
+    free(ow);
+    return 0;
+}
