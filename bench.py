@@ -369,6 +369,17 @@ def _extra_workloads(dev, stream, peak_gbs):
     res["pool_build_b8_n262144"] = {"us": t * 1e6, "score_bytes_read": w3.B * w3.N * 4}
     del planes, qs, outs3, k3, full3
     torch.cuda.empty_cache()
+    # sliding-window branch (FP8 window of 128 tokens) merged in place with a sparse-branch output, B=32
+    qs_ = gen.normal_bf16(11, 1, (32, 1, 64, 576), device=dev)
+    kvw = gen.e4m3_bytes(torch.randn(32, 128, 576, generator=torch.Generator(device=dev).manual_seed(3), device=dev))
+    slw = torch.full((32,), 128, dtype=torch.int32, device=dev)
+    osp = torch.randn(32, 1, 64, 512, device=dev)
+    lsp = torch.randn(32, 1, 64, device=dev)
+    t = _time_graph(lambda: csa2.csa2_swa_attn_fp8(qs_, kvw, slw, osp, 1 / 24.0, o_sparse=osp, lse_sparse=lsp,
+                                                   lse=lsp, stream=stream), stream, 50)
+    sb = 32 * 128 * 576 + 2 * 32 * 64 * 512 * 4
+    res["swa_merge_b32_w128"] = {"us": t * 1e6, "algorithmic_bytes": sb, "gbs": sb / t / 1e9}
+    del qs_, kvw, osp, lsp
     # attention alone at larger token counts (T=1 decode tokens, H=64, Top-512 of 16384 entries):
     # the same kernel once the launch holds more than one token per SM group; two
     # rotating input sets whose gathered rows exceed L2

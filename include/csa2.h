@@ -248,6 +248,31 @@ csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H, int D, int
 size_t csa2_sparse_attn_workspace_bytes(int B, int T, int H, int D, int dv, int K);
 
 /*
+ * csa2_swa_attn_fp8 -- the sliding-window branch over an FP8 window KV,
+ * merged with the sparse branch.  [ENG] "效率组件四件" item 4 (the SWA KV stays
+ * FP8); [HUNT] (every layer also has a sliding window).  The pages give neither
+ * the window size nor the FP8 layout; READINGS: window rows are E4M3 without a
+ * scale, K = all D channels, V = the first dv (as the sparse branch), and query
+ * row (b, t) attends to the first swa_len[b*T+t] rows of sequence b's window
+ * (all visible: the caller keeps the last window of tokens there).  The
+ * merge is the softmax over both branches' entries:
+ *     M = max(lse_w, lse_s), a = e^(lse_w - M), c = e^(lse_s - M),
+ *     out = (a o_w + c o_s) / (a + c),  lse = M + log(a + c).
+ *
+ * q          bf16 [B, T, H, D], D = 576, dv = 512, H a multiple of 64.
+ * swa_kv     E4M3 [B, W, D], 1 <= W <= 512, 16-byte aligned.
+ * swa_len    int32 [B*T], clamped to [0, W].
+ * o_sparse, lse_sparse  fp32 [B, T, H, dv] and [B, T, H] from
+ *            csa2_sparse_attn_fp4, or both NULL (window branch alone).
+ * out        fp32 [B, T, H, dv]; may be o_sparse itself (merged in place).
+ * lse        fp32 [B, T, H] merged log-sum-exp, or NULL.
+ * An empty window with lse_s = -inf gives out = 0, lse = -inf.
+ */
+csa2_status csa2_swa_attn_fp8(int B, int T, int H, int D, int dv, const void *q, const uint8_t *swa_kv, int W,
+                              const int32_t *swa_len, float sm_scale, const float *o_sparse, const float *lse_sparse,
+                              float *out, float *lse, uint32_t *err_flag, csa2_stream_t stream);
+
+/*
  * csa2_sparse_attn_fp4_noalloc -- csa2_sparse_attn_fp4 without a caller
  * workspace.  The pages have no counterpart to this call: it exists for
  * callers that may not allocate device memory at all, such as an engine that

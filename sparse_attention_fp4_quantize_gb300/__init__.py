@@ -54,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "csa2_sparse_attn_fp4": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P, P,
                                   P, u64, P], i32),
         "csa2_sparse_attn_workspace_bytes": ([i32, i32, i32, i32, i32, i32], u64),
+        "csa2_swa_attn_fp8": ([i32, i32, i32, i32, i32, P, P, i32, P, f32, P, P, P, P, P, P], i32),
         "csa2_sparse_attn_fp4_noalloc": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P,
                                           P, P], i32),
         "csa2_sparse_attn_noalloc_max_scratch_bytes": ([], u64),
@@ -73,7 +74,7 @@ _lib = _load()
 
 def exported_symbols():
     return ["csa2_quantize_kv_fp4", "csa2_rope_quantize_kv_fp4", "csa2_index_score", "csa2_build_pool", "csa2_build_pool_workspace_bytes",
-            "csa2_topk", "csa2_topk_workspace_bytes", "csa2_index_topk", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes",
+            "csa2_topk", "csa2_topk_workspace_bytes", "csa2_index_topk", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes", "csa2_swa_attn_fp8",
             "csa2_sparse_attn_fp4_noalloc", "csa2_sparse_attn_noalloc_max_scratch_bytes",
             "csa2_status_string", "csa2_last_error", "csa2_version"]
 
@@ -181,6 +182,19 @@ def csa2_index_topk(mode, q_idx, w, k_idx, kv_len, idx, pool_blocks=None, pool_o
     _check(_lib.csa2_index_topk(int(mode), B, T, N, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), _ptr(k_idx),
                                 _dtype_code(k_idx), _ptr(kv_len), _ptr(pool_blocks), P, idx.shape[-1], _ptr(idx),
                                 _ptr(pool_out), P_out, _ptr(err_flag), _stream(stream)))
+
+
+def csa2_swa_attn_fp8(q, swa_kv, swa_len, out, sm_scale, o_sparse=None, lse_sparse=None, lse=None, err_flag=None,
+                      stream=None):
+    """Sliding-window branch: q bf16 [B,T,H,D], swa_kv E4M3 [B,W,D] (uint8 or
+    float8_e4m3fn), swa_len int32 [B*T] -> out fp32 [B,T,H,dv] (and lse),
+    merged with (o_sparse, lse_sparse) when given; out may be o_sparse."""
+    _cuda(q, swa_kv, swa_len, out, o_sparse, lse_sparse, lse, err_flag)
+    B, T, H, D = q.shape
+    W = swa_kv.shape[1]
+    _check(_lib.csa2_swa_attn_fp8(B, T, H, D, out.shape[-1], _ptr(q), _ptr(swa_kv), W, _ptr(swa_len),
+                                  float(sm_scale), _ptr(o_sparse), _ptr(lse_sparse), _ptr(out), _ptr(lse),
+                                  _ptr(err_flag), _stream(stream)))
 
 
 def csa2_sparse_attn_workspace_bytes(B, T, H, D, dv, K) -> int:

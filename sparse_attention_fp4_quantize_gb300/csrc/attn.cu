@@ -611,3 +611,25 @@ extern "C" csa2_status csa2_sparse_attn_fp4_noalloc(csa2_mode mode, int B, int T
     return csa2_sparse_attn_fp4(mode, B, T, H, D, dv, q, codes, scales, N, idx, K, kv_len, sm_scale, out, out_dt,
                                 lse, err_flag, scratch, need > 0 ? kNoAllocScratchBytes : 0, stream);
 }
+
+extern "C" csa2_status csa2_swa_attn_fp8(int B, int T, int H, int D, int dv, const void *q, const uint8_t *swa_kv, int W,
+                                         const int32_t *swa_len, float sm_scale, const float *o_sparse,
+                                         const float *lse_sparse, float *out, float *lse, uint32_t *err_flag,
+                                         csa2_stream_t stream) {
+    clear_error();
+    CSA2_REQUIRE(B >= 0 && T >= 0 && H >= 0, "swa_attn: negative shape");
+    CSA2_REQUIRE(W >= 1 && W <= 512, "swa_attn: window capacity W=%d not in [1,512]", W);
+    if (!(D == 576 && dv == 512 && H % 64 == 0)) {
+        set_error("swa_attn: unsupported (D=%d, dv=%d, H=%d): D=576, dv=512, H a multiple of 64", D, dv, H);
+        return CSA2_ERR_UNSUPPORTED;
+    }
+    CSA2_REQUIRE((o_sparse == nullptr) == (lse_sparse == nullptr), "swa_attn: o_sparse and lse_sparse go together");
+    if ((int64_t)B * T == 0 || H == 0) return CSA2_OK;
+    CSA2_REQUIRE(q && swa_kv && swa_len && out, "swa_attn: null pointer");
+    CSA2_REQUIRE(aligned(q, 16) && aligned(swa_kv, 16) && aligned(out, 16) && aligned(swa_len, 4) &&
+                     aligned(o_sparse, 16) && aligned(lse_sparse, 4) && aligned(lse, 4),
+                 "swa_attn: q, swa_kv, out, o_sparse need 16-byte alignment");
+    CSA2_REQUIRE((int64_t)B * T <= 0x7FFFFFFFLL, "swa_attn: too many query tokens");
+    return launch_swa_attn_tc(B, T, H, q, swa_kv, W, swa_len, sm_scale, o_sparse, lse_sparse, out, lse, err_flag,
+                              stream_of(stream));
+}

@@ -71,7 +71,8 @@ constexpr uint32_t OFF_W = OFF_L + HB * 4;        // float[MAX_S][64] merge weig
 constexpr uint32_t OFF_LSE = OFF_W + MAX_S * HB * 4;      // float[64]
 constexpr uint32_t OFF_IL = OFF_LSE + HB * 4;             // float[64] 1 / row sum
 constexpr uint32_t OFF_STATS = OFF_IL + HB * 4;           // float[MAX_S][2][64] every CTA's (max, sum)
-constexpr uint32_t SMEM = OFF_STATS + MAX_S * 2 * HB * 4;
+constexpr uint32_t OFF_BETA = OFF_STATS + MAX_S * 2 * HB * 4;   // float[64] sparse-branch weight (FP8W merge)
+constexpr uint32_t SMEM = OFF_BETA + HB * 4;
 // Merge payload: the normalised partial O (O / L) of W channels as f16 rows of
 // RSH halves (136 bytes: 8-byte accesses by consecutive channels are
 // conflict-free).
@@ -101,7 +102,24 @@ struct TcArgs {
     float *out;
     float *lse;
     uint32_t *err_flag;
+    // sliding-window branch (FP8W): E4M3 rows [B, W, D], the first swa_len[bt]
+    // of them attended; merged with the sparse branch's (o_sparse, lse_sparse)
+    const uint8_t *kv8;
+    int W;
+    const int32_t *swa_len;
+    const float *o_sparse;
+    const float *lse_sparse;
 };
+
+// 16 E4M3 bytes -> 16 f16 (exact), as 8 f16x2 words.
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4 v, uint32_t (&r)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r[2 * k]) : "h"((uint16_t)(w[k] & 0xFFFFu)));
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r[2 * k + 1]) : "h"((uint16_t)(w[k] >> 16)));
+    }
+}
 
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
     uint32_t r;
@@ -139,9 +157,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
@@ -157,8 +172,11 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_remote, uint32_t src_local
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
+// FP8W = false: the sparse branch (FP4 entries gathered by idx).  FP8W = true:
+// the sliding-window branch (the first swa_len E4M3 rows of the window,
+// contiguous, no scales) merged at the end with the sparse branch's output.
+template <bool FP8W>
 __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     cg::cluster_group cluster = cg::this_cluster();
@@ -176,7 +194,6 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     uint8_t *sQ = smem + OFF_Q;
     float *sT = reinterpret_cast<float *>(smem + OFF_ST);
     uint8_t *sP = smem + OFF_P;
-    float *sRecv = reinterpret_cast<float *>(smem + OFF_K);  // received partial O after P V
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     int *sValid = reinterpret_cast<int *>(smem + OFF_VALID);
     float *sCs = reinterpret_cast<float *>(smem + OFF_CS);
@@ -186,6 +203,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     float *sLse = reinterpret_cast<float *>(smem + OFF_LSE);
     float *sIL = reinterpret_cast<float *>(smem + OFF_IL);
     float *sStats = reinterpret_cast<float *>(smem + OFF_STATS);
+    float *sBeta = reinterpret_cast<float *>(smem + OFF_BETA);
     const uint32_t bar_q = tc::smem_u32(smem + OFF_BAR);   // Q rows landed
     const uint32_t bar_ld = bar_q + 8;                       // code rows landed
     const uint32_t bar_s = bar_q + 16;                       // S MMA done
@@ -210,9 +228,16 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     // cluster barrier, first half: this CTA runs; the wait comes before the first remote store
     if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     pdl_wait();   // the set-up above overlaps the previous kernel's tail
-    const int64_t j = (sel < a.K) ? (int64_t)__ldg(a.idx + bt * a.K + sel) : -1;   // this thread's entry
-    int64_t len = a.kv_len ? (int64_t)a.kv_len[bt] : a.N;
-    len = len < a.N ? len : a.N;
+    int64_t j, len;
+    if constexpr (FP8W) {   // window row sel of the first swa_len
+        len = a.swa_len[bt];
+        len = len < a.W ? (len > 0 ? len : 0) : a.W;
+        j = sel < len ? sel : -1;
+    } else {
+        j = (sel < a.K) ? (int64_t)__ldg(a.idx + bt * a.K + sel) : -1;   // this thread's entry
+        len = a.kv_len ? (int64_t)a.kv_len[bt] : a.N;
+        len = len < a.N ? len : a.N;
+    }
 
     // ---- 1. gather: TMA bulk copies of Q rows and the selected code rows
     if (qt == 0 && e < HB) {        // Q rows do not depend on the indices: first
@@ -224,16 +249,30 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     if (qt == 0) {
         if (!valid && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
         sValid[e] = valid ? 1 : 0;
-        mbar_arrive_expect_tx(bar_ld, valid ? D / 2 : 0);
-        if (valid)
+        mbar_arrive_expect_tx(bar_ld, (valid && !FP8W) ? D / 2 : 0);
+        if (valid && !FP8W)
             bulk_g2s(tc::smem_u32(smem + OFF_CRAW + e * CRAW_STRIDE), a.codes + (b * a.N + j) * (D / 2), D / 2, bar_ld);
+    }
+    // FP8W: this thread's nine 16-byte groups of its window row, loaded now (their
+    // latency overlaps the Q conversion); the same group split as below
+    uint4 w8[2][5];
+    if constexpr (FP8W) {
+        const uint8_t *row = a.kv8 + (b * a.W + (valid ? j : 0)) * (int64_t)D;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int qh = (qt + 2 * h) & 3, nh = qh < 2 ? 5 : 4;
+#pragma unroll
+            for (int i = 0; i < 5; ++i)
+                w8[h][i] = (valid && i < nh) ? __ldg(reinterpret_cast<const uint4 *>(row + 16 * (18 * h + qh + 4 * i)))
+                                              : make_uint4(0, 0, 0, 0);
+        }
     }
     // the entry's 36 scale bytes as 9 words (consumed only by the dequantiser, so
     // their latency overlaps the Q conversion)
     uint32_t sw[9];
 #pragma unroll
     for (int i = 0; i < 9; ++i) sw[i] = 0u;
-    if (valid) {
+    if (valid && !FP8W) {
         const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + (b * a.N + j) * (D / 16));
 #pragma unroll
         for (int i = 0; i < 9; ++i) sw[i] = __ldg(srow + i);
@@ -286,8 +325,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     // second half is dequantised.  In half h the thread takes local groups
     // qh, qh + 4, ... (< 18) with qh = (qt + 2h) mod 4: nine groups in all.
     ok = tc::mbar_wait(bar_ld, 0, MAX_POLLS) && ok;
-    uint2 cw[2][5];   // per half: up to five groups, 8 code bytes (16 channels) each
-    {
+    uint2 cw[2][5] = {};   // per half: up to five groups, 8 code bytes (16 channels) each
+    if constexpr (!FP8W) {
         const uint8_t *craw = smem + OFF_CRAW + e * CRAW_STRIDE;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -311,7 +350,9 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
                 const uint32_t word = h == 0 ? sw[i] : ((qh >> 1) ? sw[i < 4 ? 5 + i : 8] : sw[4 + i]);
                 const int byte = h == 0 ? qh : ((2 + qh) & 3);
                 uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                if (valid) {
+                if (FP8W) {
+                    e4m3x16_to_f16(w8[h][i], r);   // zero bytes for an invalid entry
+                } else if (valid) {
                     const uint32_t sc = e4m3_to_f16x2_bcast((word >> (8 * byte)) & 0xFFu);
 #pragma unroll
                     for (int bb = 0; bb < 4; ++bb) {
@@ -510,6 +551,26 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         for (int c = 0; c < MAX_S; ++c)
             if (c < S) sW[c * HB + tid] *= inv;
         sLse[tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+        if constexpr (FP8W) {
+            // merge with the sparse branch: the softmax over both branches' entries
+            float beta = 0.f;
+            if (a.o_sparse) {
+                const float lw = sLse[tid], ls = a.lse_sparse[(bt * a.H) + h0 + tid];
+                const float mx = fmaxf(lw, ls);
+                float alpha = 0.f, lo = -INFINITY;
+                if (mx != -INFINITY) {
+                    const float ea = expf(lw - mx), eb = expf(ls - mx);
+                    alpha = ea / (ea + eb);
+                    beta = eb / (ea + eb);
+                    lo = mx + logf(ea + eb);
+                }
+#pragma unroll
+                for (int c = 0; c < MAX_S; ++c)
+                    if (c < S) sW[c * HB + tid] *= alpha;
+                sLse[tid] = lo;
+            }
+            sBeta[tid] = beta;
+        }
     }
     for (int o = (S > 1 ? 1 : 0); o < S; ++o) {
         stage_slice(o);
@@ -551,6 +612,11 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
                 }
             }
             float *o = a.out + ((bt * a.H) + h0 + 8 * h8) * (int64_t)DV + c_lo + c;
+            if (FP8W && a.o_sparse) {
+                const float *os = a.o_sparse + ((bt * a.H) + h0 + 8 * h8) * (int64_t)DV + c_lo + c;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] += sBeta[8 * h8 + i] * os[i * DV];   // os may alias o
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) o[i * DV] = acc[i];
         }
@@ -566,20 +632,15 @@ bool sparse_attn_tc_supported(int D_, int dv, int H, int K) {
     return D_ == D && dv == DV && H % HB == 0 && K >= 1 && K <= MAX_S * TM;
 }
 
-csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const void *q, const uint8_t *codes,
-                                  const uint8_t *scales, const int32_t *idx, const int32_t *kv_len, float sm_scale,
-                                  float *out, float *lse, uint32_t *err_flag, cudaStream_t stream) {
+template <bool FP8W>
+static csa2_status launch_tc(TcArgs &a, int B, int entries, cudaStream_t stream) {
     static bool smem_set[64];
-    CSA2_CUDA_CALL(ensure_smem_limit((const void *)sparse_attn_tc_kernel, (int)SMEM, smem_set),
+    CSA2_CUDA_CALL(ensure_smem_limit((const void *)sparse_attn_tc_kernel<FP8W>, (int)SMEM, smem_set),
                    "sparse_attn_tc: smem attribute");
-    TcArgs a;
-    a.T = T; a.H = H; a.K = K; a.N = N;
-    const int tiles = (K + TM - 1) / TM;
+    const int tiles = (entries + TM - 1) / TM;
     a.csize = tiles <= 1 ? 1 : (tiles <= 2 ? 2 : 4);   // 1, 2 or 4: the channel slices divide 512
-    a.hblocks = H / HB;
-    a.q = (const uint16_t *)q; a.codes = codes; a.scales = scales; a.idx = idx; a.kv_len = kv_len;
-    a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.err_flag = err_flag;
-    const int64_t grid = (int64_t)B * T * a.hblocks * a.csize;
+    a.hblocks = a.H / HB;
+    const int64_t grid = (int64_t)B * a.T * a.hblocks * a.csize;
     if (grid > 0x7FFFFFFF) {
         set_error("sparse_attn_tc: grid too large");
         return CSA2_ERR_UNSUPPORTED;
@@ -597,9 +658,29 @@ csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const v
     attr[1] = pdl_attribute();
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    CSA2_CUDA_CALL(cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel, a), "sparse_attn_tc_kernel launch");
+    CSA2_CUDA_CALL(cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<FP8W>, a), "sparse_attn_tc_kernel launch");
     CSA2_LAUNCH_CHECK("sparse_attn_tc_kernel");
     return CSA2_OK;
+}
+
+csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const void *q, const uint8_t *codes,
+                                  const uint8_t *scales, const int32_t *idx, const int32_t *kv_len, float sm_scale,
+                                  float *out, float *lse, uint32_t *err_flag, cudaStream_t stream) {
+    TcArgs a = {};
+    a.T = T; a.H = H; a.K = K; a.N = N;
+    a.q = (const uint16_t *)q; a.codes = codes; a.scales = scales; a.idx = idx; a.kv_len = kv_len;
+    a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.err_flag = err_flag;
+    return launch_tc<false>(a, B, K, stream);
+}
+
+csa2_status launch_swa_attn_tc(int B, int T, int H, const void *q, const uint8_t *kv8, int W, const int32_t *swa_len,
+                               float sm_scale, const float *o_sparse, const float *lse_sparse, float *out, float *lse,
+                               uint32_t *err_flag, cudaStream_t stream) {
+    TcArgs a = {};
+    a.T = T; a.H = H; a.K = W; a.N = W;
+    a.q = (const uint16_t *)q; a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.err_flag = err_flag;
+    a.kv8 = kv8; a.W = W; a.swa_len = swa_len; a.o_sparse = o_sparse; a.lse_sparse = lse_sparse;
+    return launch_tc<true>(a, B, W, stream);
 }
 
 }  // namespace csa2

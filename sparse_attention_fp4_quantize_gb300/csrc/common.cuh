@@ -65,6 +65,9 @@ bool sparse_attn_tc_supported(int D, int dv, int H, int K);
 csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const void *q, const uint8_t *codes,
                                   const uint8_t *scales, const int32_t *idx, const int32_t *kv_len, float sm_scale,
                                   float *out, float *lse, uint32_t *err_flag, cudaStream_t stream);
+csa2_status launch_swa_attn_tc(int B, int T, int H, const void *q, const uint8_t *kv8, int W, const int32_t *swa_len,
+                               float sm_scale, const float *o_sparse, const float *lse_sparse, float *out, float *lse,
+                               uint32_t *err_flag, cudaStream_t stream);
 
 // tcgen05 prefill scoring (index_score_tc.cu): FP8, Full mode, T >= 64.
 bool index_score_prefill_tc_supported(int T, csa2_dtype dt);
