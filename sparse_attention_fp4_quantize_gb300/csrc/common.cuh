@@ -86,8 +86,8 @@ __device__ __forceinline__ uint32_t score_key(float f) {
     return (k <= 0x007FFFFFu) ? 0u : k;
 }
 
-// Programmatic dependent launch.  The library's kernels (all but the Top-K
-// kernel) are launched with programmatic stream serialization allowed, so
+// Programmatic dependent launch.  The library's kernels (all but the
+// standalone Top-K) are launched with programmatic stream serialization allowed, so
 // they may start while the previous kernel on the stream drains.  Before
 // pdl_wait() a kernel touches only its own shared memory, TMEM and barriers;
 // pdl_wait() returns once the previous grid has completed with its memory
