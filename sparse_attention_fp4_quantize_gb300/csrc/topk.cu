@@ -390,9 +390,6 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t4 = lane & 3;
     const bool full = a.mode == CSA2_MODE_FULL;
-    const int64_t beg = (int64_t)cta * a.chunk;
-    int nm = 0;
-    if (beg < a.M) nm = (int)((a.M - beg) < a.chunk ? (a.M - beg) : a.chunk);
     reset_fine(sm);
     if (C > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     pdl_wait();
@@ -400,6 +397,19 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
     // ---------------------------------------------------------------- score this slice
     int64_t len = a.kv_len[row];
     len = len < a.N ? (len > 0 ? len : 0) : a.N;
+    // Full: the row's len valid positions are shared evenly by the cluster (slices of a
+    // multiple of 128, in position order); Reindex: the 8P pool candidates, chunk by chunk
+    int64_t beg, share;
+    if (full) {
+        share = (((len + C - 1) / C) + 127) & ~int64_t(127);
+        if (share > a.chunk) share = a.chunk;   // cannot happen: len <= M
+    } else {
+        share = a.chunk;
+    }
+    beg = (int64_t)cta * share;
+    const int64_t lim = full ? len : a.M;
+    int nm = 0;
+    if (beg < lim) nm = (int)((lim - beg) < share ? (lim - beg) : share);
     const int64_t nblocks_n = (a.N + 7) / 8;
     const uint4 q8 = (g < 4) ? __ldg(reinterpret_cast<const uint4 *>(a.q + (row * 4 + g) * 64 + 16 * t4))
                              : make_uint4(0, 0, 0, 0);
