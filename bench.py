@@ -515,7 +515,8 @@ def run_gpu(args):
             "frac": (achieved / peak) if achieved else None,
             "peak_kind": "burst copy (%s; the kernel is timed alone)" % peak_kind,
             "algorithmic_bytes_per_launch": ab,
-            "traffic": _traffic_record({"sparse_attn": "sparse_attn_tc_kernel", "index_score": "index_score_decode_kernel", "topk": "topk_radix_kernel"}.get(kname, kname)),
+            "traffic": _traffic_record({"sparse_attn": "sparse_attn_tc_kernel", "index_topk": "index_topk_kernel",
+                                        "quantize": "quantize_fp4_kernel"}.get(kname, kname)),
             "avg_launch_us": dom[1]["avg_s"] * 1e6}
     path_bytes = alg["keys"] + alg["gathered"] + alg["outputs"]
 
