@@ -9,10 +9,10 @@
 //
 // Decode-shaped (few query tokens per sequence): the work is a stream over
 // the 64-byte keys, so one warp takes 16 keys at a time and puts them on the
-// tensor cores as the A operand of mma.m16n8k16 (f16 inputs, fp32
-// accumulation).  FP8 E4M3 values convert to f16 exactly and their products
-// are exact, so only the fp32 accumulation rounds.  The B operand holds the 4
-// heads of up to two query tokens of the same sequence (8 columns).
+// tensor cores as the A operand of an MMA with fp32 accumulation: FP8 keys
+// and queries go straight into mma.m16n8k32 (e4m3 x e4m3; the products are
+// exact), bf16 ones into mma.m16n8k16.  The B operand holds the 4 heads of up
+// to two query tokens of the same sequence (8 columns).
 //
 // The dot product sums over d, so the k-order inside the MMA is free: lane
 // (g, t) of the warp loads bytes [16t, 16t+16) of key rows g and g+8 with one

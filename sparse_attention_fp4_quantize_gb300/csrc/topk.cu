@@ -1,4 +1,5 @@
-// csa2_topk and csa2_build_pool: per-row Top-K by radix select.
+// csa2_topk, csa2_build_pool and the fused decode indexer csa2_index_topk:
+// per-row Top-K by radix select.
 // Sources: "DeepSeek-V4.1-Flash：把 KV Cache 压缩到极限的百万上下文 MoE", CSA2
 // section (Top-512 in every layer) and "Hierarchical Sparse Indexer" (a pool
 // of at most 2048 blocks x 8 positions built from block scores);
@@ -10,17 +11,21 @@
 // shared memory as order-preserving uint32 keys.  The K-th largest key of the
 // row is then found by a radix select over the whole cluster: for each digit
 // (bits 31..21, 20..10, 9..0) every CTA histograms its slice into 2048 fine
-// and 64 coarse bins, one cluster barrier publishes the histograms, and every
-// warp of every CTA locates the boundary bin itself by reading the cluster's
-// coarse bins and then the 32 fine bins of the boundary coarse bin through
-// distributed shared memory, so nothing waits for another CTA's answer.  A
-// digit ends the search early when the boundary bin is taken whole (random
-// float scores need two digits).  The selection is then compacted in
-// position order across the cluster: every warp publishes its counts above
-// and at the threshold, one more barrier lets each warp sum the counts before
-// it, and each CTA writes its own ids straight to the output.  Ties at the
-// K-th value go to the lowest positions.  Only hardware barriers are used: no
-// flag spinning.
+// and 64 coarse bins and pushes its coarse bins into every CTA; after one
+// cluster barrier every warp of every CTA locates the boundary bin itself
+// from the coarse bins and the 32 fine bins of the boundary coarse bin, read
+// from each CTA through distributed shared memory, so nothing waits for
+// another CTA's answer.  A digit ends the search early when the boundary bin
+// is taken whole (random float scores need two digits).  The selection is
+// then compacted in position order across the cluster: every warp pushes its
+// counts above and at the threshold into every CTA, one more barrier lets
+// each warp sum the counts before it, and each CTA writes its own ids straight
+// to the output.  Ties at the K-th value go to the lowest positions.  Only
+// hardware barriers are used: no flag spinning.
+//
+// The fused indexer scores its slice of candidates (FP8 keys, the decode
+// scorer's MMA tiling) straight into the same shared-memory keys, so the
+// scores of a decode row never reach HBM.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
