@@ -106,7 +106,9 @@ __device__ __forceinline__ uint32_t encode_word(uint32_t w, float inv) {
 }
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+// Units per thread per pass (UNR): 8 for large plain appends, 4 with RoPE
+// (where the position -> table load chain makes 8 slower), 2 for small
+// appends (a decode step's few hundred rows), which then spread over more SMs.
 
 // RoPE of the append path, fused ahead of the quantiser: interleaved pairs
 // (2i, 2i+1) of the last rope_dim channels rotated by a caller-supplied fp32
@@ -127,7 +129,7 @@ __device__ __forceinline__ uint32_t rope_word(uint32_t w, float2 cs) {
            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(rb)) << 16);
 }
 
-template <bool ROPE>
+template <bool ROPE, int UNR>
 __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(
     const uint16_t *__restrict__ kv, uint32_t total_units, FastDiv upr_div, int D, int64_t stride,
     int64_t row0, const int64_t *__restrict__ dst_slot, int64_t n_slots, uint8_t *__restrict__ codes,
@@ -137,6 +139,7 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(
     const int lane = threadIdx.x & 31;
     const uint32_t nthreads = gridDim.x * kThreads;
     const uint32_t upr = upr_div.d;
+    constexpr int kUnroll = UNR;
     // Warp-aligned base so that lane parity == unit parity (pairs share a group).
     for (uint32_t base = blockIdx.x * kThreads + (threadIdx.x & ~31u); base < total_units;
          base += nthreads * kUnroll) {
@@ -212,19 +215,19 @@ static csa2_status launch_quantize(const void *kv, int64_t rows, int D, int64_t 
     for (int64_t r0 = 0; r0 < rows; r0 += max_rows) {
         int64_t nr = rows - r0 < max_rows ? rows - r0 : max_rows;
         uint32_t units = (uint32_t)(nr * upr);
-        int64_t want = ((int64_t)units + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
+        // Small appends use the short unroll; large ones the long one (the
+        // grid then covers every SM several times over).
+        const bool small = (int64_t)units < (int64_t)num_sms() * kThreads * 16;
+        const int unr = small ? 2 : (rope ? 4 : 8);
+        const int64_t per_block = (int64_t)kThreads * unr;
+        int64_t want = ((int64_t)units + per_block - 1) / per_block;
         int blocks = (int)(want < max_blocks ? want : max_blocks);
         if (blocks < 1) blocks = 1;
-        if (rope)
-            CSA2_CUDA_CALL(launch_pdl(quantize_fp4_kernel<true>, dim3(blocks), dim3(kThreads), 0, stream_of(stream),
-                                      (const uint16_t *)kv, units, fd, D, kv_row_stride, r0, dst_slot, n_slots,
-                                      codes, scales, err_flag, ra),
-                           "quantize_fp4_kernel launch");
-        else
-            CSA2_CUDA_CALL(launch_pdl(quantize_fp4_kernel<false>, dim3(blocks), dim3(kThreads), 0, stream_of(stream),
-                                      (const uint16_t *)kv, units, fd, D, kv_row_stride, r0, dst_slot, n_slots,
-                                      codes, scales, err_flag, ra),
-                           "quantize_fp4_kernel launch");
+        auto kern = rope ? (small ? quantize_fp4_kernel<true, 2> : quantize_fp4_kernel<true, 4>)
+                         : (small ? quantize_fp4_kernel<false, 2> : quantize_fp4_kernel<false, 8>);
+        CSA2_CUDA_CALL(launch_pdl(kern, dim3(blocks), dim3(kThreads), 0, stream_of(stream), (const uint16_t *)kv,
+                                  units, fd, D, kv_row_stride, r0, dst_slot, n_slots, codes, scales, err_flag, ra),
+                       "quantize_fp4_kernel launch");
         CSA2_LAUNCH_CHECK("quantize_fp4_kernel");
     }
     return CSA2_OK;

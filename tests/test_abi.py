@@ -72,6 +72,20 @@ def test_quantize_rejects_bad_arguments_on_host(lib):
     assert f(NULL, 0, 64, 64, NULL, 0, NULL, NULL, NULL, NULL) == 0          # empty: no-op
 
 
+def test_rope_quantize_rejects_bad_arguments_on_host(lib):
+    f = lib.csa2_rope_quantize_kv_fp4
+    P = ctypes.c_void_p
+    f.argtypes = [P, I64, ctypes.c_int, I64, P, P, I64, ctypes.c_int, P, I64, P, P, P, P]
+    fake = P(0x1000)
+    assert f(fake, 4, 576, 576, fake, fake, 16, 24, NULL, 4, fake, fake, NULL, NULL) == 1   # rope_dim % 16
+    assert "rope_dim=24" in _last_error(lib)
+    assert f(fake, 4, 576, 576, fake, fake, 0, 64, NULL, 4, fake, fake, NULL, NULL) == 1    # empty table
+    assert f(fake, 4, 576, 576, fake, P(0x1004), 16, 64, NULL, 4, fake, fake, NULL, NULL) == 1  # table not 8-B aligned
+    assert "misaligned" in _last_error(lib)
+    assert f(fake, 4, 576, 576, P(0x1002), fake, 16, 64, NULL, 4, fake, fake, NULL, NULL) == 1  # pos misaligned
+    assert f(NULL, 0, 576, 576, NULL, NULL, 16, 64, NULL, 0, NULL, NULL, NULL, NULL) == 0   # empty: no-op
+
+
 def test_index_score_rejects_bad_arguments_on_host(lib):
     f = lib.csa2_index_score
     P = ctypes.c_void_p
