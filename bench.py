@@ -59,6 +59,18 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _bf16_peak_tflops():
+    """Measured dense bf16 burst rate (cuBLAS) from MEASURED_PEAKS.json, else
+    the fallback 1900 TFLOP/s."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        if j.get("bf16_tflops"):
+            return float(j["bf16_tflops"])
+    return 1900.0
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -338,6 +350,18 @@ def _extra_workloads(dev, stream, peak_gbs):
     idx4 = torch.empty(1, w4.T, 512, dtype=torch.int32, device=dev)
     t = _time_graph(lambda: csa2.csa2_topk(0, sc4, idx4, kv_len=kl4, stream=stream), stream, 5)
     res["prefill_topk_t4096_n32768"] = {"us": t * 1e6, "score_read_gbs": w4.T * w4.N * 4 / t / 1e9}
+    # the same Top-512 by the fused dense indexer (block maxima -> threshold -> candidates -> Top-K):
+    # two tensor-core scoring passes, no score matrix
+    ws4 = torch.empty(csa2.csa2_index_topk_dense_workspace_bytes(1, w4.T, w4.N, 512), dtype=torch.uint8, device=dev)
+    idx4d = torch.empty(1, w4.T, 512, dtype=torch.int32, device=dev)
+    t = _time_graph(lambda: csa2.csa2_index_topk_dense(q4, ww4, k4, kl4, idx4d, workspace=ws4, stream=stream),
+                    stream, 10)
+    fp8_peak = 2.0 * _bf16_peak_tflops()   # FP8 dense = 2 x the measured bf16 burst rate (nominal ratio)
+    res["prefill_index_topk_dense_t4096_n32768"] = {
+        "us": t * 1e6, "tflops": flops / t / 1e12, "passes": 2,
+        "fp8_peak_tflops": fp8_peak, "fp8_peak_frac": flops / t / 1e12 / fp8_peak,
+        "vs_unfused_us": res["prefill_score_t4096_n32768"]["us"] + res["prefill_topk_t4096_n32768"]["us"]}
+    del ws4, idx4d
     # the chunk's attention: 4096 queries x 64 heads over their Top-512 of the FP4 cache
     c4, s4 = gen.fp4_planes(w4.seed, 50, w4.N, 576, device=dev)
     qa4 = gen.normal_bf16(w4.seed, 51, (1, w4.T, 64, 576), device=dev)

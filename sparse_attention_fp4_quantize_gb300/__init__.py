@@ -8,6 +8,7 @@ CPU fallback: if the shared library is missing the import fails loudly.
 
 Names follow the C ABI: ``csa2_quantize_kv_fp4``, ``csa2_index_score``,
 ``csa2_build_pool``, ``csa2_topk``, ``csa2_index_topk`` (fused decode indexer),
+``csa2_index_topk_dense`` (fused indexer for many query tokens),
 ``csa2_sparse_attn_fp4`` and the
 ``*_workspace_bytes`` helpers.
 """
@@ -23,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 BF16, FP8_E4M3, FP32 = 0, 1, 2
-FLAG_BAD_INDEX, FLAG_BAD_POOL, FLAG_BAD_SLOT = 0x1, 0x2, 0x4
+FLAG_BAD_INDEX, FLAG_BAD_POOL, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLAG_OVERFLOW = 0x1, 0x2, 0x4, 0x8, 0x10
 INDEX_HEADS, INDEX_DIM, POOL_BLOCK, MAX_POOL, MAX_K = 4, 64, 8, 2048, 2048
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3: "CSA2_ERR_WORKSPACE",
@@ -51,6 +52,8 @@ def _load() -> ctypes.CDLL:
         "csa2_topk": ([i32, i32, i32, i64, P, P, P, i32, i32, P, P, u64, P], i32),
         "csa2_topk_workspace_bytes": ([i32, i32, i64, i32], u64),
         "csa2_index_topk": ([i32, i32, i32, i64, P, i32, P, P, i32, P, P, i32, i32, P, P, i32, P, P], i32),
+        "csa2_index_topk_dense": ([i32, i32, i64, P, i32, P, P, i32, P, i32, P, P, P, u64, P], i32),
+        "csa2_index_topk_dense_workspace_bytes": ([i32, i32, i64, i32], u64),
         "csa2_sparse_attn_fp4": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P, P,
                                   P, u64, P], i32),
         "csa2_sparse_attn_workspace_bytes": ([i32, i32, i32, i32, i32, i32], u64),
@@ -74,7 +77,8 @@ _lib = _load()
 
 def exported_symbols():
     return ["csa2_quantize_kv_fp4", "csa2_rope_quantize_kv_fp4", "csa2_index_score", "csa2_build_pool", "csa2_build_pool_workspace_bytes",
-            "csa2_topk", "csa2_topk_workspace_bytes", "csa2_index_topk", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes", "csa2_swa_attn_fp8",
+            "csa2_topk", "csa2_topk_workspace_bytes", "csa2_index_topk", "csa2_index_topk_dense",
+            "csa2_index_topk_dense_workspace_bytes", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes", "csa2_swa_attn_fp8",
             "csa2_sparse_attn_fp4_noalloc", "csa2_sparse_attn_noalloc_max_scratch_bytes",
             "csa2_status_string", "csa2_last_error", "csa2_version"]
 
@@ -182,6 +186,29 @@ def csa2_index_topk(mode, q_idx, w, k_idx, kv_len, idx, pool_blocks=None, pool_o
     _check(_lib.csa2_index_topk(int(mode), B, T, N, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), _ptr(k_idx),
                                 _dtype_code(k_idx), _ptr(kv_len), _ptr(pool_blocks), P, idx.shape[-1], _ptr(idx),
                                 _ptr(pool_out), P_out, _ptr(err_flag), _stream(stream)))
+
+
+def csa2_index_topk_dense_workspace_bytes(B, T, N, K) -> int:
+    return int(_lib.csa2_index_topk_dense_workspace_bytes(B, T, N, K))
+
+
+def csa2_index_topk_dense(q_idx, w, k_idx, kv_len, idx, workspace=None, err_flag=None, stream=None):
+    """Fused dense indexer for many query tokens (FP8, Full mode): the Top-K
+    of csa2_index_score's scores, as csa2_topk selects it, without the score
+    matrix.  q_idx [B,T,4,64], w fp32 [B,T,4], k_idx [B,N,64], kv_len int32
+    [B*T] -> idx int32 [B,T,K].  workspace: a CUDA byte tensor of at least
+    csa2_index_topk_dense_workspace_bytes(B, T, N, K) bytes (allocated here
+    when None)."""
+    _cuda(q_idx, w, k_idx, kv_len, idx, workspace, err_flag)
+    B, T = q_idx.shape[0], q_idx.shape[1]
+    N, K = k_idx.shape[1], idx.shape[-1]
+    if workspace is None:
+        workspace = torch.empty(max(1, csa2_index_topk_dense_workspace_bytes(B, T, N, K)), dtype=torch.uint8,
+                                device=idx.device)
+    ws = workspace.numel() * workspace.element_size()
+    _check(_lib.csa2_index_topk_dense(B, T, N, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), _ptr(k_idx),
+                                      _dtype_code(k_idx), _ptr(kv_len), K, _ptr(idx), _ptr(err_flag),
+                                      _ptr(workspace), ws, _stream(stream)))
 
 
 def csa2_swa_attn_fp8(q, swa_kv, swa_len, out, sm_scale, o_sparse=None, lse_sparse=None, lse=None, err_flag=None,
