@@ -706,10 +706,39 @@ def run_reference(args):
 
 
 def run_profile_case(args):
-    """One input set (about 3.6 GB on the device), three eager decode steps:
-    a small, self-terminating case for a full ncu capture of one kernel."""
+    """Small, self-terminating cases for full ncu captures of one kernel:
+    decode: one input set (about 3.6 GB on the device), three eager decode steps;
+    append: the 1,048,576-row quantise, twice (about 1.6 GB);
+    prefill: the 4096 x 32768 fused dense indexer, twice (about 0.3 GB)."""
     import torch
-    import sparse_attention_fp4_quantize_gb300  # noqa: F401
+    import gen
+    import sparse_attention_fp4_quantize_gb300 as csa2
+    case = args.profile_case
+    if case == "append":
+        w5 = gen.APPEND_POOL
+        R = w5.B * w5.N
+        rows = gen.kv_rows(w5.seed, 10, R, D, rms=False, device="cuda")
+        c = torch.empty(R, D // 2, dtype=torch.uint8, device="cuda")
+        s = torch.empty(R, D // 16, dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            csa2.csa2_quantize_kv_fp4(rows, c, s)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": "append_quantize_1m_rows", "calls": 2}))
+        return
+    if case == "prefill":
+        w4 = gen.PREFILL_CHUNK
+        q4, ww4, k4 = gen.indexer_inputs(w4, device="cuda")
+        kl4 = gen.kv_lengths(w4).to("cuda")
+        ws = torch.empty(csa2.csa2_index_topk_dense_workspace_bytes(1, w4.T, w4.N, K), dtype=torch.uint8,
+                         device="cuda")
+        idx = torch.empty(1, w4.T, K, dtype=torch.int32, device="cuda")
+        flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            csa2.csa2_index_topk_dense(q4, ww4, k4, kl4, idx, workspace=ws, err_flag=flag)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": "prefill_index_topk_dense_t4096_n32768", "calls": 2,
+                          "error_flag": int(flag.item())}))
+        return
     from sparse_attention_fp4_quantize_gb300.decode import DecoderStep, StepShape
     st = DecoderStep(StepShape(B=B, N=NCAP, D=D, dv=DV, H=H, K=K, P=P), device="cuda")
     _fill_instance(st, seed=1)
@@ -728,7 +757,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' timings")
-    ap.add_argument("--profile-case", action="store_true", help="3 eager steps on one input set (for ncu)")
+    ap.add_argument("--profile-case", nargs="?", const="decode", default=None, choices=["decode", "append", "prefill"],
+                    help="a small case for ncu: 3 eager decode steps (default), the 1M-row append, or the prefill indexer")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
