@@ -239,14 +239,18 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         len = len < a.N ? len : a.N;
     }
 
-    // ---- 1. gather: TMA bulk copies of Q rows and the selected code rows
-    if (qt == 0 && e < HB) {        // Q rows do not depend on the indices: first
+    // ---- 1. gather: TMA bulk copies of Q rows and the selected code rows.
+    // The copies of entry / head e are issued by the thread (e, qt) with
+    // qt = (e / 8) mod 4, which spreads them over all 16 warps (8 or 16 each):
+    // a warp issues its lanes' bulk copies one after another.
+    const bool issuer = qt == ((e >> 3) & 3);
+    if (issuer && e < HB) {        // Q rows do not depend on the indices: first
         const uint16_t *qrow = a.q + ((bt * a.H) + h0 + e) * (int64_t)D;
         mbar_arrive_expect_tx(bar_q, D * 2);
         bulk_g2s(tc::smem_u32(smem + OFF_QRAW + e * QRAW_STRIDE), qrow, D * 2, bar_q);
     }
     const bool valid = j >= 0 && j < len;
-    if (qt == 0) {
+    if (issuer) {
         if (!valid && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
         sValid[e] = valid ? 1 : 0;
         mbar_arrive_expect_tx(bar_ld, (valid && !FP8W) ? D / 2 : 0);
