@@ -326,6 +326,19 @@ def _extra_workloads(dev, stream, peak_gbs):
     res["append_rope_quantize_1m_rows"] = {"us": t * 1e6, "bytes": rbytes, "gbs": rbytes / t / 1e9,
                                           "hbm_frac": rbytes / t / 1e9 / peak_gbs}
     del rows, outs, tab, pos
+    # decode rows: Top-512 of 32 rows x 16384 scores, csa2_topk against torch.topk
+    w2 = gen.FULL_BATCHED_DECODE
+    q2, ww2, k2 = gen.indexer_inputs(w2, device=dev)
+    kl2 = gen.kv_lengths(w2).to(dev)
+    sc2 = torch.empty(w2.B, 1, w2.N, device=dev)
+    csa2.csa2_index_score(0, q2, ww2, k2, kl2, sc2, stream=stream)
+    i2 = torch.empty(w2.B, 1, 512, dtype=torch.int32, device=dev)
+    t_c = _time_graph(lambda: csa2.csa2_topk(0, sc2, i2, kv_len=kl2, stream=stream), stream, 50)
+    v2 = torch.empty(w2.B, 1, 512, device=dev)
+    x2 = torch.empty(w2.B, 1, 512, dtype=torch.int64, device=dev)
+    t_t = _time_graph(lambda: torch.topk(sc2, 512, dim=2, out=(v2, x2)), stream, 50)
+    res["topk_b32_n16384"] = {"csa2_us": t_c * 1e6, "torch_topk_us": t_t * 1e6, "csa2_topk_speedup": t_t / t_c}
+    del q2, ww2, k2, sc2, i2, v2, x2
     # pool for 16 x 65536 entries from Full scores
     q5, w5w, k5 = gen.indexer_inputs(w5, device=dev)
     kl5 = gen.kv_lengths(w5).to(dev)
@@ -350,6 +363,14 @@ def _extra_workloads(dev, stream, peak_gbs):
     idx4 = torch.empty(1, w4.T, 512, dtype=torch.int32, device=dev)
     t = _time_graph(lambda: csa2.csa2_topk(0, sc4, idx4, kv_len=kl4, stream=stream), stream, 5)
     res["prefill_topk_t4096_n32768"] = {"us": t * 1e6, "score_read_gbs": w4.T * w4.N * 4 / t / 1e9}
+    # context for the pages' DeepSelect claim (2-20x over torch.topk, no hardware stated): torch.topk on the
+    # same rows, here and on the decode rows below
+    vals = torch.empty(1, w4.T, 512, device=dev)
+    tix = torch.empty(1, w4.T, 512, dtype=torch.int64, device=dev)
+    t = _time_graph(lambda: torch.topk(sc4, 512, dim=2, out=(vals, tix)), stream, 5)
+    res["torch_topk_t4096_n32768"] = {"us": t * 1e6,
+                                      "csa2_topk_speedup": t * 1e6 / res["prefill_topk_t4096_n32768"]["us"]}
+    del vals, tix
     # the same Top-512 by the fused dense indexer (block maxima -> threshold -> candidates -> Top-K):
     # two tensor-core scoring passes, no score matrix
     ws4 = torch.empty(csa2.csa2_index_topk_dense_workspace_bytes(1, w4.T, w4.N, 512), dtype=torch.uint8, device=dev)

@@ -65,7 +65,6 @@ typedef enum { CSA2_BF16 = 0, CSA2_FP8_E4M3 = 1, CSA2_FP32 = 2 } csa2_dtype;
 #define CSA2_FLAG_BAD_POOL 0x2u   /* pool block id outside [-1, ceil(N/8))           */
 #define CSA2_FLAG_BAD_SLOT 0x4u   /* quantise dst_slot outside [0, n_slots)          */
 #define CSA2_FLAG_TIMEOUT 0x8u    /* a bounded on-chip wait gave up (results invalid)  */
-#define CSA2_FLAG_OVERFLOW 0x10u  /* a bounded candidate list overflowed (results invalid) */
 
 /* Fixed indexer shape: 4 heads of dimension 64, one 64-dim key per entry. */
 #define CSA2_INDEX_HEADS 4
@@ -220,24 +219,24 @@ csa2_status csa2_index_topk(csa2_mode mode, int B, int T, int64_t N, const void 
  * Sparse Indexer (Full layers score every entry, Top-512 per query); the
  * fusion and its passes are not on the pages.
  *
- * Exact by construction, in four kernels on the stream:
- *  1. tensor-core scoring, keeping only the maximum of each aligned block of
- *     8 positions;
- *  2. per query, tau = the K-th largest block maximum (0 = none when fewer
- *     than K blocks hold a visible position).  K blocks reach tau, so the
- *     K-th largest score is >= tau, and fewer than K blocks exceed it, so at
- *     most 8(K-1) scores exceed tau;
- *  3. tensor-core scoring again (the same fp32 values), keeping the
- *     positions whose score exceeds tau and up to K of those equal to it;
- *  4. per query, the Top-K of those candidates.
+ * Two kernels on the stream:
+ *  1. tensor-core scoring of every (query, key), keeping only the maximum of
+ *     each aligned block of 8 positions;
+ *  2. per query, tau = the K-th largest block maximum and the K blocks that
+ *     reach it (ties at tau broken arbitrarily); every score outside them is
+ *     <= tau <= the K-th largest score, so the Top-K of the 8K scores inside
+ *     them (rescored from the FP8 keys) is a Top-K of the row.  The two
+ *     kernels may round a score differently in the last bits of fp32, which
+ *     can only move a selection among scores tied at the K-th value within
+ *     that rounding.
  * Selection rules, ties, -1 padding: those of csa2_topk (FULL).
  *
  * q_idx FP8 E4M3 [B, T, 4, 64], w fp32 [B, T, 4], k_idx FP8 E4M3 [B, N, 64]
  * (both 16-byte aligned), kv_len int32 [B*T] (required), idx int32
  * [B, T, K], 1 <= K <= 2048, N <= 262144 (else CSA2_ERR_UNSUPPORTED).
  * workspace: csa2_index_topk_dense_workspace_bytes() bytes, 16-byte
- * aligned (block maxima, thresholds, candidate lists); too small:
- * CSA2_ERR_WORKSPACE.  err_flag: CSA2_FLAG_TIMEOUT, CSA2_FLAG_OVERFLOW.
+ * aligned (the block maxima, 4 bytes per 8 positions per query); too
+ * small: CSA2_ERR_WORKSPACE.  err_flag: CSA2_FLAG_TIMEOUT.
  */
 csa2_status csa2_index_topk_dense(int B, int T, int64_t N, const void *q_idx, csa2_dtype q_dt, const float *w,
                                   const void *k_idx, csa2_dtype k_dt, const int32_t *kv_len, int K, int32_t *idx,

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 BF16, FP8_E4M3, FP32 = 0, 1, 2
-FLAG_BAD_INDEX, FLAG_BAD_POOL, FLAG_BAD_SLOT, FLAG_TIMEOUT, FLAG_OVERFLOW = 0x1, 0x2, 0x4, 0x8, 0x10
+FLAG_BAD_INDEX, FLAG_BAD_POOL, FLAG_BAD_SLOT, FLAG_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 INDEX_HEADS, INDEX_DIM, POOL_BLOCK, MAX_POOL, MAX_K = 4, 64, 8, 2048, 2048
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3: "CSA2_ERR_WORKSPACE",

@@ -74,16 +74,11 @@ bool index_score_prefill_tc_supported(int T, csa2_dtype dt);
 csa2_status launch_index_score_prefill_tc(int B, int T, int64_t N, const void *q, const float *w, const void *k,
                                           const int32_t *kv_len, float *scores, uint32_t *err_flag,
                                           cudaStream_t stream);
-// The two passes of the fused dense indexer (same tiles and MMAs as above):
-// 8-key block-maximum keys [B*T, nblk], and the candidate lists at or above
-// tau (the filter pass reads the block maxima to skip blocks below tau).
+// The first pass of the fused dense indexer (same tiles and MMAs as above):
+// 8-key block-maximum keys [B*T, nblk].
 csa2_status launch_prefill_block_max(int B, int T, int64_t N, const void *q, const float *w, const void *k,
                                      const int32_t *kv_len, uint32_t *bmax, int64_t nblk, uint32_t *err_flag,
                                      cudaStream_t stream);
-csa2_status launch_prefill_filter(int B, int T, int64_t N, const void *q, const float *w, const void *k,
-                                  const int32_t *kv_len, const uint32_t *bmax, int64_t nblk, const uint32_t *tau,
-                                  uint32_t *cnt, uint2 *cand, int cap_gt, int cap_eq, uint32_t *err_flag,
-                                  cudaStream_t stream);
 
 // --------------------------------------------------------------- device side
 // Order-preserving map of an fp32 score to uint32: larger score -> larger key.

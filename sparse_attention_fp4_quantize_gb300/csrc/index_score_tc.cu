@@ -22,27 +22,19 @@
 // Key tiles beyond every query's kv_len skip the MMA and store -inf.  The
 // scores are fp32 [B, T, N]: this kernel is bound by writing them.
 //
-// The same main loop has two more epilogues, the passes of the fused dense
+// The same main loop has a second epilogue, the first pass of the fused dense
 // indexer (csa2_index_topk_dense) that never writes the score matrix:
-//  - BLOCKMAX: the order-preserving key of each 8-key block's maximum score.
-//    Three xor-shuffle steps reduce over the 8 lanes (= keys) of a block and
-//    transpose at the same time (each step keeps half of the queries), so
-//    one 32-lane store writes the 8 queries x 4 blocks of a warp;
-//  - FILTER: given each query's threshold tau (the K-th largest block
-//    maximum), every score at or above tau is appended by its lane to the
-//    query's list in shared memory; at the end of the work item one global
-//    atomic per query and list reserves room, and the entries go to the
-//    "above" list (key > tau) or the "tie" list (key == tau, first K kept).
-// Both recompute the score with the same instructions (explicit rounding,
-// no contraction choices left to the compiler), so the two passes see the
-// same fp32 values bit for bit.
+// BLOCKMAX keeps the order-preserving key of each 8-key block's maximum
+// score.  Three xor-shuffle steps reduce over the 8 lanes (= keys) of a block
+// and transpose at the same time (each step keeps half of the queries), so
+// one 32-lane store writes the 8 queries x 4 blocks of a warp.
 #include "common.cuh"
 #include "tc.cuh"
 
 namespace csa2 {
 namespace {
 
-enum { EPI_SCORES = 0, EPI_BLOCKMAX = 1, EPI_FILTER = 2 };
+enum { EPI_SCORES = 0, EPI_BLOCKMAX = 1 };
 
 constexpr int QT = 64;                 // queries per tile
 constexpr int QR = QT * 4;             // query-head rows (MMA N)
@@ -56,18 +48,11 @@ constexpr uint32_t SBO = 4 * 128;               // 8-row group stride (64 B rows
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
 constexpr uint32_t OFF_W = OFF_K + STAGES * K_BYTES;  // float[QT][4]
-constexpr uint32_t OFF_LT = OFF_W + QT * 16;          // int2[QT]: (kv_len clamped to N, tau as fp32 bits)
+constexpr uint32_t OFF_LT = OFF_W + QT * 16;          // int2[QT]: (kv_len clamped to N, 0)
 constexpr uint32_t OFF_BAR = OFF_LT + QT * 8;         // 2 mbarriers
 constexpr uint32_t OFF_TMEM = OFF_BAR + 16;
-// FILTER: each query's candidates of the current work item are staged in
-// shared memory (CAND_Q per query; more go straight to global memory) and
-// flushed with one global atomic per query at the end of the item.
-constexpr int CAND_Q = 128;
 constexpr uint32_t OFF_SMAX = OFF_TMEM + 8;              // int[2]: longest kv_len of the tile's queries
-constexpr uint32_t OFF_SCNT = OFF_TMEM + 16;             // uint32[QT]
-constexpr uint32_t OFF_STAUK = OFF_SCNT + QT * 4;        // uint32[QT]: tau keys (FILTER)
-constexpr uint32_t OFF_SCAND = OFF_STAUK + QT * 4;       // uint2[QT][CAND_Q]
-constexpr uint32_t SMEM_USED = OFF_SCAND + QT * CAND_Q * 8;
+constexpr uint32_t SMEM_USED = OFF_SMAX + 8;
 // request more than half of the SM's shared memory: one CTA per SM, so the
 // CTA's 512 TMEM columns are never contended
 constexpr uint32_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
@@ -88,12 +73,6 @@ struct PrefillArgs {
     // BLOCKMAX: keys of the 8-key block maxima, [B*T, nblk]
     uint32_t *bmax;
     int64_t nblk;
-    // FILTER: threshold key per query row, (gt, eq) counters per row and the
-    // candidate lists [B*T, cap_gt + cap_eq] of (key, position)
-    const uint32_t *tau;
-    uint32_t *cnt;
-    uint2 *cand;
-    int cap_gt, cap_eq;
 };
 
 // sum_h w_h * max(x_h, 0) with every rounding spelled out, so that each pass
@@ -103,29 +82,6 @@ __device__ __forceinline__ float head_sum(const float4 wq, const uint32_t *r) {
     s = __fmaf_rn(wq.y, fmaxf(__uint_as_float(r[1]), 0.f), s);
     s = __fmaf_rn(wq.z, fmaxf(__uint_as_float(r[2]), 0.f), s);
     return __fmaf_rn(wq.w, fmaxf(__uint_as_float(r[3]), 0.f), s);
-}
-
-// score_key of a finite score: -0 becomes +0, then the sign flip.
-__device__ __forceinline__ uint32_t finite_key(float s) {
-    const uint32_t u = __float_as_uint(__fadd_rn(s, 0.0f));
-    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
-}
-
-// One candidate (score key >= tau) of query ql, by its own lane: into the
-// query's shared staging list, or straight to the global lists when that is
-// full (above tau: list 0; equal: list 1, at most cap_eq kept).
-__device__ __forceinline__ void append_one(const PrefillArgs &a, uint32_t *sCnt, uint2 *sCand, int ql, int64_t row,
-                                           uint32_t key, uint32_t tau, uint32_t pos) {
-    const uint32_t slot = atomicAdd(sCnt + ql, 1u);
-    if (slot < (uint32_t)CAND_Q) {
-        sCand[ql * CAND_Q + slot] = make_uint2(key, pos);
-        return;
-    }
-    const int which = key == tau ? 1 : 0;
-    const uint32_t g = atomicAdd(a.cnt + row * 2 + which, 1u);
-    const uint32_t cap = which ? (uint32_t)a.cap_eq : (uint32_t)a.cap_gt;
-    if (g < cap) a.cand[row * (int64_t)(a.cap_gt + a.cap_eq) + (which ? a.cap_gt : 0) + g] = make_uint2(key, pos);
-    else if (!which) flag_error(a.err_flag, CSA2_FLAG_OVERFLOW);   // cannot happen when tau is the K-th block maximum
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
@@ -143,10 +99,7 @@ __global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(Pref
     const float4 *sW4 = reinterpret_cast<const float4 *>(smem + OFF_W);
     int2 *sLT = reinterpret_cast<int2 *>(smem + OFF_LT);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
-    uint32_t *sCnt = reinterpret_cast<uint32_t *>(smem + OFF_SCNT);
     int *sMax = reinterpret_cast<int *>(smem + OFF_SMAX);
-    uint32_t *sTauKey = reinterpret_cast<uint32_t *>(smem + OFF_STAUK);
-    uint2 *sCand = reinterpret_cast<uint2 *>(smem + OFF_SCAND);
     const uint32_t bar0 = tc::smem_u32(smem + OFF_BAR);
     const uint32_t sq = tc::smem_u32(smem + OFF_Q), sk = tc::smem_u32(smem + OFF_K);
     const float NEG_INF = __int_as_float(0xff800000);
@@ -157,7 +110,6 @@ __global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(Pref
         tc::mbar_init_fence();
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
-    if (EPI == EPI_FILTER && tid < QT) sCnt[tid] = 0u;
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -191,15 +143,7 @@ __global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(Pref
             for (int h = 0; h < 4; ++h) sW[tid * 4 + h] = v ? a.w[row * 4 + h] : 0.f;
             int64_t len = v ? (int64_t)a.kv_len[row] : 0;
             const int lc = (int)(len < 0 ? 0 : (len < a.N ? len : a.N));
-            int tf = __float_as_int(NEG_INF);   // tau as a float: every valid score is >= it
-            if (EPI == EPI_FILTER) {
-                const uint32_t tk = v ? a.tau[row] : 0xFFFFFFFFu;
-                sTauKey[tid] = tk;
-                // inverse of the key map; key 0 (no threshold) -> -inf, an absent query -> +inf (no hits)
-                if (!v) tf = 0x7f800000;
-                else if (tk != 0u) tf = (int)((tk & 0x80000000u) ? (tk & 0x7FFFFFFFu) : ~tk);
-            }
-            sLT[tid] = make_int2(lc, tf);
+            sLT[tid] = make_int2(lc, 0);
             const int m = __reduce_max_sync(0xFFFFFFFFu, lc);
             if (lane == 0) sMax[warp] = m;
         }
@@ -237,7 +181,7 @@ __global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(Pref
                 tc::fence_after();
             }
             // A skipped tile has no visible key for any query of the tile:
-            // nothing to write for the block maxima or the candidates.
+            // nothing to write for the block maxima.
             if (EPI != EPI_SCORES && !did_mma) return;
             const uint32_t ta = tmem + ((uint32_t)(32 * lq) << 16) + buf * 256 + 64 * qg;
             // eight queries of this warp's sixteen, from 32 TMEM columns.
@@ -246,28 +190,6 @@ __global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(Pref
             // chains interleave.
             auto eight = [&](const uint32_t (&r)[32], int h) {
                 const int q0 = 16 * qg + 8 * h;
-                if constexpr (EPI == EPI_FILTER) {
-                    // About K of a row's N scores are at or above tau.  The
-                    // test is a float compare against tau's value (-inf for
-                    // tau = 0), the same order as the keys; each hit lane
-                    // appends its own, above / equal are told apart at the
-                    // flush.
-                    const int64_t rowh = row0 + 8 * h;
-                    float s[8];
-                    bool hit[8];
-#pragma unroll
-                    for (int qq = 0; qq < 8; ++qq) {
-                        const float4 wq = sW4[q0 + qq];
-                        const int2 lt = sLT[q0 + qq];
-                        s[qq] = head_sum(wq, r + 4 * qq);
-                        hit[qq] = key < lt.x && s[qq] >= __int_as_float(lt.y);
-                    }
-#pragma unroll
-                    for (int qq = 0; qq < 8; ++qq)
-                        if (__any_sync(0xFFFFFFFFu, hit[qq]) && hit[qq])
-                            append_one(a, sCnt, sCand, q0 + qq, rowh + qq, finite_key(s[qq]), sTauKey[q0 + qq],
-                                       (uint32_t)key);
-                } else {
                 float s[8];
 #pragma unroll
                 for (int qq = 0; qq < 8; ++qq) {
@@ -306,7 +228,6 @@ __global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(Pref
                     const int qs = 4 * b0 + 2 * b1 + b2;
                     const int64_t blk = (key - lane + 8 * (lane >> 3)) >> 3;   // this lane's block
                     if (qs < nq && 8 * blk < a.N) a.bmax[(rowh + qs) * a.nblk + blk] = score_key(m);
-                }
                 }
             };
             if constexpr (EPI == EPI_SCORES) {
@@ -359,41 +280,6 @@ __global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(Pref
         }
         if (prev_tile >= 0) epilogue(prev_tile, prev_buf, prev_mma);
         cp_wait<0>();
-        if constexpr (EPI == EPI_FILTER) {
-            // flush the item's staged candidates: warp w takes queries w, w+16, w+32, w+48
-            __syncthreads();
-            for (int ql = warp; ql < QT; ql += THREADS / 32) {
-                const uint32_t n = min(sCnt[ql], (uint32_t)CAND_Q);
-                if (n == 0) continue;   // also every query past T
-                const int64_t row = b * a.T + t0 + ql;
-                const uint32_t tau = sTauKey[ql];
-                uint2 *dst = a.cand + row * (int64_t)(a.cap_gt + a.cap_eq);
-                for (uint32_t i0 = 0; i0 < n; i0 += 32) {
-                    const uint32_t i = i0 + lane;
-                    const uint2 c = i < n ? sCand[ql * CAND_Q + i] : make_uint2(0u, 0u);
-                    const uint32_t gt = __ballot_sync(0xFFFFFFFFu, i < n && c.x != tau);
-                    const uint32_t eq = __ballot_sync(0xFFFFFFFFu, i < n && c.x == tau);
-                    uint32_t bg = 0, be = 0;
-                    if (lane == 0) {
-                        if (gt) bg = atomicAdd(a.cnt + row * 2, (uint32_t)__popc(gt));
-                        if (eq) be = atomicAdd(a.cnt + row * 2 + 1, (uint32_t)__popc(eq));
-                    }
-                    bg = __shfl_sync(0xFFFFFFFFu, bg, 0);
-                    be = __shfl_sync(0xFFFFFFFFu, be, 0);
-                    const uint32_t below = (1u << lane) - 1u;
-                    if ((gt >> lane) & 1u) {
-                        const uint32_t j = bg + (uint32_t)__popc(gt & below);
-                        if (j < (uint32_t)a.cap_gt) dst[j] = c;
-                        else flag_error(a.err_flag, CSA2_FLAG_OVERFLOW);
-                    } else if ((eq >> lane) & 1u) {
-                        const uint32_t j = be + (uint32_t)__popc(eq & below);
-                        if (j < (uint32_t)a.cap_eq) dst[a.cap_gt + j] = c;
-                    }
-                }
-            }
-            __syncthreads();
-            if (tid < QT) sCnt[tid] = 0u;
-        }
     }
     if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
     tc::fence_before();
@@ -449,19 +335,5 @@ csa2_status launch_prefill_block_max(int B, int T, int64_t N, const void *q, con
     return launch_prefill<EPI_BLOCKMAX>(a, stream);
 }
 
-csa2_status launch_prefill_filter(int B, int T, int64_t N, const void *q, const float *w, const void *k,
-                                  const int32_t *kv_len, const uint32_t *bmax, int64_t nblk, const uint32_t *tau,
-                                  uint32_t *cnt, uint2 *cand, int cap_gt, int cap_eq, uint32_t *err_flag,
-                                  cudaStream_t stream) {
-    PrefillArgs a = prefill_args(B, T, N, q, w, k, kv_len, err_flag);
-    a.bmax = const_cast<uint32_t *>(bmax);   // read only in this pass
-    a.nblk = nblk;
-    a.tau = tau;
-    a.cnt = cnt;
-    a.cand = cand;
-    a.cap_gt = cap_gt;
-    a.cap_eq = cap_eq;
-    return launch_prefill<EPI_FILTER>(a, stream);
-}
 
 }  // namespace csa2

@@ -6,213 +6,254 @@
 // state what is selected.
 //
 // Why it is exact.  Split each query's visible positions into aligned blocks
-// of 8 and let tau be the K-th largest block maximum.  K blocks have a
-// maximum >= tau, so at least K scores are >= tau: the K-th largest score is
-// >= tau.  At most K-1 blocks have a maximum > tau, so at most 8(K-1) scores
-// are > tau.  The Top-K is therefore every score > tau plus (K minus their
-// count) of the scores equal to tau, and both sets fit in bounded lists.
+// of 8 and let tau be the K-th largest block maximum.  K blocks reach tau, so
+// the K-th largest score is >= tau; a score outside the K blocks whose
+// maximum is largest (ties at tau broken arbitrarily) is <= tau.  So the
+// Top-K of the scores inside those K blocks (8K candidates) is a Top-K of the
+// row, the same argument as the hierarchical pool's.  The rescoring below
+// uses the FP8 mma.sync tiling of the decode scorer while the block maxima
+// come from the tensor-core pass, so the two may round a score differently
+// in the last bits of fp32: a difference only at the K-th value, inside the
+// selection's tie band.
 //
 // Kernels, in stream order:
-//  1. index_score_prefill_tc_kernel<BLOCKMAX>: keys of the block maxima;
-//  2. dense_threshold_kernel: one warp per query, tau by a three-pass 11-bit
-//     radix select over the row's block maxima (staged in shared memory);
-//     also clears the query's candidate counters;
-//  3. index_score_prefill_tc_kernel<FILTER>: the same scores, appended to the
-//     "above" list (key > tau) or the "tie" list (key == tau, first K kept);
-//  4. dense_select_kernel: one warp per query, Top-K of the candidates (a
-//     four-pass 8-bit radix select when K or more lie above tau, else all of
-//     them, then ties, then -1).
+//  1. index_score_prefill_tc_kernel<BLOCKMAX>: keys of the 8-position block
+//     maxima, [B*T, nblk] (the dense tcgen05 pass over every (query, key));
+//  2. dense_rescore_kernel: one CTA per query.  The row's block maxima are
+//     staged in shared memory; tau and the K blocks by a block-wide radix
+//     select; the 8K candidates gathered (blocks are 512 contiguous bytes of
+//     keys) and rescored with FP8 mma.sync; the Top-K of their scores by the
+//     same radix select, written in any order, -1 padded.
 #include "common.cuh"
 
 namespace csa2 {
 namespace {
 
-constexpr int SEL_WARPS = 8;               // one warp per query row
-constexpr int SEL_THREADS = 32 * SEL_WARPS;
+constexpr int RS_THREADS = 256;
+constexpr int RS_WARPS = RS_THREADS / 32;
 constexpr int64_t MAX_N = 262144;
-
-// The K-th largest of n >= K >= 1 keys key_at(0 .. n-1), by one warp, in
-// radix passes of BITS-bit digits from the top (11: digits [31:21], [20:10],
-// [9:0]; 8: four bytes).  Each pass counts the digits of the keys that share
-// the prefix found so far in the warp's 2^BITS-bin shared histogram (plain
-// shared atomics: lanes that hit the same bin are serialised by the
-// hardware), then picks the bin where the count from the top reaches K.
-template <int BITS>
-__device__ __forceinline__ uint32_t warp_pick_bin(const uint32_t *hist, uint32_t k, uint32_t &before) {
-    constexpr int PER = (1 << BITS) / 32;   // bins per lane: lane l holds bins PER l .. PER l + PER - 1
-    const int lane = threadIdx.x & 31;
-    uint32_t own = 0;
-    const uint4 *h4 = reinterpret_cast<const uint4 *>(hist + PER * lane);
-#pragma unroll
-    for (int j = 0; j < PER / 4; ++j) {
-        const uint4 v = h4[j];
-        own += v.x + v.y + v.z + v.w;
-    }
-    uint32_t incl = own;   // inclusive suffix sum over lanes >= lane
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, incl, o);
-        if (lane + o < 32) incl += v;
-    }
-    const uint32_t above = incl - own;   // keys in the bins of the lanes above
-    const int L = __ffs(__ballot_sync(0xFFFFFFFFu, above < k && k <= above + own)) - 1;
-    const uint32_t aboveL = __shfl_sync(0xFFFFFFFFu, above, L);
-    // the warp scans lane L's PER bins together: lane j takes bins j*PER/32 ..
-    constexpr int SUB = PER >= 32 ? PER / 32 : 1;   // bins per lane in this scan
-    uint32_t cnt = 0;
-    if (SUB * lane < PER) {
-#pragma unroll
-        for (int j = 0; j < SUB; ++j) cnt += hist[PER * L + SUB * lane + j];
-    }
-    uint32_t inc2 = cnt;   // inclusive suffix sum over the bins of lanes >= lane
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, inc2, o);
-        if (lane + o < 32) inc2 += v;
-    }
-    const uint32_t ab2 = aboveL + inc2 - cnt;
-    const bool hit = SUB * lane < PER && ab2 < k && k <= ab2 + cnt;
-    const int M = __ffs(__ballot_sync(0xFFFFFFFFu, hit)) - 1;
-    uint32_t d = 0, b = 0;
-    if (lane == M) {
-        uint32_t c = ab2;
-#pragma unroll
-        for (int j = SUB - 1; j >= 0; --j) {
-            const uint32_t h = hist[PER * L + SUB * lane + j];
-            if (c + h >= k) {
-                d = (uint32_t)(PER * L + SUB * lane + j);
-                b = c;
-                break;
-            }
-            c += h;
-        }
-    }
-    before = __shfl_sync(0xFFFFFFFFu, b, M);
-    return __shfl_sync(0xFFFFFFFFu, d, M);
-}
-
-template <int BITS, typename KeyAt>
-__device__ uint32_t warp_kth_largest(KeyAt key_at, int n, int K, uint32_t *hist) {
-    constexpr int NB = 1 << BITS;
-    const int lane = threadIdx.x & 31;
-    uint32_t prefix = 0u, mask = 0u, k = (uint32_t)K;
-#pragma unroll 1
-    for (int shift = 32 - BITS; shift > -BITS; shift -= BITS) {
-        const int sh = shift < 0 ? 0 : shift;
-        const uint32_t dmask = (uint32_t)(NB - 1) >> (sh - shift);   // the last digit may be narrower
-        uint4 *h4 = reinterpret_cast<uint4 *>(hist);
-#pragma unroll
-        for (int j = 0; j < NB / 128; ++j) h4[32 * j + lane] = make_uint4(0u, 0u, 0u, 0u);
-        __syncwarp();
-        for (int base = 0; base < n; base += 128) {
-            uint32_t kk[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = base + 32 * j + lane;
-                kk[j] = i < n ? key_at(i) : 0u;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = base + 32 * j + lane;
-                if (i < n && (kk[j] & mask) == prefix) atomicAdd(&hist[(kk[j] >> sh) & dmask], 1u);
-            }
-        }
-        __syncwarp();
-        uint32_t before;
-        const uint32_t d = warp_pick_bin<BITS>(hist, k, before);
-        prefix |= d << sh;
-        mask |= dmask << sh;
-        k -= before;
-        __syncwarp();
-    }
-    return prefix;
-}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
 }
 
-// One warp per query row (blockDim.x / 32 rows per CTA).  The row's block
-// maxima (nblk words, nblk a multiple of 4: rows are 16-byte aligned) are
-// copied to the warp's slice of dynamic shared memory first, so the four
-// radix passes read shared memory.
-__global__ void __launch_bounds__(SEL_THREADS) dense_threshold_kernel(const uint32_t *__restrict__ bmax, int64_t nblk,
-                                                                      const int32_t *__restrict__ kv_len, int64_t N,
-                                                                      int rows, int K, uint32_t *__restrict__ tau,
-                                                                      uint32_t *__restrict__ cnt) {
-    extern __shared__ __align__(16) uint32_t dyn[];
-    pdl_wait();
-    pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nw = blockDim.x >> 5;
-    uint32_t *hist = dyn + (int64_t)nw * nblk + 2048 * warp;   // after the staged maxima
-    const int64_t r = (int64_t)blockIdx.x * nw + warp;
-    if (r >= rows) return;
-    int64_t len = kv_len[r];
-    len = len < 0 ? 0 : (len > N ? N : len);
-    const int nb = (int)((len + 7) / 8);
-    if (lane == 0) {
-        cnt[2 * r] = 0u;
-        cnt[2 * r + 1] = 0u;
-    }
-    uint32_t t = 0u;   // fewer than K blocks: every visible position is a candidate
-    if (nb >= K) {
-        uint32_t *sk = dyn + (int64_t)warp * nblk;
-        const uint32_t *row = bmax + r * nblk;
-        for (int i = lane; 4 * i < nb; i += 32) cp_async16((uint32_t)__cvta_generic_to_shared(sk + 4 * i), row + 4 * i);
-        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-        __syncwarp();
-        t = warp_kth_largest<11>([&](int i) { return sk[i]; }, nb, K, hist);
-    }
-    if (lane == 0) tau[r] = t;
+// Sum of one value per thread over the CTA (scratch: RS_WARPS words; the
+// caller's next barrier separates two uses).
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t *scratch) {
+    v = __reduce_add_sync(0xFFFFFFFFu, v);
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint32_t s = 0;
+#pragma unroll
+    for (int i = 0; i < RS_WARPS; ++i) s += scratch[i];
+    __syncthreads();
+    return s;
 }
 
-__global__ void __launch_bounds__(SEL_THREADS) dense_select_kernel(const uint32_t *__restrict__ cnt,
-                                                                   const uint2 *__restrict__ cand, int cap_gt,
-                                                                   int cap_eq, int rows, int K,
-                                                                   int32_t *__restrict__ idx) {
-    __shared__ __align__(16) uint32_t hist[SEL_WARPS][256];
+__device__ __forceinline__ uint32_t warp_suffix(uint32_t v) {   // sum over lanes >= lane
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, v, o);
+        if (lane + o < 32) v += y;
+    }
+    return v;
+}
+
+// The K-th largest of n >= K >= 1 keys in shared memory, by the whole CTA:
+// three radix passes over the digits [31:21], [20:10], [9:0].  Each pass
+// histograms the keys that share the prefix found so far (2048 shared bins,
+// shared atomics), then the thread whose 8 bins hold the K-th key from the
+// top publishes the bin.  scratch: at least RS_WARPS + 2 words.
+__device__ uint32_t block_kth_largest(const uint32_t *keys, int n, int K, uint32_t *hist, uint32_t *scratch) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t prefix = 0u, mask = 0u, k = (uint32_t)K;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const uint32_t dmask = pass == 2 ? 1023u : 2047u;
+        reinterpret_cast<uint4 *>(hist)[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4 *>(hist)[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+        for (int i = tid; i < n; i += RS_THREADS) {
+            const uint32_t key = keys[i];
+            if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dmask], 1u);
+        }
+        __syncthreads();
+        uint32_t h[8], own = 0;   // this thread's bins 8 tid .. 8 tid + 7
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            h[j] = hist[8 * tid + j];
+            own += h[j];
+        }
+        const uint32_t incl = warp_suffix(own);
+        if (lane == 0) scratch[warp] = incl;   // warp totals
+        __syncthreads();
+        uint32_t above = incl - own;
+        for (int w2 = warp + 1; w2 < RS_WARPS; ++w2) above += scratch[w2];
+        if (above < k && k <= above + own) {   // exactly one thread
+            uint32_t c = above;
+            for (int j = 7; j >= 0; --j) {
+                if (c + h[j] >= k) {
+                    scratch[RS_WARPS] = 8u * (uint32_t)tid + (uint32_t)j;
+                    scratch[RS_WARPS + 1] = c;
+                    break;
+                }
+                c += h[j];
+            }
+        }
+        __syncthreads();
+        const uint32_t bin = scratch[RS_WARPS], before = scratch[RS_WARPS + 1];
+        const uint32_t inbin = hist[bin];
+        prefix |= bin << sh;
+        mask |= dmask << sh;
+        k -= before;
+        __syncthreads();   // scratch and the histogram are reused
+        // the boundary bin is taken whole: exactly K keys are >= its lower
+        // edge, so every key above edge - 1 is selected (prefix >= 2^21 here)
+        if (inbin == k) return prefix - 1u;
+    }
+    return prefix;
+}
+
+// Writes to out[0, K): every i < n with keys[i] > T, then keys[i] == T until K
+// are taken (T = 0: every nonzero key), then -1; pos(i) gives the output id.
+// Slots come from one shared atomic per warp and 32 keys (ballots order the
+// lanes), so the writes never contend on a single counter lane by lane.
+template <typename PosFn>
+__device__ void block_emit(const uint32_t *keys, int n, uint32_t T, int K, int32_t *out, PosFn pos,
+                           uint32_t *scratch) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t c = 0;
+    for (int i = tid; i < n; i += RS_THREADS) c += (keys[i] > T) ? 1u : 0u;
+    const uint32_t above = block_sum(c, scratch);   // < K unless T = 0 or the boundary bin was taken whole
+    if (tid == 0) {
+        scratch[RS_WARPS] = 0u;
+        scratch[RS_WARPS + 1] = 0u;
+    }
+    __syncthreads();
+    const uint32_t room = above < (uint32_t)K ? (uint32_t)K - above : 0u;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int base = 32 * warp; base < n; base += RS_THREADS) {
+        const int i = base + lane;
+        const uint32_t key = i < n ? keys[i] : 0u;
+        const uint32_t gt = __ballot_sync(0xFFFFFFFFu, key > T);
+        const uint32_t eq = __ballot_sync(0xFFFFFFFFu, T != 0u && i < n && key == T);
+        if (gt) {
+            uint32_t b0 = 0;
+            if (lane == 0) b0 = atomicAdd(&scratch[RS_WARPS], (uint32_t)__popc(gt));
+            b0 = __shfl_sync(0xFFFFFFFFu, b0, 0);
+            const uint32_t s = b0 + (uint32_t)__popc(gt & lt);
+            if (((gt >> lane) & 1u) && s < (uint32_t)K) out[s] = pos(i);
+        }
+        if (eq && room) {
+            uint32_t b1 = 0;
+            if (lane == 0) b1 = atomicAdd(&scratch[RS_WARPS + 1], (uint32_t)__popc(eq));
+            b1 = __shfl_sync(0xFFFFFFFFu, b1, 0);
+            const uint32_t t = b1 + (uint32_t)__popc(eq & lt);
+            if (((eq >> lane) & 1u) && t < room) out[above + t] = pos(i);
+        }
+    }
+    __syncthreads();
+    const uint32_t taken = min((uint32_t)K, scratch[RS_WARPS]) + min(room, scratch[RS_WARPS + 1]);
+    for (int i = (int)taken + tid; i < K; i += RS_THREADS) out[i] = -1;
+}
+
+struct RescoreArgs {
+    int T;
+    int64_t N;
+    int K;
+    const uint32_t *bmax;   // [B*T, nblk] block-maximum keys
+    int64_t nblk;           // multiple of 4
+    const uint8_t *q;       // FP8 [B*T, 4, 64]
+    const float *w;         // [B*T, 4]
+    const uint8_t *k;       // FP8 [B, N, 64]
+    const int32_t *kv_len;  // [B*T]
+    int32_t *idx;           // [B*T, K]
+};
+
+__global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArgs a) {
+    extern __shared__ __align__(16) uint32_t dyn[];   // [nblk] maxima | [16 ceil(K/2)] candidate keys | [K] blocks
+    __shared__ __align__(16) uint32_t hist[2048];
+    __shared__ uint32_t scratch[RS_WARPS + 2];
     pdl_wait();
     pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t r = (int64_t)blockIdx.x * SEL_WARPS + warp;
-    if (r >= rows) return;
-    const uint2 *c = cand + r * (int64_t)(cap_gt + cap_eq);
-    int32_t *out = idx + r * K;
-    const uint32_t c_gt = cnt[2 * r], c_eq = cnt[2 * r + 1];
-    const int n_gt = (int)(c_gt < (uint32_t)cap_gt ? c_gt : (uint32_t)cap_gt);
-    const int n_eq = (int)(c_eq < (uint32_t)cap_eq ? c_eq : (uint32_t)cap_eq);
-    if (n_gt < K) {
-        // all candidates above tau, then ties at tau, then padding
-        for (int i = lane; i < n_gt; i += 32) out[i] = (int32_t)c[i].y;
-        const int ne = n_eq < K - n_gt ? n_eq : K - n_gt;
-        for (int i = lane; i < ne; i += 32) out[n_gt + i] = (int32_t)c[cap_gt + i].y;
-        for (int i = n_gt + ne + lane; i < K; i += 32) out[i] = -1;
-        return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int64_t r = blockIdx.x, b = r / a.T;
+    int64_t len = a.kv_len[r];
+    len = len < 0 ? 0 : (len > a.N ? a.N : len);
+    const int nb = (int)((len + 7) / 8);
+    uint32_t *sBm = dyn;
+    uint32_t *sSc = dyn + a.nblk;   // 16 ceil(K / 2) slots: whole two-block tiles
+    int32_t *sBlk = reinterpret_cast<int32_t *>(sSc + 16 * ((a.K + 1) / 2));
+    int32_t *out = a.idx + r * a.K;
+
+    // ---- the K blocks with the largest maxima (all of them when nb <= K)
+    int nsel;
+    if (nb <= a.K) {
+        for (int i = tid; i < nb; i += RS_THREADS) sBlk[i] = i;
+        nsel = nb;
+    } else {
+        const uint32_t *row = a.bmax + r * a.nblk;
+        for (int i = tid; 4 * i < nb; i += RS_THREADS) cp_async16((uint32_t)__cvta_generic_to_shared(sBm + 4 * i), row + 4 * i);
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        const uint32_t tau = block_kth_largest(sBm, nb, a.K, hist, scratch);
+        block_emit(sBm, nb, tau, a.K, sBlk, [](int i) { return (int32_t)i; }, scratch);
+        nsel = a.K;
     }
-    const uint32_t t = warp_kth_largest<8>([&](int i) { return c[i].x; }, n_gt, K, hist[warp]);
-    // keys above t (fewer than K) first, then ties at t up to K, in list order
-    uint32_t n_above = 0;
-    for (int base = 0; base < n_gt; base += 32) {
-        const int i = base + lane;
-        const bool p = i < n_gt && c[i].x > t;
-        n_above += (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, p));
-    }
-    uint32_t o_above = 0, o_tie = n_above;
-    for (int base = 0; base < n_gt; base += 32) {
-        const int i = base + lane;
-        const uint32_t k = i < n_gt ? c[i].x : 0u;
-        const uint32_t ba = __ballot_sync(0xFFFFFFFFu, i < n_gt && k > t);
-        const uint32_t be = __ballot_sync(0xFFFFFFFFu, i < n_gt && k == t);
-        const uint32_t below = (1u << lane) - 1u;
-        if ((ba >> lane) & 1u) out[o_above + __popc(ba & below)] = (int32_t)c[i].y;
-        if ((be >> lane) & 1u) {
-            const uint32_t j = o_tie + (uint32_t)__popc(be & below);
-            if (j < (uint32_t)K) out[j] = (int32_t)c[i].y;
+    __syncthreads();
+
+    // ---- rescore the 8 nsel candidates: a tile is two blocks (16 keys); lane
+    // (g, t4) loads 16 bytes of keys g and g + 8, the decode scorer's FP8
+    // mma.sync fragments (4 heads as columns 0-3 of n8)
+    const uint4 q8 = (g < 4) ? __ldg(reinterpret_cast<const uint4 *>(a.q + (r * 4 + g) * 64 + 16 * t4))
+                             : make_uint4(0u, 0u, 0u, 0u);
+    const float w0 = (t4 < 2) ? a.w[r * 4 + 2 * t4] : 0.f;
+    const float w1 = (t4 < 2) ? a.w[r * 4 + 2 * t4 + 1] : 0.f;
+    const int ntile = (nsel + 1) / 2;
+    const uint8_t *kb = a.k + b * a.N * 64;
+    for (int t0 = warp; t0 < ntile; t0 += 4 * RS_WARPS) {
+        uint4 raw[4][2];
+        bool v[4][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int tl = t0 + u * RS_WARPS;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int bi = 2 * tl + rr;
+                const int64_t p = bi < nsel ? (int64_t)sBlk[bi] * 8 + g : len;
+                v[u][rr] = tl < ntile && p < len;
+                raw[u][rr] = v[u][rr] ? __ldg(reinterpret_cast<const uint4 *>(kb + p * 64 + 16 * t4))
+                                      : make_uint4(0u, 0u, 0u, 0u);
+            }
         }
-        o_above += (uint32_t)__popc(ba);
-        o_tie += (uint32_t)__popc(be);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int tl = t0 + u * RS_WARPS;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_e4m3_16832(acc, raw[u][0].x, raw[u][1].x, raw[u][0].y, raw[u][1].y, q8.x, q8.y);
+            mma_e4m3_16832(acc, raw[u][0].z, raw[u][1].z, raw[u][0].w, raw[u][1].w, q8.z, q8.w);
+            float s0 = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);
+            float s1 = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);
+            s0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
+            s1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
+            if (t4 == 0 && tl < ntile) {
+                sSc[16 * tl + g] = v[u][0] ? score_key(s0) : 0u;
+                sSc[16 * tl + 8 + g] = v[u][1] ? score_key(s1) : 0u;
+            }
+        }
     }
+    __syncthreads();
+
+    // ---- Top-K of the candidates (every valid one when at most K)
+    const int m = 16 * ntile;   // candidate slots (an odd block count leaves 8 empty)
+    uint32_t nv = 0;
+    for (int i = tid; i < m; i += RS_THREADS) nv += sSc[i] != 0u ? 1u : 0u;
+    nv = block_sum(nv, scratch);
+    const uint32_t T = nv <= (uint32_t)a.K ? 0u : block_kth_largest(sSc, m, a.K, hist, scratch);
+    block_emit(sSc, m, T, a.K, out, [&](int i) { return sBlk[i >> 3] * 8 + (i & 7); }, scratch);
 }
 
 }  // namespace
@@ -222,29 +263,11 @@ using namespace csa2;
 
 static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-struct DenseLayout {
-    size_t bmax, tau, cnt, cand, total;
-    int64_t nblk;
-    int cap_gt, cap_eq;
-};
-
-static DenseLayout dense_layout(int B, int T, int64_t N, int K) {
-    DenseLayout L;
-    const size_t R = (size_t)B * (size_t)T;
-    L.nblk = ((N + 7) / 8 + 3) / 4 * 4;   // block-maximum rows padded to 16 bytes
-    L.cap_gt = 8 * (K - 1);
-    L.cap_eq = K;
-    L.bmax = 0;
-    L.tau = L.bmax + align256(R * (size_t)L.nblk * 4);
-    L.cnt = L.tau + align256(R * 4);
-    L.cand = L.cnt + align256(R * 8);
-    L.total = L.cand + align256(R * (size_t)(L.cap_gt + L.cap_eq) * 8);
-    return L;
-}
+static int64_t nblk_for(int64_t N) { return ((N + 7) / 8 + 3) / 4 * 4; }   // block-maximum rows padded to 16 bytes
 
 extern "C" size_t csa2_index_topk_dense_workspace_bytes(int B, int T, int64_t N, int K) {
     if (B < 0 || T < 0 || N < 0 || K < 1 || K > CSA2_MAX_K) return 0;
-    return dense_layout(B, T, N, K).total;
+    return align256((size_t)B * (size_t)T * (size_t)nblk_for(N) * 4);
 }
 
 extern "C" csa2_status csa2_index_topk_dense(int B, int T, int64_t N, const void *q_idx, csa2_dtype q_dt,
@@ -265,43 +288,28 @@ extern "C" csa2_status csa2_index_topk_dense(int B, int T, int64_t N, const void
     CSA2_REQUIRE(N == 0 || (aligned(q_idx, 16) && aligned(k_idx, 16)),
                  "index_topk_dense: q_idx/k_idx must be 16-byte aligned");
     CSA2_REQUIRE(aligned(w, 4) && aligned(kv_len, 4) && aligned(idx, 4), "index_topk_dense: misaligned w/kv_len/idx");
-    const DenseLayout L = dense_layout(B, T, N, K);
-    if (!workspace || ws_bytes < L.total || !aligned(workspace, 16)) {
-        set_error("index_topk_dense: workspace needs %zu bytes, 16-byte aligned (got %zu)", L.total, ws_bytes);
+    const int64_t nblk = nblk_for(N);
+    const size_t need = csa2_index_topk_dense_workspace_bytes(B, T, N, K);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 16)) {
+        set_error("index_topk_dense: workspace needs %zu bytes, 16-byte aligned (got %zu)", need, ws_bytes);
         return CSA2_ERR_WORKSPACE;
     }
-    uint8_t *ws = (uint8_t *)workspace;
-    uint32_t *bmax = (uint32_t *)(ws + L.bmax);
-    uint32_t *tau = (uint32_t *)(ws + L.tau);
-    uint32_t *cnt = (uint32_t *)(ws + L.cnt);
-    uint2 *cand = (uint2 *)(ws + L.cand);
-    const unsigned rows = (unsigned)((int64_t)B * T);
+    uint32_t *bmax = (uint32_t *)workspace;
     cudaStream_t s = stream_of(stream);
-    csa2_status st;
     if (N > 0) {
-        st = launch_prefill_block_max(B, T, N, q_idx, w, k_idx, kv_len, bmax, L.nblk, err_flag, s);
+        const csa2_status st = launch_prefill_block_max(B, T, N, q_idx, w, k_idx, kv_len, bmax, nblk, err_flag, s);
         if (st != CSA2_OK) return st;
     }
-    // rows per threshold CTA: as many as fit in 64 KB of staged maxima (1 to 8)
-    int64_t tw = 65536 / (L.nblk * 4 > 0 ? L.nblk * 4 : 1);
-    tw = tw < 1 ? 1 : (tw > SEL_WARPS ? SEL_WARPS : tw);
-    static bool thr_smem[64];
-    CSA2_CUDA_CALL(ensure_smem_limit((const void *)dense_threshold_kernel, (int)(MAX_N / 8 * 4 + 8192), thr_smem),
-                   "dense_threshold_kernel: smem attribute");
-    CSA2_CUDA_CALL(launch_pdl(dense_threshold_kernel, dim3((unsigned)((rows + tw - 1) / tw)), dim3((unsigned)(32 * tw)),
-                              (size_t)(tw * (L.nblk + 2048) * 4), s, (const uint32_t *)bmax, L.nblk, kv_len, N, (int)rows, K,
-                              tau, cnt),
-                   "dense_threshold_kernel launch");
-    CSA2_LAUNCH_CHECK("dense_threshold_kernel");
-    if (N > 0) {
-        st = launch_prefill_filter(B, T, N, q_idx, w, k_idx, kv_len, bmax, L.nblk, tau, cnt, cand, L.cap_gt, L.cap_eq,
-                                   err_flag, s);
-        if (st != CSA2_OK) return st;
-    }
-    const unsigned sel_grid = (rows + SEL_WARPS - 1) / SEL_WARPS;
-    CSA2_CUDA_CALL(launch_pdl(dense_select_kernel, dim3(sel_grid), dim3(SEL_THREADS), 0, s,
-                              (const uint32_t *)cnt, (const uint2 *)cand, L.cap_gt, L.cap_eq, (int)rows, K, idx),
-                   "dense_select_kernel launch");
-    CSA2_LAUNCH_CHECK("dense_select_kernel");
+    RescoreArgs ra;
+    ra.T = T; ra.N = N; ra.K = K; ra.bmax = bmax; ra.nblk = nblk;
+    ra.q = (const uint8_t *)q_idx; ra.w = w; ra.k = (const uint8_t *)k_idx; ra.kv_len = kv_len; ra.idx = idx;
+    const size_t smem = (size_t)(nblk + 16 * (int64_t)((K + 1) / 2) + K) * 4;
+    static bool smem_set[64];
+    CSA2_CUDA_CALL(ensure_smem_limit((const void *)dense_rescore_kernel,
+                                     (int)((nblk_for(MAX_N) + 9 * CSA2_MAX_K) * 4), smem_set),
+                   "dense_rescore_kernel: smem attribute");
+    CSA2_CUDA_CALL(launch_pdl(dense_rescore_kernel, dim3((unsigned)((int64_t)B * T)), dim3(RS_THREADS), smem, s, ra),
+                   "dense_rescore_kernel launch");
+    CSA2_LAUNCH_CHECK("dense_rescore_kernel");
     return CSA2_OK;
 }

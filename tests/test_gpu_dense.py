@@ -1,5 +1,5 @@
 """csa2_index_topk_dense (fused indexer for many query tokens: block maxima ->
-threshold -> filtered candidates -> Top-K, FP8) against the oracle's unfused
+the K best blocks -> their 8K candidates rescored -> Top-K, FP8) against the oracle's unfused
 chain index_score -> topk on the same seeded inputs.  Selections must agree
 outside the tie band of the oracle's fp64 scores (the GPU selects on its
 fp32 scores)."""
@@ -119,12 +119,13 @@ def test_dense_prefill_chunk_full_size(csa2):
     a = torch.sort(idx[0], dim=1).values
     b = torch.sort(idx_u[0], dim=1).values
     same = (a == b).all(1)
-    # rows that differ may only differ by ties at the 512th fp32 score
+    # rows that differ may only differ at the 512th fp32 score (the rescoring
+    # may round a score differently in the last bits)
     for t in torch.nonzero(~same).flatten().tolist():
         s = scores[0, t]
-        kth = torch.topk(s, 512).values[-1]
+        kth = float(torch.topk(s, 512).values[-1])
         d = set(idx[0, t].tolist()) ^ set(idx_u[0, t].tolist())
-        assert all(float(s[j]) == float(kth) for j in d), "row %d differs off the tie" % t
+        assert all(abs(float(s[j]) - kth) <= 1e-5 * abs(kth) for j in d), "row %d differs off the tie" % t
     rows = torch.linspace(0, T - 1, 24).long()
     qs, ws, kls = q[:, rows].cpu(), wt[:, rows].cpu(), kl[rows].cpu()
     ref = _ref_scores(qs, ws, k.cpu(), kls)
