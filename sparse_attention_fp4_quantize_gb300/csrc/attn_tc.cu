@@ -576,7 +576,51 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
             sBeta[tid] = beta;
         }
     }
-    for (int o = (S > 1 ? 1 : 0); o < S; ++o) {
+    if (S == 1) {
+        // ---- 7'. one CTA holds every entry: O / L straight from TMEM to the
+        // output in fp32 (lanes = 32 consecutive channels of one head per
+        // store), times the merge weight (1, or the window's share) plus the
+        // sparse branch's share
+        ok = tc::mbar_wait(bar_rx, 0, MAX_POLLS) && ok;   // (no bytes expected: completes the phase)
+        __syncthreads();                                   // the weights of the block above
+        if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
+        const int64_t hbase = (bt * a.H) + h0 + 16 * hh;
+        // two 128-channel blocks at a time: their sparse-branch values are
+        // loaded together, after the TMEM loads' wait
+#pragma unroll 1
+        for (int mb = 0; mb < DV / 128; mb += 2) {
+            uint32_t r[2][16];
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * HB + 16 * hh, r[0]);
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + (mb + 1) * HB + 16 * hh, r[1]);
+            tc::tmem_ld_wait();
+            float os[2][16];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int c = (mb + u) * 128 + 32 * quarter + lane;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    os[u][jj] = (FP8W && a.o_sparse) ? a.o_sparse[(hbase + jj) * (int64_t)DV + c] : 0.f;   // may alias out
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int c = (mb + u) * 128 + 32 * quarter + lane;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int h = 16 * hh + jj;
+                    float v = __uint_as_float(r[u][jj]) * il[jj] * sW[h];
+                    if (FP8W) v += sBeta[h] * os[u][jj];
+                    a.out[(hbase + jj) * (int64_t)DV + c] = v;
+                }
+            }
+        }
+        if (a.lse && tid < HB) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+        return;
+    }
+    for (int o = 1; o < S; ++o) {
         stage_slice(o);
         if (o + 1 < S) {
             tc::fence_async_smem();
