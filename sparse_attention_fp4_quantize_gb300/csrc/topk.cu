@@ -421,20 +421,26 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
     const float w0 = (t4 < 2) ? a.w[row * 4 + 2 * t4] : 0.f;
     const float w1 = (t4 < 2) ? a.w[row * 4 + 2 * t4 + 1] : 0.f;
     const int nchunks = (nm + 127) / 128;
+    // Reindex: a chunk's 16 pool block ids, checked (lanes 0-15 hold them)
+    auto pool_ids = [&](int cb, int l) -> int32_t {
+        const int64_t pidx = (beg + (int64_t)cb * 128) / 8 + l;
+        if (cb >= nchunks || pidx >= a.P) return -1;
+        int64_t blk = a.pool_in[row * a.P + pidx];
+        if (blk < -1 || blk >= nblocks_n) {
+            flag_error(a.err_flag, CSA2_FLAG_BAD_POOL);
+            blk = -1;
+        }
+        return (int32_t)blk;
+    };
+    // the ids of this warp's first two chunks are loaded together (lanes
+    // 0-15: chunk warp, lanes 16-31: chunk warp + kWarps), off the chain of
+    // dependent loads of each chunk
+    const int32_t pre_blk = full ? -1 : pool_ids(warp + (lane >= 16 ? kWarps : 0), lane & 15);
     for (int cb = warp; cb < nchunks; cb += kWarps) {   // 8 groups of 16 candidates per warp chunk
         const int i0 = cb * 128;
-        int32_t myblk = -1;
-        if (!full && lane < 16) {
-            const int64_t pidx = (beg + i0) / 8 + lane;
-            if (pidx < a.P) {
-                int64_t blk = a.pool_in[row * a.P + pidx];
-                if (blk < -1 || blk >= nblocks_n) {
-                    flag_error(a.err_flag, CSA2_FLAG_BAD_POOL);
-                    blk = -1;
-                }
-                myblk = (int32_t)blk;
-            }
-        }
+        const int it = (cb - warp) / kWarps;
+        int32_t myblk = __shfl_sync(0xFFFFFFFFu, pre_blk, (lane & 15) + 16 * (it & 1));
+        if (!full && it >= 2) myblk = lane < 16 ? pool_ids(cb, lane) : -1;
         uint4 raw[8][2];
         bool v[8][2];
 #pragma unroll
