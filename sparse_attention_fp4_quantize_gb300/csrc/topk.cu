@@ -436,15 +436,18 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
     // 0-15: chunk warp, lanes 16-31: chunk warp + kWarps), off the chain of
     // dependent loads of each chunk
     const int32_t pre_blk = full ? -1 : pool_ids(warp + (lane >= 16 ? kWarps : 0), lane & 15);
-    for (int cb = warp; cb < nchunks; cb += kWarps) {   // 8 groups of 16 candidates per warp chunk
-        const int i0 = cb * 128;
-        const int it = (cb - warp) / kWarps;
-        int32_t myblk = __shfl_sync(0xFFFFFFFFu, pre_blk, (lane & 15) + 16 * (it & 1));
-        if (!full && it >= 2) myblk = lane < 16 ? pool_ids(cb, lane) : -1;
-        uint4 raw[8][2];
-        bool v[8][2];
+    // A warp scores its chunks (cb = warp, warp + kWarps, ...) in halves of 4
+    // groups (64 candidates), software-pipelined over two register buffers:
+    // the loads of half k + 1 are in flight while half k is scored.
+    const int nhalf = warp < nchunks ? 2 * ((nchunks - warp + kWarps - 1) / kWarps) : 0;
+    int32_t chunk_blk = -1;   // Reindex, chunks past the first two: ids reloaded per chunk
+    auto load_half = [&](int k, uint4 (&raw)[4][2], bool (&v)[4][2]) {
+        const int it = k >> 1, cb = warp + kWarps * it, i0 = cb * 128 + 64 * (k & 1);
+        if (!full && it >= 2 && (k & 1) == 0) chunk_blk = lane < 16 ? pool_ids(cb, lane) : -1;
+        const int32_t ids = it < 2 ? pre_blk : chunk_blk;
+        const int base_lane = (it < 2 ? 16 * (it & 1) : 0) + 8 * (k & 1);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int i = i0 + 16 * c + g + 8 * r;
@@ -452,7 +455,7 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
                 if (full) {
                     j = beg + i;
                 } else {
-                    const int32_t blk = __shfl_sync(0xFFFFFFFFu, myblk, 2 * c + r);
+                    const int32_t blk = __shfl_sync(0xFFFFFFFFu, ids, base_lane + 2 * c + r);
                     j = blk >= 0 ? (int64_t)blk * 8 + g : -1;
                 }
                 v[c][r] = i < nm && j >= 0 && j < len;
@@ -460,8 +463,11 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
                                     : make_uint4(0, 0, 0, 0);
             }
         }
+    };
+    auto score_half = [&](int k, const uint4 (&raw)[4][2], const bool (&v)[4][2]) {
+        const int i0 = (warp + kWarps * (k >> 1)) * 128 + 64 * (k & 1);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             mma_e4m3_16832(acc, raw[c][0].x, raw[c][1].x, raw[c][0].y, raw[c][1].y, q8.x, q8.y);
             mma_e4m3_16832(acc, raw[c][0].z, raw[c][1].z, raw[c][0].w, raw[c][1].w, q8.z, q8.w);
@@ -473,6 +479,17 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
                 keys[i0 + 16 * c + g] = v[c][0] ? score_key(s0) : 0u;
                 keys[i0 + 16 * c + g + 8] = v[c][1] ? score_key(s1) : 0u;
             }
+        }
+    };
+    {
+        uint4 ra[4][2], rb[4][2];
+        bool va[4][2], vb[4][2];
+        if (nhalf > 0) load_half(0, ra, va);
+        for (int k = 0; k < nhalf; k += 2) {   // nhalf is even
+            load_half(k + 1, rb, vb);
+            score_half(k, ra, va);
+            if (k + 2 < nhalf) load_half(k + 2, ra, va);
+            score_half(k + 1, rb, vb);
         }
     }
     __syncthreads();   // keys [0, 128 nchunks) written; the rest of [0, 4 nm4) is never read
