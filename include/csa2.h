@@ -331,6 +331,17 @@ csa2_status csa2_sparse_attn_fp4_noalloc(csa2_mode mode, int B, int T, int H, in
                                          uint32_t *err_flag, csa2_stream_t stream);
 size_t csa2_sparse_attn_noalloc_max_scratch_bytes(void);
 
+/*
+ * csa2_selftest_bounded_wait -- exercises the library's bounded wait on an
+ * mbarrier (the one every tensor-core kernel uses for its TMA copies and
+ * MMAs) with an arrival that never comes: one CTA polls an mbarrier nothing
+ * arrives on, gives up after max_polls polls (1 <= max_polls <= 2^22), sets
+ * CSA2_FLAG_TIMEOUT in *err_flag (device, required) and returns, leaving the
+ * context usable.  Test infrastructure for the failure path; no fault, trap
+ * or unbounded spin is involved.
+ */
+csa2_status csa2_selftest_bounded_wait(uint32_t max_polls, uint32_t *err_flag, csa2_stream_t stream);
+
 /* Status helpers. */
 const char *csa2_status_string(csa2_status s);
 const char *csa2_last_error(void); /* thread-local detail of the last non-OK status */

@@ -61,6 +61,7 @@ def _load() -> ctypes.CDLL:
         "csa2_sparse_attn_fp4_noalloc": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P,
                                           P, P], i32),
         "csa2_sparse_attn_noalloc_max_scratch_bytes": ([], u64),
+        "csa2_selftest_bounded_wait": ([ctypes.c_uint32, P, P], i32),
         "csa2_status_string": ([i32], ctypes.c_char_p),
         "csa2_last_error": ([], ctypes.c_char_p),
         "csa2_version": ([], i32),
@@ -80,7 +81,7 @@ def exported_symbols():
             "csa2_topk", "csa2_topk_workspace_bytes", "csa2_index_topk", "csa2_index_topk_dense",
             "csa2_index_topk_dense_workspace_bytes", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes", "csa2_swa_attn_fp8",
             "csa2_sparse_attn_fp4_noalloc", "csa2_sparse_attn_noalloc_max_scratch_bytes",
-            "csa2_status_string", "csa2_last_error", "csa2_version"]
+            "csa2_selftest_bounded_wait", "csa2_status_string", "csa2_last_error", "csa2_version"]
 
 
 def _ptr(t):
@@ -110,6 +111,13 @@ def _cuda(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def csa2_selftest_bounded_wait(err_flag, max_polls=4096, stream=None):
+    """The kernels' bounded mbarrier wait on an arrival that never comes:
+    sets FLAG_TIMEOUT in err_flag (int32/uint32 CUDA tensor) and returns."""
+    _cuda(err_flag)
+    _check(_lib.csa2_selftest_bounded_wait(int(max_polls), _ptr(err_flag), _stream(stream)))
 
 
 def version() -> int:

@@ -3,6 +3,7 @@
 #include <string.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace csa2 {
 
@@ -39,6 +40,36 @@ int max_smem_optin() {
 }
 
 }  // namespace csa2
+
+namespace csa2 {
+namespace {
+
+// One CTA: an mbarrier expecting one arrival that never comes, waited on with
+// the kernels' bounded wait; on giving up the CTA flags the timeout.
+__global__ void bounded_wait_selftest_kernel(uint32_t max_polls, uint32_t *err_flag) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = tc::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        tc::mbar_init(b, 1);
+        tc::mbar_init_fence();
+    }
+    __syncthreads();
+    const bool ok = tc::mbar_wait(b, 0, max_polls);
+    if (!ok && threadIdx.x == 0) flag_error(err_flag, CSA2_FLAG_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace csa2
+
+extern "C" csa2_status csa2_selftest_bounded_wait(uint32_t max_polls, uint32_t *err_flag, csa2_stream_t stream) {
+    csa2::clear_error();
+    CSA2_REQUIRE(err_flag, "selftest_bounded_wait: err_flag required");
+    CSA2_REQUIRE(max_polls >= 1 && max_polls <= (1u << 22), "selftest_bounded_wait: max_polls=%u not in [1, 2^22]",
+                 max_polls);
+    csa2::bounded_wait_selftest_kernel<<<1, 32, 0, csa2::stream_of(stream)>>>(max_polls, err_flag);
+    CSA2_LAUNCH_CHECK("bounded_wait_selftest_kernel");
+    return CSA2_OK;
+}
 
 extern "C" const char *csa2_status_string(csa2_status s) {
     switch (s) {

@@ -86,6 +86,15 @@ def test_rope_quantize_rejects_bad_arguments_on_host(lib):
     assert f(NULL, 0, 576, 576, NULL, NULL, 16, 64, NULL, 0, NULL, NULL, NULL, NULL) == 0   # empty: no-op
 
 
+def test_selftest_bounded_wait_rejects_bad_arguments_on_host(lib):
+    f = lib.csa2_selftest_bounded_wait
+    f.argtypes = [ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(16, NULL, NULL) == 1                          # err_flag required
+    assert f(0, ctypes.c_void_p(0x1000), NULL) == 1         # max_polls 0
+    assert f((1 << 22) + 1, ctypes.c_void_p(0x1000), NULL) == 1
+    assert "max_polls" in _last_error(lib)
+
+
 def test_index_score_rejects_bad_arguments_on_host(lib):
     f = lib.csa2_index_score
     P = ctypes.c_void_p

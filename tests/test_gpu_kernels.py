@@ -390,3 +390,20 @@ def test_sparse_attn_workspace_is_required_when_split(csa2):
     with pytest.raises(csa2.Csa2Error) as e:
         csa2.csa2_sparse_attn_fp4(0, q, codes, scales, 100, idx, out, 0.1)
     assert e.value.status == 3
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    """A wait that nothing completes gives up, flags CSA2_FLAG_TIMEOUT, and the
+    next launch on the same context runs normally."""
+    import sparse_attention_fp4_quantize_gb300 as csa2
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    csa2.csa2_selftest_bounded_wait(flag, max_polls=2048)
+    torch.cuda.synchronize()
+    assert int(flag.item()) & csa2.FLAG_TIMEOUT
+    rows = gen.kv_rows(0, 1, 64, 128, device="cuda")
+    codes = torch.empty(64, 64, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(64, 8, dtype=torch.uint8, device="cuda")
+    csa2.csa2_quantize_kv_fp4(rows, codes, scales)
+    torch.cuda.synchronize()
+    want_c, want_s = oracle.quantize_kv_fp4(gen.as_numpy(rows).reshape(64, 128))
+    assert (codes.cpu().numpy() == want_c).all() and (scales.cpu().numpy() == want_s).all()
