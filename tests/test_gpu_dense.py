@@ -64,6 +64,25 @@ def test_dense_matches_oracle_chain(csa2, B, T, N, K, first_pos):
     _check_rows(got, want, ref, K, "dense topk")
 
 
+def test_dense_long_context_and_single_query_rows(csa2):
+    """1M-token context (262144 entries: the block maxima of a row take 128 KB
+    of shared memory) with 16 queries, and B=3 sequences of one query each."""
+    q = gen.normal_e4m3(34, 1, (1, 16, 4, 64))
+    k = gen.normal_e4m3(34, 2, (1, 262144, 64))
+    w = gen.uniform01(34, 3, (1, 16, 4))
+    kl = _causal_lengths(16, 262144, 1048576 - 16)
+    ref = _ref_scores(q, w, k, kl)
+    want = oracle.topk(oracle.FULL, ref.astype(np.float32), gen.as_numpy(kl), K=512)
+    _check_rows(_dense(csa2, q, w, k, kl, 512), want, ref, 512, "dense topk (1M context)")
+    q1 = gen.normal_e4m3(35, 1, (3, 1, 4, 64))
+    k1 = gen.normal_e4m3(35, 2, (3, 9000, 64))
+    w1 = gen.uniform01(35, 3, (3, 1, 4))
+    kl1 = torch.tensor([9000, 4321, 600], dtype=torch.int32)
+    ref1 = _ref_scores(q1, w1, k1, kl1)
+    want1 = oracle.topk(oracle.FULL, ref1.astype(np.float32), gen.as_numpy(kl1), K=512)
+    _check_rows(_dense(csa2, q1, w1, k1, kl1, 512), want1, ref1, 512, "dense topk (T=1)")
+
+
 def test_dense_short_and_empty_rows(csa2):
     """Rows with no visible entry (all -1), fewer than K visible entries (all
     of them, then -1), fewer than K blocks but more than K entries, and
