@@ -607,7 +607,7 @@ csa2_status launch_index_topk(const FusedArgs &in, cudaStream_t stream) {
     auto smem_for = [&](int c) { return (size_t)(chunk_for(c) + chunk_for(c) / 8 + 4) * sizeof(uint32_t); };
     int C = 1;
     while (C < kMaxCluster && smem_for(C) > (size_t)kSmemCap) C *= 2;
-    while (C < 4 && chunk_for(C) > 4096 && a.rows * C * 2 <= (int64_t)num_sms()) C *= 2;
+    while (C < kMaxCluster && chunk_for(C) > 2048 && a.rows * C * 2 <= (int64_t)num_sms()) C *= 2;
     const int64_t chunk = chunk_for(C);
     const size_t smem = smem_for(C);
     if (smem > (size_t)kSmemCap) {
