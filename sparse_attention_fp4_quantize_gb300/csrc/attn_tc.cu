@@ -28,7 +28,9 @@
 //     one cluster barrier the TMA engine copies the slices into the owners'
 //     shared memory (bulk shared -> remote shared copies completing on the
 //     owner's mbarrier).  Each owner combines its slice with the weights
-//     L_c 2^(m_c - M) / sum_c' L_c' 2^(m_c' - M) and writes it out.
+//     L_c 2^(m_c - M) / sum_c' L_c' 2^(m_c' - M) and writes it out, its own
+//     part read straight from TMEM in fp32 (a single-CTA cluster writes all
+//     of O / L that way, with no staging).
 // Waits on the mbarriers are bounded; on timeout the kernel sets
 // CSA2_FLAG_TIMEOUT and still runs every cluster barrier, so it always ends.
 #include <cooperative_groups.h>
@@ -620,53 +622,61 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
         return;
     }
-    for (int o = 1; o < S; ++o) {
+    for (int o = 1; o + 1 < S; ++o) {   // the other CTAs' slices; the own one stays in TMEM
         stage_slice(o);
-        if (o + 1 < S) {
-            tc::fence_async_smem();
-            __syncthreads();
-            if (tid == 0) send_slice(o);
-        }
+        tc::fence_async_smem();
+        __syncthreads();
+        if (tid == 0) send_slice(o);
     }
     if (tid == 0) bulk_wait_read0();           // staging reads done before this CTA may exit
     ok = tc::mbar_wait(bar_rx, 0, MAX_POLLS) && ok;   // the other CTAs' slices have landed
     __syncthreads();
     if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
 
-    // ---- 7. combine this CTA's channel slice with the weights
+    // ---- 7. combine this CTA's channel slice with the weights: its own part
+    // straight from TMEM in fp32 (the TMEM lane mapping: lane = channel, 16
+    // heads per thread, every store of a warp covers 32 consecutive channels
+    // of one head), the other CTAs' parts from their f16 slices
     {
-        // thread -> (8 heads, channel): lanes take consecutive channels (conflict-free
-        // 8-byte reads of the 136-byte rows; every output store of a warp covers 32
-        // consecutive channels of one head)
         const int c_lo = rank * W;
-        const int wshift = S == 1 ? 9 : (S == 2 ? 8 : 7);   // log2 W
-        for (int t = tid; t < (HB / 8) * W; t += THREADS) {
-            const int h8 = t >> wshift, c = t & (W - 1);
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int bi = 0; bi < bpo; ++bi) {
+            uint32_t r[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + (rank * bpo + bi) * HB + 16 * hh, r);
+            tc::tmem_ld_wait();
+            const int cl = bi * 128 + 32 * quarter + lane;   // channel within the slice
+            const int64_t orow = (bt * a.H) + h0 + 16 * hh;
 #pragma unroll
-            for (int src = 0; src < MAX_S; ++src) {
-                if (src < S) {
-                    const uint8_t *rp = recv + (size_t)src * slice_bytes + (size_t)c * (RSH * 2) + 16 * h8;
-                    const uint2 v0 = *reinterpret_cast<const uint2 *>(rp);
-                    const uint2 v1 = *reinterpret_cast<const uint2 *>(rp + 8);
-                    const float4 w0 = *reinterpret_cast<const float4 *>(sW + src * HB + 8 * h8);
-                    const float4 w1 = *reinterpret_cast<const float4 *>(sW + src * HB + 8 * h8 + 4);
-                    const float2 a01 = __half22float2(*reinterpret_cast<const __half2 *>(&v0.x));
-                    const float2 a23 = __half22float2(*reinterpret_cast<const __half2 *>(&v0.y));
-                    const float2 a45 = __half22float2(*reinterpret_cast<const __half2 *>(&v1.x));
-                    const float2 a67 = __half22float2(*reinterpret_cast<const __half2 *>(&v1.y));
-                    acc[0] += w0.x * a01.x; acc[1] += w0.y * a01.y; acc[2] += w0.z * a23.x; acc[3] += w0.w * a23.y;
-                    acc[4] += w1.x * a45.x; acc[5] += w1.y * a45.y; acc[6] += w1.z * a67.x; acc[7] += w1.w * a67.y;
+            for (int half = 0; half < 2; ++half) {
+                float acc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int jj = 8 * half + i;
+                    acc[i] = __uint_as_float(r[jj]) * il[jj] * sW[rank * HB + 16 * hh + jj];
+                }
+#pragma unroll
+                for (int src = 0; src < MAX_S; ++src) {
+                    if (src < S && src != rank) {
+                        const uint8_t *rp = recv + (size_t)src * slice_bytes + (size_t)cl * (RSH * 2) + 32 * hh + 16 * half;
+                        const uint2 v0 = *reinterpret_cast<const uint2 *>(rp);
+                        const uint2 v1 = *reinterpret_cast<const uint2 *>(rp + 8);
+                        const float *wsrc = sW + src * HB + 16 * hh + 8 * half;
+                        const float2 a01 = __half22float2(*reinterpret_cast<const __half2 *>(&v0.x));
+                        const float2 a23 = __half22float2(*reinterpret_cast<const __half2 *>(&v0.y));
+                        const float2 a45 = __half22float2(*reinterpret_cast<const __half2 *>(&v1.x));
+                        const float2 a67 = __half22float2(*reinterpret_cast<const __half2 *>(&v1.y));
+                        acc[0] += wsrc[0] * a01.x; acc[1] += wsrc[1] * a01.y; acc[2] += wsrc[2] * a23.x;
+                        acc[3] += wsrc[3] * a23.y; acc[4] += wsrc[4] * a45.x; acc[5] += wsrc[5] * a45.y;
+                        acc[6] += wsrc[6] * a67.x; acc[7] += wsrc[7] * a67.y;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int64_t oi = (orow + 8 * half + i) * (int64_t)DV + c_lo + cl;
+                    float v = acc[i];
+                    if (FP8W && a.o_sparse) v += sBeta[16 * hh + 8 * half + i] * a.o_sparse[oi];   // may alias out
+                    a.out[oi] = v;
                 }
             }
-            float *o = a.out + ((bt * a.H) + h0 + 8 * h8) * (int64_t)DV + c_lo + c;
-            if (FP8W && a.o_sparse) {
-                const float *os = a.o_sparse + ((bt * a.H) + h0 + 8 * h8) * (int64_t)DV + c_lo + c;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] += sBeta[8 * h8 + i] * os[i * DV];   // os may alias o
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i * DV] = acc[i];
         }
         if (rank == 0 && a.lse && tid < HB) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
     }
