@@ -95,6 +95,27 @@ def test_selftest_bounded_wait_rejects_bad_arguments_on_host(lib):
     assert "max_polls" in _last_error(lib)
 
 
+def test_dense_index_topk_rejects_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+    f = lib.csa2_index_topk_dense
+    f.argtypes = [ctypes.c_int, ctypes.c_int, I64, P, ctypes.c_int, P, P, ctypes.c_int, P, ctypes.c_int, P, P, P,
+                  ctypes.c_size_t, P]
+    wsb = lib.csa2_index_topk_dense_workspace_bytes
+    wsb.argtypes = [ctypes.c_int, ctypes.c_int, I64, ctypes.c_int]
+    wsb.restype = ctypes.c_size_t
+    fake = P(0x1000)
+    FP8, BF16 = 1, 0
+    need = wsb(1, 64, 4096, 512)
+    assert need == 64 * (4096 // 8) * 4                                                   # 4 B per 8 positions per query
+    assert f(1, 64, 4096, fake, BF16, fake, fake, BF16, fake, 512, fake, NULL, fake, need, NULL) == 1   # bf16
+    assert f(1, 64, 4096, fake, FP8, fake, fake, FP8, fake, 0, fake, NULL, fake, need, NULL) == 1       # K = 0
+    assert f(1, 64, 4096, fake, FP8, fake, fake, FP8, fake, 4096, fake, NULL, fake, need, NULL) == 1    # K > 2048
+    assert f(1, 64, 262145, fake, FP8, fake, fake, FP8, fake, 512, fake, NULL, fake, need, NULL) == 2   # N too large
+    assert f(1, 64, 4096, fake, FP8, fake, fake, FP8, fake, 512, fake, NULL, fake, need - 1, NULL) == 3  # workspace
+    assert f(1, 64, 4096, fake, FP8, fake, fake, FP8, NULL, 512, fake, NULL, fake, need, NULL) == 1     # kv_len null
+    assert f(0, 64, 4096, NULL, FP8, NULL, NULL, FP8, NULL, 512, NULL, NULL, NULL, 0, NULL) == 0        # empty: no-op
+
+
 def test_index_score_rejects_bad_arguments_on_host(lib):
     f = lib.csa2_index_score
     P = ctypes.c_void_p
