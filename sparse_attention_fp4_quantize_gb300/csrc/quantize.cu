@@ -131,9 +131,9 @@ __device__ __forceinline__ uint32_t rope_word(uint32_t w, float2 cs) {
 
 template <bool ROPE, int UNR>
 __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(
-    const uint16_t *__restrict__ kv, uint32_t total_units, FastDiv upr_div, int D, int64_t stride,
-    int64_t row0, const int64_t *__restrict__ dst_slot, int64_t n_slots, uint8_t *__restrict__ codes,
-    uint8_t *__restrict__ scales, uint32_t *err_flag, RopeArgs rope) {
+    const uint16_t *__restrict__ kv, uint32_t total_units, FastDiv upr_div, uint32_t first_unit, int D,
+    int64_t stride, int64_t row0, const int64_t *__restrict__ dst_slot, int64_t n_slots,
+    uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, uint32_t *err_flag, RopeArgs rope) {
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(
             ok[k] = u < total_units;
             uint32_t r = fdiv(ok[k] ? u : 0u, upr_div);
             rr[k] = r;
-            ur[k] = (ok[k] ? u : 0u) - r * upr;
+            ur[k] = first_unit + ((ok[k] ? u : 0u) - r * upr);
             v[k] = make_uint4(0, 0, 0, 0);
             if (ok[k]) v[k] = ld_stream_v4(kv + (row0 + r) * stride + (int64_t)ur[k] * 8);
         }
@@ -202,14 +202,14 @@ __global__ void __launch_bounds__(kThreads) quantize_fp4_kernel(
 
 using namespace csa2;
 
-static csa2_status launch_quantize(const void *kv, int64_t rows, int D, int64_t kv_row_stride,
-                                   const int64_t *dst_slot, int64_t n_slots, uint8_t *codes, uint8_t *scales,
-                                   uint32_t *err_flag, const RopeArgs *rope, csa2_stream_t stream) {
-    const uint32_t upr = (uint32_t)(D / 8);
+// Units (16-byte pieces of a row) [first_unit, first_unit + upr) of every row,
+// in launches whose unit count fits comfortably in 32 bits.
+template <bool ROPE>
+static csa2_status launch_quantize_units(const void *kv, int64_t rows, int D, int64_t kv_row_stride, uint32_t first_unit,
+                                         uint32_t upr, const int64_t *dst_slot, int64_t n_slots, uint8_t *codes,
+                                         uint8_t *scales, uint32_t *err_flag, const RopeArgs &ra, csa2_stream_t stream) {
     FastDiv fd;
     fd.init(upr);
-    const RopeArgs ra = rope ? *rope : RopeArgs{nullptr, nullptr, 0, 0};
-    // Launch in chunks whose unit count fits comfortably in 32 bits.
     const int64_t max_rows = (int64_t)(0x7FFFFFFFu / upr);
     const int max_blocks = num_sms() * 8;
     for (int64_t r0 = 0; r0 < rows; r0 += max_rows) {
@@ -218,19 +218,40 @@ static csa2_status launch_quantize(const void *kv, int64_t rows, int D, int64_t 
         // Small appends use the short unroll; large ones the long one (the
         // grid then covers every SM several times over).
         const bool small = (int64_t)units < (int64_t)num_sms() * kThreads * 16;
-        const int unr = small ? 2 : (rope ? 4 : 8);
+        const int unr = small ? 2 : (ROPE ? 4 : 8);
         const int64_t per_block = (int64_t)kThreads * unr;
         int64_t want = ((int64_t)units + per_block - 1) / per_block;
         int blocks = (int)(want < max_blocks ? want : max_blocks);
         if (blocks < 1) blocks = 1;
-        auto kern = rope ? (small ? quantize_fp4_kernel<true, 2> : quantize_fp4_kernel<true, 4>)
-                         : (small ? quantize_fp4_kernel<false, 2> : quantize_fp4_kernel<false, 8>);
+        auto kern = small ? quantize_fp4_kernel<ROPE, 2> : quantize_fp4_kernel<ROPE, ROPE ? 4 : 8>;
         CSA2_CUDA_CALL(launch_pdl(kern, dim3(blocks), dim3(kThreads), 0, stream_of(stream), (const uint16_t *)kv,
-                                  units, fd, D, kv_row_stride, r0, dst_slot, n_slots, codes, scales, err_flag, ra),
+                                  units, fd, first_unit, D, kv_row_stride, r0, dst_slot, n_slots, codes, scales,
+                                  err_flag, ra),
                        "quantize_fp4_kernel launch");
         CSA2_LAUNCH_CHECK("quantize_fp4_kernel");
     }
     return CSA2_OK;
+}
+
+// Without RoPE: every unit of every row in one pass.  With RoPE: the latent
+// units by the plain kernel (no rotation work, no divergence), then the
+// rotated units by the RoPE kernel, whose warps all rotate.
+static csa2_status launch_quantize(const void *kv, int64_t rows, int D, int64_t kv_row_stride,
+                                   const int64_t *dst_slot, int64_t n_slots, uint8_t *codes, uint8_t *scales,
+                                   uint32_t *err_flag, const RopeArgs *rope, csa2_stream_t stream) {
+    const uint32_t upr = (uint32_t)(D / 8);
+    const RopeArgs none = {nullptr, nullptr, 0, 0};
+    if (!rope)
+        return launch_quantize_units<false>(kv, rows, D, kv_row_stride, 0, upr, dst_slot, n_slots, codes, scales,
+                                            err_flag, none, stream);
+    const uint32_t u0 = (uint32_t)(D - rope->rope_dim) / 8;
+    if (u0 > 0) {
+        const csa2_status st = launch_quantize_units<false>(kv, rows, D, kv_row_stride, 0, u0, dst_slot, n_slots,
+                                                            codes, scales, err_flag, none, stream);
+        if (st != CSA2_OK) return st;
+    }
+    return launch_quantize_units<true>(kv, rows, D, kv_row_stride, u0, upr - u0, dst_slot, n_slots, codes, scales,
+                                       err_flag, *rope, stream);
 }
 
 #define CSA2_QUANT_CHECKS()                                                                                    \
