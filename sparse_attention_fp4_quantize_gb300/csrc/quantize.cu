@@ -106,9 +106,9 @@ __device__ __forceinline__ uint32_t encode_word(uint32_t w, float inv) {
 }
 
 constexpr int kThreads = 256;
-// Units per thread per pass (UNR): 8 for large plain appends, 4 with RoPE
-// (where the position -> table load chain makes 8 slower), 2 for small
-// appends (a decode step's few hundred rows), which then spread over more SMs.
+// Units per thread per pass (UNR): 8 for large plain appends, 2 for small
+// appends (a decode step's few hundred rows, which then spread over more
+// SMs), 1 for the rotated units of the RoPE pass.
 
 // RoPE of the append path, fused ahead of the quantiser: interleaved pairs
 // (2i, 2i+1) of the last rope_dim channels rotated by a caller-supplied fp32
@@ -215,15 +215,21 @@ static csa2_status launch_quantize_units(const void *kv, int64_t rows, int D, in
     for (int64_t r0 = 0; r0 < rows; r0 += max_rows) {
         int64_t nr = rows - r0 < max_rows ? rows - r0 : max_rows;
         uint32_t units = (uint32_t)(nr * upr);
-        // Small appends use the short unroll; large ones the long one (the
-        // grid then covers every SM several times over).
+        // Plain units: the short unroll for small appends, the long one for
+        // large ones (the grid then covers every SM several times over).
+        // Rotated units: one per thread (the position -> table chain of each
+        // unit is latency-bound: 2 or 4 per thread measured 346 / 364 us at
+        // 1M rows against 345, 8 per thread 392).
         const bool small = (int64_t)units < (int64_t)num_sms() * kThreads * 16;
-        const int unr = small ? 2 : (ROPE ? 4 : 8);
+        const int unr = ROPE ? 1 : (small ? 2 : 8);
         const int64_t per_block = (int64_t)kThreads * unr;
         int64_t want = ((int64_t)units + per_block - 1) / per_block;
         int blocks = (int)(want < max_blocks ? want : max_blocks);
         if (blocks < 1) blocks = 1;
-        auto kern = small ? quantize_fp4_kernel<ROPE, 2> : quantize_fp4_kernel<ROPE, ROPE ? 4 : 8>;
+        void (*kern)(const uint16_t *, uint32_t, FastDiv, uint32_t, int, int64_t, int64_t, const int64_t *, int64_t,
+                     uint8_t *, uint8_t *, uint32_t *, RopeArgs);
+        if constexpr (ROPE) kern = quantize_fp4_kernel<true, 1>;
+        else kern = small ? quantize_fp4_kernel<false, 2> : quantize_fp4_kernel<false, 8>;
         CSA2_CUDA_CALL(launch_pdl(kern, dim3(blocks), dim3(kThreads), 0, stream_of(stream), (const uint16_t *)kv,
                                   units, fd, first_unit, D, kv_row_stride, r0, dst_slot, n_slots, codes, scales,
                                   err_flag, ra),
