@@ -4,8 +4,8 @@
 // "效率组件四件", item 4 "FP4 主 KV Cache" (E2M1 + per-16-channel E4M3 scale,
 // NVFP4-like without the second-level scale, quantised after RoPE).
 //
-// HBM-bound streaming kernel.  Each thread owns one 16-byte unit (8 bf16
-// channels); the two lanes of a pair own the two halves of a 16-channel
+// HBM-bound streaming kernel.  A thread takes 16-byte units (8 bf16 channels),
+// UNR per pass; the two lanes of a pair own the two halves of a 16-channel
 // group and exchange their half-amax with one shuffle.  Loads are 128-bit,
 // read-only and L1-bypassing; each unit writes 4 code bytes and (even lane)
 // 1 scale byte.
