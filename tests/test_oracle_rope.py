@@ -50,6 +50,22 @@ def test_unit_vectors_give_the_table_rounded_to_bf16():
     assert (out[1, 0::2] == _bits(-s)).all() and (out[1, 1::2] == _bits(c)).all()
 
 
+def test_equal_cos_and_sin_cancel_exactly_without_fma():
+    """With cos = sin (the same fp32 value) and a pair (a, a), the two products
+    of the first output are the same rounded fp32 number, so it is exactly +0;
+    the second is twice that product.  A fused multiply-add would leave the
+    product's rounding error in the first output instead of 0."""
+    rng = np.random.default_rng(8)
+    a = _bits(rng.standard_normal(4 * 32) * 5).reshape(4, 32)
+    x = np.stack([a, a], -1).reshape(4, 64)
+    c = np.float32(np.sqrt(0.5))
+    out = oracle.rope_bf16(x, np.zeros(4, np.int32), _table([[c, c]] * 32), rope_dim=64)
+    prod = _vals(a) * c                                   # fp32 product, rounded once
+    assert (out[:, 0::2] == 0).all()                      # +0 bits
+    assert (out[:, 1::2] == _bits(prod + prod)).all()
+    assert (_vals(a).astype(np.float64) * float(c) != prod).any()   # the products are inexact
+
+
 def test_channels_before_the_rope_range_pass_through_and_positions_select_rows():
     rng = np.random.default_rng(3)
     x = _bits(rng.standard_normal((6, 576)))
