@@ -606,6 +606,9 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(budget_s=args.cpu_budget)
+        if args.cpu_workers != 1:
+            cpu["all_cores"] = cpu_baseline_all_cores(LAYERS / cpu["value"], budget_s=args.cpu_budget,
+                                                      workers=args.cpu_workers or None)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -691,8 +694,84 @@ def cpu_baseline(budget_s=15.0, per_step_budget=None):
     _oracle_step(orc, s, n_seq, DECODER_SCHEDULE)
     el = time.perf_counter() - t
     return {"value": n_seq * LAYERS / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d of %d sequences x %d layers (one decode step), single-threaded C fp64; %.1f s"
-                      % (n_seq, B, LAYERS, el)}
+            "sample": "%d of %d sequences x %d layers (one decode step), single-threaded C fp64, %s; %.1f s"
+                      % (n_seq, B, LAYERS, _cpu_model(), el)}
+
+
+def _cpu_model():
+    """CPU model string for the report (``model name`` on x86, the Arm part
+    number otherwise), with the architecture."""
+    import platform
+    name = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                k, _, v = ln.partition(":")
+                if k.strip() in ("model name", "CPU part") and v.strip():
+                    name = v.strip() if k.strip() == "model name" else "Arm CPU part " + v.strip()
+                    break
+    except OSError:
+        pass
+    return "%s (%s)" % (name or "unknown", platform.machine())
+
+
+def _oracle_worker(seed, n_seq, schedule, barrier, out_q):
+    """One process of the all-cores CPU baseline: its own seeded sequences
+    through the same oracle step, timed from a common start."""
+    import oracle as orc
+    try:
+        s = _oracle_sample(n_seq, seed=seed)
+        barrier.wait(timeout=600)
+        t0 = time.monotonic()
+        _oracle_step(orc, s, n_seq, schedule)
+        out_q.put((t0, time.monotonic(), n_seq, None))
+    except Exception as e:  # reported to the parent, which raises
+        out_q.put((0.0, 0.0, 0, repr(e)))
+
+
+def cpu_baseline_all_cores(per_seq_s, budget_s=10.0, workers=None):
+    """The oracle as it stands, one process per host core (the rows spread
+    over cores; each process runs whole sequences of its own seed through the
+    20-layer step).  Value = all processes' token-layers / (last end - first
+    start).  Processes are spawned, never forked, so no CUDA state is shared."""
+    import multiprocessing as mp
+    import oracle as orc
+    from sparse_attention_fp4_quantize_gb300.decode import DECODER_SCHEDULE
+    orc.build()
+    n = int(workers or os.cpu_count() or 1)
+    n_seq = int(max(1, min(4, budget_s // max(per_seq_s, 1e-3))))
+    ctx = mp.get_context("spawn")
+    barrier, q = ctx.Barrier(n), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(1000 + i, n_seq, list(DECODER_SCHEDULE), barrier, q))
+             for i in range(n)]
+    for pr in procs:
+        pr.start()
+    import queue
+    res, deadline = [], time.monotonic() + 1800
+    try:
+        while len(res) < n:
+            try:
+                res.append(q.get(timeout=1.0))
+            except queue.Empty:
+                # a process that died (or every process ended) without its result
+                if any(pr.exitcode not in (None, 0) for pr in procs) or time.monotonic() > deadline or \
+                        not any(pr.is_alive() for pr in procs):
+                    raise RuntimeError("oracle workers ended without a result (exit codes %s)"
+                                       % [pr.exitcode for pr in procs])
+    finally:
+        for pr in procs:
+            pr.join(timeout=5 if len(res) < n else 60)
+            if pr.is_alive():
+                pr.terminate()
+                pr.join(timeout=10)
+    errs = [r[3] for r in res if r[3]]
+    if errs:
+        raise RuntimeError("oracle worker failed: " + errs[0])
+    el = max(r[1] for r in res) - min(r[0] for r in res)
+    total = sum(r[2] for r in res)
+    return {"value": total * LAYERS / el, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": "%d processes x %d sequences x %d layers (one decode step each), C fp64, %s; %.2f s"
+                      % (n, n_seq, LAYERS, _cpu_model(), el)}
 
 
 def run_reference(args):
@@ -777,6 +856,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-workers", type=int, default=0,
+                    help="processes for the all-cores oracle baseline (0: one per host core; 1: skip it)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' timings")
     ap.add_argument("--profile-case", nargs="?", const="decode", default=None, choices=["decode", "append", "prefill"],
                     help="a small case for ncu: 3 eager decode steps (default), the 1M-row append, or the prefill indexer")

@@ -84,3 +84,13 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     # must return at once: no oracle build, no output
     assert bench.run_reference(Args()) is None
     assert capsys.readouterr().out == ""
+
+
+def test_all_cores_cpu_baseline_spawns_workers_and_counts_their_work():
+    """The all-cores oracle baseline: two spawned processes, one sequence
+    each through the 20-layer oracle step; the value counts both."""
+    r = bench.cpu_baseline_all_cores(per_seq_s=100.0, budget_s=0.0, workers=2)
+    assert r["cores"] == 2 and r["kind"] == "oracle" and r["unit"] == bench.UNIT
+    assert r["sample"].startswith("2 processes x 1 sequences x 20 layers")
+    el = float(r["sample"].rsplit(";", 1)[1].strip().rstrip("s"))
+    assert r["value"] == pytest.approx(2 * bench.LAYERS / el, rel=0.03)
