@@ -212,21 +212,27 @@ def _kernel_breakdown(steps, stream, rounds):
     orig = {fn: getattr(dec, fn) for fn in kinds.values()}
     out = {}
     for kind, keep in kinds.items():
-        count = [0]
+        count, dry = [0], [True]
 
         def make(fn_name, fn):
             def inner(*a, **kw):
                 if fn_name != keep:
                     return None
                 if fn_name in ("csa2_index_score", "csa2_topk", "csa2_index_topk") and a[0] == csa2.MODE_REUSE:
-                    return fn(*a, **kw)          # no launch
+                    return None if dry[0] else fn(*a, **kw)          # no launch
                 count[0] += 1
-                return fn(*a, **kw)
+                return None if dry[0] else fn(*a, **kw)
             return inner
 
         for fn_name, fn in orig.items():
             setattr(dec, fn_name, make(fn_name, fn))
         try:
+            # count this kind's calls first (nothing launched): a kind the
+            # step never calls gets no (empty) graph
+            steps[0].run(stream=stream)
+            if count[0] == 0:
+                continue
+            dry[0] = False
             graphs = []
             for st in steps:
                 count[0] = 0
