@@ -72,3 +72,31 @@ def test_bound_on_adversarial_rows():
     ]
     for row in rows:
         _check(row, K)
+
+
+def test_bound_with_interval_block_maxima():
+    """With only an interval L_b <= max_b <= U_b per block (e.g. from packed
+    low-precision arithmetic), let tau_L be the K-th largest L_b: at least K
+    scores reach tau_L, so the blocks with U_b >= tau_L hold a Top-K of the
+    row (every score elsewhere is < tau_L)."""
+    rng = np.random.default_rng(11)
+    K = 64
+    for trial in range(40):
+        n = int(rng.integers(600, 4000))
+        row = rng.standard_normal(n) if trial % 2 else rng.integers(0, 6, n).astype(float)
+        row = row.astype(np.float32).astype(np.float64)      # the values the selection sees
+        nb = (n + 7) // 8
+        bm = np.concatenate([row, np.full(nb * 8 - n, -np.inf)]).reshape(nb, 8).max(1)
+        err = 10.0 ** rng.uniform(-6, -2)
+        lo = bm - err * (np.abs(bm) + 1) * rng.random(nb)
+        hi = bm + err * (np.abs(bm) + 1) * rng.random(nb)
+        tau_l = np.sort(lo)[::-1][K - 1]
+        keep = np.nonzero(hi >= tau_l)[0]
+        assert keep.size >= K
+        cand = np.concatenate([np.arange(8 * b, min(8 * b + 8, n)) for b in keep])
+        outside = np.setdiff1d(np.arange(n), cand)
+        assert (row[outside] < tau_l).all()
+        want = oracle.topk(oracle.FULL, row.astype(np.float32)[None, None, :], None, K=K)[0, 0]
+        kth = min(row[j] for j in want)
+        got = cand[np.argsort(-row[cand], kind="stable")[:K]]
+        assert all(row[j] == kth for j in set(got.tolist()) ^ set(want.tolist()))
