@@ -49,7 +49,7 @@ typedef enum {
     CSA2_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required     */
     CSA2_ERR_CUDA = 4,         /* a CUDA runtime error at launch                 */
     CSA2_ERR_DEVICE_FLAG = 5,  /* reserved for callers that map *err_flag        */
-    CSA2_ERR_TIMEOUT = 6       /* reserved: no kernel here spin-waits            */
+    CSA2_ERR_TIMEOUT = 6       /* reserved for callers that map CSA2_FLAG_TIMEOUT */
 } csa2_status;
 
 typedef enum {
@@ -251,8 +251,10 @@ size_t csa2_index_topk_dense_workspace_bytes(int B, int T, int64_t N, int K);
  *   z_j = sm_scale * sum_{c<D} q[c] * Khat[j][c]
  *   out[c] = sum_j softmax(z)_j * Khat[j][c]   for c < dv
  *   lse = log sum_j exp(z_j)
- * Khat is the dequantised entry (E2M1 value x its group's E4M3 scale),
- * computed in registers from the FP4 planes; V is its first dv channels.
+ * Khat is the dequantised entry (E2M1 value x its group's E4M3 scale,
+ * exact in f16), computed on chip from the FP4 planes; V is its first dv
+ * channels.  The scores and P V run on the tensor cores with fp32
+ * accumulation; P is rounded to f16.
  * An empty J gives out = 0 and lse = -inf.
  * mode  any: REUSE layers pass their source layer's idx (and KV, or their
  *       own KV) unchanged ([ENG] CSA2 section; [55ZB], [HUNT] CSA2 paragraphs).
@@ -266,9 +268,13 @@ size_t csa2_index_topk_dense_workspace_bytes(int B, int T, int64_t N, int K);
  * idx     int32 [B, T, K], entries j in [0, kv_len) or -1 (skipped);
  *         anything else is skipped and sets CSA2_FLAG_BAD_INDEX.  K <= 2048.
  * kv_len  int32 [B*T] or NULL (= N).
- * out     fp32 [B, T, H, dv] (out_dt must be CSA2_FP32); lse fp32 [B, T, H]
- *         or NULL.
- * workspace csa2_sparse_attn_workspace_bytes() bytes (split-KV partials).
+ * out     fp32 [B, T, H, dv] (out_dt must be CSA2_FP32), 16-byte aligned;
+ *         lse fp32 [B, T, H] or NULL.
+ * err_flag  CSA2_FLAG_BAD_INDEX as above; CSA2_FLAG_TIMEOUT if a bounded
+ *         on-chip wait gave up (that launch's results are invalid).
+ * workspace csa2_sparse_attn_workspace_bytes() bytes: 0 for D = 576 with
+ *         K <= 512 (a cluster of CTAs merges its partials on chip), else the
+ *         split-KV partials; NULL allowed when 0.
  */
 csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H, int D, int dv,
                                  const void *q, const uint8_t *codes, const uint8_t *scales,
