@@ -6,11 +6,13 @@ pointers, shapes and the current CUDA stream to the C ABI declared in
 ``include/csa2.h`` and raises ``Csa2Error`` on a non-OK status.  There is no
 CPU fallback: if the shared library is missing the import fails loudly.
 
-Names follow the C ABI: ``csa2_quantize_kv_fp4``, ``csa2_index_score``,
-``csa2_build_pool``, ``csa2_topk``, ``csa2_index_topk`` (fused decode indexer),
+Names follow the C ABI: ``csa2_quantize_kv_fp4``, ``csa2_rope_quantize_kv_fp4``
+(RoPE fused ahead of the quantiser), ``csa2_index_score``, ``csa2_build_pool``,
+``csa2_topk``, ``csa2_index_topk`` (fused decode indexer),
 ``csa2_index_topk_dense`` (fused indexer for many query tokens),
-``csa2_sparse_attn_fp4`` and the
-``*_workspace_bytes`` helpers.
+``csa2_sparse_attn_fp4`` (and ``csa2_sparse_attn_fp4_noalloc``),
+``csa2_swa_attn_fp8`` (sliding-window branch and merge),
+``csa2_selftest_bounded_wait`` and the ``*_workspace_bytes`` helpers.
 """
 from __future__ import annotations
 
