@@ -339,9 +339,9 @@ def _attn_gpu(csa2, q, codes, scales, N, idx, kv_len, sm, dv, flag=None):
     ("full", 40, 1, 3000, 512, 64, 0.0),      # many rows: no split-KV
     ("full", 1, 1, 600, 33, 64, 0.0),
     ("full", 2, 1, 2000, 1, 64, 0.0),
-    ("full", 3, 1, 4000, 1024, 64, 0.1),      # 8-CTA cluster
-    ("full", 2, 2, 3000, 700, 64, 0.0),       # 6-CTA cluster, ragged channel slices
-    ("full", 1, 1, 3000, 1500, 64, 0.0),      # K > 1024: split-KV path
+    ("full", 3, 1, 4000, 1024, 64, 0.1),      # K > 512: the mma.sync kernel
+    ("full", 2, 2, 3000, 700, 64, 0.0),       # K > 512, not a multiple of the entry tile
+    ("full", 1, 1, 3000, 1500, 64, 0.0),      # one row, K = 1500: split-KV partials + combine
 ])
 def test_sparse_attn_matches_oracle(csa2, base, B, T, N, K, H, pad):
     w0 = gen.TINY_FULL_DECODE if base == "tiny" else gen.FULL_BATCHED_DECODE
@@ -383,7 +383,7 @@ def test_sparse_attn_workspace_is_required_when_split(csa2):
     q = torch.zeros(1, 1, 64, 576, dtype=torch.int16, device=DEV)
     codes = torch.zeros(100, 288, dtype=torch.uint8, device=DEV)
     scales = torch.zeros(100, 36, dtype=torch.uint8, device=DEV)
-    idx = torch.zeros(1, 1, 1536, dtype=torch.int32, device=DEV)     # K > 1024: split-KV path
+    idx = torch.zeros(1, 1, 1536, dtype=torch.int32, device=DEV)     # K > 512 on one row: split-KV partials
     out = torch.zeros(1, 1, 64, 512, device=DEV)
     assert csa2.csa2_sparse_attn_workspace_bytes(1, 1, 64, 576, 512, 512) == 0   # tcgen05 path: no scratch
     assert csa2.csa2_sparse_attn_workspace_bytes(1, 1, 64, 576, 512, 1536) > 0
