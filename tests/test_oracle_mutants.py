@@ -40,6 +40,8 @@ MUTANTS = {
     "e2m1 saturates to code 6": [("if (r >= 6.0) return 7;", "if (r >= 6.0) return 6;")],
     "e2m1 step 4 in [4, 6)": [("return (uint8_t)(6 + rne((r - 4.0) / 2.0));",
                                "return (uint8_t)(6 + rne((r - 4.0) / 4.0));")],
+    "e4m3 subnormals flushed to zero": [("n = rne(a / ldexp(1.0, -9));", "n = 0.0 * a;")],
+    "e2m1 step 0.25 below 1": [("if (r < 1.0) return (uint8_t)rne(r / 0.5);", "if (r < 1.0) return (uint8_t)rne(r / 0.25);")],
     # quantiser
     "scale amax / 4": [("sbyte = orc_e4m3_encode_pos(amax / 6.0);", "sbyte = orc_e4m3_encode_pos(amax / 4.0);")],
     "amax over 8 channels": [("for (c = 16 * g; c < 16 * g + 16; ++c) {\n                double v",
@@ -65,6 +67,9 @@ MUTANTS = {
         ("y[D - rope_dim + 2 * i] = f32_to_bf16_rne(ra);", "y[D - rope_dim + i] = f32_to_bf16_rne(ra);"),
         ("y[D - rope_dim + 2 * i + 1] = f32_to_bf16_rne(rb);", "y[D - rope_dim / 2 + i] = f32_to_bf16_rne(rb);")],
     "bf16 rounding truncates": [("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0u;")],
+    "RoPE on the first channels": [
+        ("const float a = bf16_to_f32(x[D - rope_dim + 2 * i]);", "const float a = bf16_to_f32(x[2 * i]);"),
+        ("const float b = bf16_to_f32(x[D - rope_dim + 2 * i + 1]);", "const float b = bf16_to_f32(x[2 * i + 1]);")],
     # indexer scores
     "ReLU dropped": [("s += (double)w[woff + h] * (dot > 0.0 ? dot : 0.0);", "s += (double)w[woff + h] * dot;")],
     "head 0's weight for every head": [("s += (double)w[woff + h] * (dot > 0.0 ? dot : 0.0);",
@@ -80,6 +85,8 @@ MUTANTS = {
     "block maximum skips the 8th position": [("for (j = beta * G; j < beta * G + G && j < len; ++j) {",
                                               "for (j = beta * G; j < beta * G + G - 1 && j < len; ++j) {")],
     "block score is its first position": [("if (v > m) m = v;", "if (m == -INFINITY) m = v;")],
+    "partial last block never scores": [("for (j = beta * G; j < beta * G + G && j < len; ++j) {",
+                                         "for (j = beta * G; j < beta * G + G && beta * G + G <= len; ++j) {")],
     # selection
     "ties go to the higher position": [("return (x->i < y->i) ? -1 : (x->i > y->i);",
                                         "return (x->i > y->i) ? -1 : (x->i < y->i);")],
@@ -98,7 +105,13 @@ MUTANTS = {
     "one scale per 32 channels": [("orc_e4m3_value(srow[c / 16]);", "orc_e4m3_value(srow[c / 32]);")],
     "dequant reads the nibbles swapped": [("uint8_t code = (c & 1) ? (byte >> 4) : (byte & 0xF);",
                                            "uint8_t code = (c & 1) ? (byte & 0xF) : (byte >> 4);")],
+    "sm_scale applied twice": [("acc += bf16_value(qr[c]) * kh[(int64_t)i * D + c];\n                z[i] = sm_scale * acc;",
+                                "acc += bf16_value(qr[c]) * kh[(int64_t)i * D + c];\n                z[i] = sm_scale * sm_scale * acc;")],
+    "query channels beyond dv ignored": [("for (c = 0; c < D; ++c) acc += bf16_value(qr[c]) * kh[(int64_t)i * D + c];",
+                                          "for (c = 0; c < dv; ++c) acc += bf16_value(qr[c]) * kh[(int64_t)i * D + c];")],
     # sliding window + merge
+    "window logits without sm_scale": [("for (c = 0; c < D; ++c) acc += bf16_value(qr[c]) * orc_e4m3_value(kr[c]);\n                z[i] = sm_scale * acc;",
+                                        "for (c = 0; c < D; ++c) acc += bf16_value(qr[c]) * orc_e4m3_value(kr[c]);\n                z[i] = acc;")],
     "merge weights swapped": [("o[c] = (a * ow[c] + cs * os) / (a + cs);", "o[c] = (cs * ow[c] + a * os) / (a + cs);")],
     "merged lse is the window's": [("if (lse) lse[bt * H + h] = M + log(a + cs);", "if (lse) lse[bt * H + h] = lw;")],
     "window V is the last dv channels": [("for (c = 0; c < dv; ++c) ow[c] += p * orc_e4m3_value(kr[c]);",
