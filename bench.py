@@ -684,7 +684,7 @@ def _oracle_step(orc, s, n_seq, schedule):
         orc.sparse_attn(s["q"][layer], codes, scales, NCAP, idx, s["kv_len"], sm, DV)
 
 
-def cpu_baseline(budget_s=15.0, per_step_budget=None):
+def cpu_baseline(budget_s=15.0):
     """Time the oracle as it stands (single-threaded C, fp64) on a bounded
     sample of the workload: whole sequences through the 20-layer schedule."""
     import oracle as orc
