@@ -1,14 +1,12 @@
 """GPU parity of each libcsa2 call against the CPU oracle on identical inputs
 (through the C ABI via the Python binding).  Marked gpu."""
-import math
-
 import numpy as np
 import pytest
 import torch
 
 import gen
 import oracle
-from helpers import check_attn, check_lse, check_scores, check_selection
+from helpers import check_attn, check_lse, check_scores
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
