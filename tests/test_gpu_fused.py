@@ -77,6 +77,27 @@ def test_fused_full_matches_oracle_chain(csa2, B, T, N, K, P_out):
         _check_rows(got_pool, want_pool, lambda b, t: bm[b, t], P_out, "fused pool")
 
 
+def test_fused_full_short_and_empty_rows(csa2):
+    """Rows with no visible entry (all -1), fewer visible entries than K or
+    than the pool's blocks, a partial last block, and kv_len beyond N
+    (clamped), with the pool written."""
+    B, T, N, K, P_out = 1, 8, 4000, 512, 2048
+    q = gen.normal_e4m3(23, 1, (B, T, 4, 64))
+    k = gen.normal_e4m3(23, 2, (B, N, 64))
+    w = gen.uniform01(23, 3, (B, T, 4))
+    kl = torch.tensor([0, 1, 7, 9, 511, 513, 4000, 10 ** 6], dtype=torch.int32)
+    ref = _ref_scores(0, q, w, k, kl)
+    s32 = ref.astype(np.float32)
+    got_idx, got_pool = _fused(csa2, 0, q, w, k, kl, K, P_out=P_out)
+    want_idx = oracle.topk(oracle.FULL, s32, gen.as_numpy(kl), K=K)
+    _check_rows(got_idx, want_idx, lambda b, t: ref[b, t], K, "fused topk (short rows)")
+    want_pool = oracle.build_pool(s32, gen.as_numpy(kl), P=P_out)
+    bm = _block_max(ref, gen.as_numpy(kl))
+    _check_rows(got_pool, want_pool, lambda b, t: bm[b, t], P_out, "fused pool (short rows)")
+    assert (got_idx[0, 0] == -1).all() and (got_pool[0, 0] == -1).all()
+    assert sorted(got_idx[0, 2][got_idx[0, 2] >= 0].tolist()) == list(range(7))
+
+
 def test_fused_full_batched_decode_full_size(csa2):
     """B=32 sequences x n_b in [8192,16384] entries, Top-512 and the 2048-block pool."""
     w = gen.FULL_BATCHED_DECODE

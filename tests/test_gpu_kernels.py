@@ -357,6 +357,32 @@ def test_sparse_attn_matches_oracle(csa2, base, B, T, N, K, H, pad):
     check_lse(glse, rlse)
 
 
+def test_sparse_attn_cluster_slices_empty_and_repeated_entries(csa2):
+    """K = 512 on the tensor-core path splits a row over 4 CTAs of 128
+    entries.  Rows whose last, first or first three slices hold only -1, a
+    row selecting one entry 512 times, one selecting every entry twice (in
+    different slices) and one with every other slot -1, against the oracle;
+    kv_len NULL stands for N."""
+    N, K = 3000, 512
+    w = gen.scaled(gen.FULL_BATCHED_DECODE, B=6, T=1, N=N, K=K, H=64)
+    codes, scales = _kv_planes(gen.FULL_BATCHED_DECODE, 6, N)
+    idx = gen.as_numpy(gen.random_indices(w, torch.full((6,), N, dtype=torch.int32))).copy()
+    idx[0, 0, 384:] = -1
+    idx[1, 0, :128] = -1
+    idx[2, 0, :384] = -1
+    idx[3, 0, :] = 1234
+    idx[4, 0, 256:] = idx[4, 0, :256]
+    idx[5, 0, 1::2] = -1
+    q = gen.attn_query(w)
+    sm = gen.softmax_scale(w.D)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got, glse = _attn_gpu(csa2, q, codes, scales, N, idx, None, sm, w.dv, flag=flag)
+    ref, rlse, bad = oracle.sparse_attn(gen.as_numpy(q), codes, scales, N, idx, None, sm, w.dv)
+    assert bad == 0 and int(flag.item()) == 0
+    check_attn(got, ref)
+    check_lse(glse, rlse)
+
+
 def test_sparse_attn_empty_rows_and_bad_indices(csa2):
     w = gen.scaled(gen.FULL_BATCHED_DECODE, B=2, T=2, N=1000, K=64)
     codes, scales = _kv_planes(gen.FULL_BATCHED_DECODE, 2, 1000)
