@@ -259,7 +259,9 @@ size_t csa2_index_topk_dense_workspace_bytes(int B, int T, int64_t N, int K);
  * mode  any: REUSE layers pass their source layer's idx (and KV, or their
  *       own KV) unchanged ([ENG] CSA2 section; [55ZB], [HUNT] CSA2 paragraphs).
  *
- * q       bf16 [B, T, H, D], 16-byte aligned.  Supported (D, dv, H):
+ * q       bf16 [B, T, H, D], 16-byte aligned, finite; on the D = 576 path each
+ *         (token, head) row's largest |q| must be below 2^76 (the row is
+ *         scaled by a power of two into f16).  Supported (D, dv, H):
  *         D = 576, dv = 512, H a multiple of 64; D = 128, dv = 64, H a
  *         multiple of 16.
  * codes   uint8 [B*N, D/2], scales uint8 [B*N, D/16]: entry j of sequence

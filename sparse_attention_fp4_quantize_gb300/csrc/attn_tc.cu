@@ -14,10 +14,10 @@
 //  1. The TMA engine gathers the operands: one bulk copy per Q head row
 //     (1152 B, on its own mbarrier) and one per selected entry's code row
 //     (288 B); the 36-byte scale rows (not 16-byte sized) are plain loads.
-//  2. Q (bf16) is scaled per head by a power of two into f16 (exact; the scale
+//  2. Q (bf16) is scaled per head by a power of two into f16 (exact down to
+//     2^-31 of the head's largest |q|, which must stay below 2^76; the scale
 //     is folded into the logit factor) while the code rows are in flight; the
-//     entries are dequantised once (E2M1 x E4M3 -> exact f16) into a
-//     no-swizzle core-matrix tile.
+//     entries are dequantised once (E2M1 x E4M3 -> exact f16) into a no-swizzle core-matrix tile.
 //  3. S^T [128 entries x 64 heads] = Khat . Q^T  (36 tcgen05.mma, M128 N64 K16)
 //  4. softmax on a transposed copy of S^T in shared memory; P -> f16.
 //  5. O^T [512 ch x 64 heads] = Vhat^T . P^T  (4 x 8 MMAs; the same Khat bytes
