@@ -298,7 +298,9 @@ size_t csa2_sparse_attn_workspace_bytes(int B, int T, int H, int D, int dv, int 
  *     M = max(lse_w, lse_s), a = e^(lse_w - M), c = e^(lse_s - M),
  *     out = (a o_w + c o_s) / (a + c),  lse = M + log(a + c).
  *
- * q          bf16 [B, T, H, D], D = 576, dv = 512, H a multiple of 64.
+ * q          bf16 [B, T, H, D], D = 576, dv = 512, H a multiple of 64; each
+ *            (token, head) row's largest |q| below 2^76, as in the sparse branch.
+ *            The window's E4M3 values enter the MMAs as exact f16.
  * swa_kv     E4M3 [B, W, D], 1 <= W <= 512, 16-byte aligned.
  * swa_len    int32 [B*T], clamped to [0, W].
  * o_sparse, lse_sparse  fp32 [B, T, H, dv] and [B, T, H] from

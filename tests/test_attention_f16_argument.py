@@ -29,6 +29,11 @@ def test_every_dequantised_value_is_an_exact_f16():
     assert nz.min() == 2.0 ** -10 and nz.max() == 2688.0
 
 
+def test_every_e4m3_window_value_is_an_exact_f16():
+    vals = np.array([oracle.e4m3_value(b) for b in range(256) if (b & 0x7F) != 0x7F])
+    assert (vals.astype(np.float16).astype(np.float64) == vals).all()
+
+
 def _bf16_positive():
     bits = np.arange(1, 0x7F80, dtype=np.uint32)
     return (bits << 16).view(np.float32).astype(np.float64)
