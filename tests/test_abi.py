@@ -158,3 +158,41 @@ def test_attention_rejects_bad_arguments_on_host(lib):
     assert f(0, 1, 1, 64, 576, 512, fake, fake, fake, 10, fake, 512, NULL, 0.1, fake, 0, NULL, NULL, NULL, 0, NULL) == 1
     # K out of range
     assert f(0, 1, 1, 64, 576, 512, fake, fake, fake, 10, fake, 0, NULL, 0.1, fake, 2, NULL, NULL, NULL, 0, NULL) == 1
+
+
+def test_fused_index_topk_rejects_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+    f = lib.csa2_index_topk
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, I64, P, ctypes.c_int, P, P, ctypes.c_int, P, P,
+                  ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int, P, P]
+    fake, FP8, BF16 = P(0x1000), 1, 0
+    assert f(2, 1, 1, 10, NULL, FP8, NULL, NULL, FP8, NULL, NULL, 0, 512, NULL, NULL, 0, NULL, NULL) == 0   # REUSE
+    assert f(5, 1, 1, 10, fake, FP8, fake, fake, FP8, fake, NULL, 0, 512, fake, NULL, 0, NULL, NULL) == 1   # bad mode
+    assert f(0, 1, 1, 10, fake, BF16, fake, fake, BF16, fake, NULL, 0, 512, fake, NULL, 0, NULL, NULL) == 1  # bf16
+    assert f(0, 1, 1, 10, fake, FP8, fake, fake, FP8, fake, NULL, 0, 0, fake, NULL, 0, NULL, NULL) == 1     # K = 0
+    assert f(0, 1, 1, 10, fake, FP8, fake, fake, FP8, fake, fake, 8, 512, fake, NULL, 0, NULL, NULL) == 1   # FULL + pool
+    assert f(0, 1, 1, 10, fake, FP8, fake, fake, FP8, fake, NULL, 0, 512, fake, fake, 4096, NULL, NULL) == 1  # P_out
+    assert f(1, 1, 1, 10, fake, FP8, fake, fake, FP8, fake, NULL, 8, 512, fake, NULL, 0, NULL, NULL) == 1   # no pool
+    assert f(1, 1, 1, 10, fake, FP8, fake, fake, FP8, fake, fake, 8, 512, fake, fake, 8, NULL, NULL) == 1   # pool_out
+    assert f(0, 1, 1, 10, P(0x1008), FP8, fake, fake, FP8, fake, NULL, 0, 512, fake, NULL, 0, NULL, NULL) == 1  # align
+    assert f(0, 1, 1, 10, fake, FP8, fake, fake, FP8, NULL, NULL, 0, 512, fake, NULL, 0, NULL, NULL) == 1   # kv_len
+    assert "kv_len" in _last_error(lib) or "null" in _last_error(lib)
+
+
+def test_swa_and_noalloc_attention_reject_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+    f = lib.csa2_swa_attn_fp8
+    f.argtypes = [ctypes.c_int] * 5 + [P, P, ctypes.c_int, P, ctypes.c_float, P, P, P, P, P, P]
+    fake = P(0x1000)
+    assert f(1, 1, 64, 576, 512, fake, fake, 0, fake, 0.1, NULL, NULL, fake, NULL, NULL, NULL) == 1     # W = 0
+    assert f(1, 1, 64, 576, 512, fake, fake, 1024, fake, 0.1, NULL, NULL, fake, NULL, NULL, NULL) == 1  # W > 512
+    assert f(1, 1, 64, 128, 64, fake, fake, 128, fake, 0.1, NULL, NULL, fake, NULL, NULL, NULL) == 2    # D = 128
+    assert f(1, 1, 32, 576, 512, fake, fake, 128, fake, 0.1, NULL, NULL, fake, NULL, NULL, NULL) == 2   # H % 64
+    assert f(1, 1, 64, 576, 512, fake, fake, 128, fake, 0.1, fake, NULL, fake, NULL, NULL, NULL) == 1   # o without lse
+    assert f(1, 1, 64, 576, 512, P(0x1004), fake, 128, fake, 0.1, NULL, NULL, fake, NULL, NULL, NULL) == 1  # align
+    assert f(0, 1, 64, 576, 512, NULL, NULL, 128, NULL, 0.1, NULL, NULL, NULL, NULL, NULL, NULL) == 0    # empty
+    g = lib.csa2_sparse_attn_fp4_noalloc
+    g.argtypes = [ctypes.c_int] * 6 + [P, P, P, I64, P, ctypes.c_int, P, ctypes.c_float, P, ctypes.c_int, P, P, P]
+    assert g(0, 1, 1, 64, 256, 192, fake, fake, fake, 10, fake, 512, NULL, 0.1, fake, 2, NULL, NULL, NULL) == 2
+    assert g(0, 1, 1, 64, 576, 512, fake, fake, fake, 10, fake, 0, NULL, 0.1, fake, 2, NULL, NULL, NULL) == 1
+    assert g(7, 1, 1, 64, 576, 512, fake, fake, fake, 10, fake, 512, NULL, 0.1, fake, 2, NULL, NULL, NULL) == 1
