@@ -94,3 +94,19 @@ def test_all_cores_cpu_baseline_spawns_workers_and_counts_their_work():
     assert r["sample"].startswith("2 processes x 1 sequences x 20 layers")
     el = float(r["sample"].rsplit(";", 1)[1].strip().rstrip("s"))
     assert r["value"] == pytest.approx(2 * bench.LAYERS / el, rel=0.03)
+
+
+def test_traffic_record_is_used_only_while_the_source_is_unchanged(tmp_path, monkeypatch):
+    import hashlib
+    import json
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1\n")
+    (tmp_path / "profiles").mkdir()
+    rec = {"k_kernel": {"source": "k.cu", "source_sha256_16": hashlib.sha256(b"kernel v1\n").hexdigest()[:16],
+                        "dram_bytes_per_launch": 1234}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._traffic_record("k_kernel") == 1234
+    assert bench._traffic_record("other_kernel") is None
+    src.write_text("kernel v2\n")                        # the kernel changed since the capture
+    assert bench._traffic_record("k_kernel") is None
