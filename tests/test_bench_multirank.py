@@ -110,3 +110,19 @@ def test_traffic_record_is_used_only_while_the_source_is_unchanged(tmp_path, mon
     assert bench._traffic_record("other_kernel") is None
     src.write_text("kernel v2\n")                        # the kernel changed since the capture
     assert bench._traffic_record("k_kernel") is None
+
+
+def test_clock_summary_takes_the_timed_window_and_the_active_reasons():
+    c = bench.ClockSampler(0)
+    row = "0, {sm}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, {cap}"
+    c.samples = [(9.0, row.format(sm=1000, cap="Not Active")),          # before the timed region
+                 (10.1, row.format(sm=2070, cap="Not Active")),
+                 (10.2, row.format(sm=1965, cap="Active")),
+                 (10.3, "garbage line"),
+                 (10.4, row.format(sm=2055, cap="Not Active")),
+                 (12.0, row.format(sm=500, cap="Not Active"))]          # after it
+    s = c.summary(10.0, 11.0)
+    assert s["samples"] == 3 and s["sm_mhz"] == 2055 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]
+    assert c.summary(10.45, 10.5)["samples"] == 3                        # shorter than a period: nearest samples
+    assert bench.ClockSampler(0).summary(0, 1)["reasons"] == ["nvidia-smi unavailable"]
