@@ -1,9 +1,10 @@
-"""Host logic of the benchmark's multi-rank mode, on CPU with gloo.
+"""Host logic of the benchmark, on the CPU (no GPU and no CUDA call).
 
 bench.py under torchrun runs one replica per GPU (the decode path shards by
 sequence and has no exchange step): every rank draws its own sequences, times
 its own steps, and the job's time is the slowest rank's.  These tests run
-that logic with two gloo ranks on the CPU; no GPU and no CUDA call is made.
+that logic with two gloo ranks, and check the all-cores oracle baseline, the
+DRAM traffic record's validity rule and the clock summary.
 """
 import os
 import socket
