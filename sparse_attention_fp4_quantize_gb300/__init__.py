@@ -3,8 +3,11 @@ cache, as hand-written CUDA kernels for GB300 (sm_103a).
 
 Argument marshalling only: every function passes torch tensors' device
 pointers, shapes and the current CUDA stream to the C ABI declared in
-``include/csa2.h`` and raises ``Csa2Error`` on a non-OK status.  There is no
-CPU fallback: if the shared library is missing the import fails loudly.
+``include/csa2.h`` and raises ``Csa2Error`` on a non-OK status.  Since the C
+calls see bare pointers, the binding first refuses (TypeError / ValueError)
+tensors whose element size does not match what the call reads or writes and
+buffers smaller than the call touches.  There is no CPU fallback: if the
+shared library is missing the import fails loudly.
 
 Names follow the C ABI: ``csa2_quantize_kv_fp4``, ``csa2_rope_quantize_kv_fp4``
 (RoPE fused ahead of the quantiser), ``csa2_index_score``, ``csa2_build_pool``,
@@ -115,6 +118,37 @@ def _cuda(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+def _elem(t, name, sizes, floating=None):
+    """The C call reads or writes t's memory as elements of one of these
+    byte sizes (and of this kind, when given)."""
+    if t is None:
+        return
+    if t.element_size() not in sizes or (floating is not None and t.is_floating_point() != floating):
+        raise TypeError("%s: %s elements do not fit this call" % (name, t.dtype))
+
+
+def _room(t, name, n):
+    """t must hold every element the call touches (the C side sees only a pointer)."""
+    if t is not None and t.numel() < n:
+        raise ValueError("%s holds %d elements, the call touches %d" % (name, t.numel(), n))
+
+
+def _flag(err_flag):
+    _elem(err_flag, "err_flag", (4,), False)
+    _room(err_flag, "err_flag", 1)
+
+
+def _indexer_operands(q_idx, w, k_idx, kv_len, B, T, N):
+    _elem(q_idx, "q_idx", (1, 2))
+    _elem(k_idx, "k_idx", (1, 2))
+    _elem(w, "w", (4,), True)
+    _elem(kv_len, "kv_len", (4,), False)
+    _room(q_idx, "q_idx", B * T * INDEX_HEADS * INDEX_DIM)
+    _room(k_idx, "k_idx", B * N * INDEX_DIM)
+    _room(w, "w", B * T * INDEX_HEADS)
+    _room(kv_len, "kv_len", B * T)
+
+
 def csa2_selftest_bounded_wait(err_flag, max_polls=4096, stream=None):
     """The kernels' bounded mbarrier wait on an arrival that never comes:
     sets FLAG_TIMEOUT in err_flag (int32/uint32 CUDA tensor) and returns."""
@@ -126,6 +160,18 @@ def version() -> int:
     return _lib.csa2_version()
 
 
+def _plane_args(kv, codes, scales, dst_slot, err_flag, R, D, n_slots):
+    _elem(kv, "kv", (2,))
+    _elem(codes, "codes", (1,))
+    _elem(scales, "scales", (1,))
+    _elem(dst_slot, "dst_slot", (8,), False)
+    _flag(err_flag)
+    if codes.dim() != 2 or codes.shape[1] != D // 2:
+        raise ValueError("codes must be [slots, D/2] = [*, %d], got %s" % (D // 2, tuple(codes.shape)))
+    _room(scales, "scales", n_slots * (D // 16))
+    _room(dst_slot, "dst_slot", R)
+
+
 def csa2_quantize_kv_fp4(kv, codes, scales, dst_slot=None, err_flag=None, stream=None):
     """kv bf16 [R, D] (or int16 bits) -> codes uint8 [S, D/2], scales uint8 [S, D/16]."""
     _cuda(codes, scales, dst_slot, err_flag)
@@ -133,6 +179,7 @@ def csa2_quantize_kv_fp4(kv, codes, scales, dst_slot=None, err_flag=None, stream
     if not kv.is_cuda or kv.stride(1) != 1:
         raise ValueError("kv must be a CUDA tensor with contiguous rows (any row stride)")
     n_slots = codes.shape[0]
+    _plane_args(kv, codes, scales, dst_slot, err_flag, R, D, n_slots)
     _check(_lib.csa2_quantize_kv_fp4(_ptr(kv), R, D, kv.stride(0), _ptr(dst_slot), n_slots, _ptr(codes),
                                      _ptr(scales), _ptr(err_flag), _stream(stream)))
 
@@ -142,6 +189,12 @@ def csa2_rope_quantize_kv_fp4(kv, pos, cos_sin, codes, scales, dst_slot=None, er
     [n_pos, rope_dim/2, 2] -> codes uint8 [S, D/2], scales uint8 [S, D/16]."""
     _cuda(kv, pos, cos_sin, codes, scales, dst_slot, err_flag)
     R, D = kv.shape
+    _plane_args(kv, codes, scales, dst_slot, err_flag, R, D, codes.shape[0])
+    _elem(pos, "pos", (4,), False)
+    _elem(cos_sin, "cos_sin", (4,), True)
+    _room(pos, "pos", R)
+    if cos_sin.dim() != 3 or cos_sin.shape[2] != 2:
+        raise ValueError("cos_sin must be [n_pos, rope_dim/2, 2], got %s" % (tuple(cos_sin.shape),))
     n_pos, half = cos_sin.shape[0], cos_sin.shape[1]
     _check(_lib.csa2_rope_quantize_kv_fp4(_ptr(kv), R, D, D, _ptr(pos), _ptr(cos_sin), n_pos, 2 * half,
                                           _ptr(dst_slot), codes.shape[0], _ptr(codes), _ptr(scales),
@@ -155,6 +208,13 @@ def csa2_index_score(mode, q_idx, w, k_idx, kv_len, scores, pool_blocks=None, er
     B, T = q_idx.shape[0], q_idx.shape[1]
     N = k_idx.shape[1]
     P = 0 if pool_blocks is None else pool_blocks.shape[-1]
+    if int(mode) != MODE_REUSE:
+        _indexer_operands(q_idx, w, k_idx, kv_len, B, T, N)
+        _elem(scores, "scores", (4,), True)
+        _elem(pool_blocks, "pool_blocks", (4,), False)
+        _flag(err_flag)
+        _room(scores, "scores", B * T * (8 * P if int(mode) == MODE_REINDEX else N))
+        _room(pool_blocks, "pool_blocks", B * T * P)
     _check(_lib.csa2_index_score(int(mode), B, T, N, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), _ptr(k_idx),
                                  _dtype_code(k_idx), _ptr(kv_len), _ptr(pool_blocks), P, _ptr(scores),
                                  _ptr(err_flag), _stream(stream)))
@@ -165,6 +225,11 @@ def csa2_build_pool(scores, kv_len, pool_blocks, workspace=None, stream=None):
     _cuda(scores, kv_len, pool_blocks, workspace)
     B, T, N = scores.shape
     P = pool_blocks.shape[-1]
+    _elem(scores, "scores", (4,), True)
+    _elem(kv_len, "kv_len", (4,), False)
+    _elem(pool_blocks, "pool_blocks", (4,), False)
+    _room(kv_len, "kv_len", B * T)
+    _room(pool_blocks, "pool_blocks", B * T * P)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.csa2_build_pool(B, T, N, _ptr(scores), _ptr(kv_len), P, POOL_BLOCK, _ptr(pool_blocks),
                                 _ptr(workspace), ws, _stream(stream)))
@@ -176,6 +241,13 @@ def csa2_topk(mode, scores, idx, kv_len=None, pool_blocks=None, workspace=None, 
     B, T, M = scores.shape
     K = idx.shape[-1]
     P = 0 if pool_blocks is None else pool_blocks.shape[-1]
+    if int(mode) != MODE_REUSE:
+        _elem(scores, "scores", (4,), True)
+        for t, name in ((idx, "idx"), (kv_len, "kv_len"), (pool_blocks, "pool_blocks")):
+            _elem(t, name, (4,), False)
+        _room(idx, "idx", B * T * K)
+        _room(kv_len, "kv_len", B * T)
+        _room(pool_blocks, "pool_blocks", B * T * P)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.csa2_topk(int(mode), B, T, M, _ptr(scores), _ptr(kv_len), _ptr(pool_blocks), P, K, _ptr(idx),
                           _ptr(workspace), ws, _stream(stream)))
@@ -193,6 +265,15 @@ def csa2_index_topk(mode, q_idx, w, k_idx, kv_len, idx, pool_blocks=None, pool_o
     N = k_idx.shape[1]
     P = 0 if pool_blocks is None else pool_blocks.shape[-1]
     P_out = 0 if pool_out is None else pool_out.shape[-1]
+    if int(mode) != MODE_REUSE:
+        if q_idx.element_size() == 1 and k_idx.element_size() == 1:   # other dtypes: rejected by the call
+            _indexer_operands(q_idx, w, k_idx, kv_len, B, T, N)
+        for t, name in ((idx, "idx"), (pool_blocks, "pool_blocks"), (pool_out, "pool_out")):
+            _elem(t, name, (4,), False)
+        _flag(err_flag)
+        _room(idx, "idx", B * T * idx.shape[-1])
+        _room(pool_blocks, "pool_blocks", B * T * P)
+        _room(pool_out, "pool_out", B * T * P_out)
     _check(_lib.csa2_index_topk(int(mode), B, T, N, _ptr(q_idx), _dtype_code(q_idx), _ptr(w), _ptr(k_idx),
                                 _dtype_code(k_idx), _ptr(kv_len), _ptr(pool_blocks), P, idx.shape[-1], _ptr(idx),
                                 _ptr(pool_out), P_out, _ptr(err_flag), _stream(stream)))
@@ -212,6 +293,11 @@ def csa2_index_topk_dense(q_idx, w, k_idx, kv_len, idx, workspace=None, err_flag
     _cuda(q_idx, w, k_idx, kv_len, idx, workspace, err_flag)
     B, T = q_idx.shape[0], q_idx.shape[1]
     N, K = k_idx.shape[1], idx.shape[-1]
+    if q_idx.element_size() == 1 and k_idx.element_size() == 1:       # other dtypes: rejected by the call
+        _indexer_operands(q_idx, w, k_idx, kv_len, B, T, N)
+    _elem(idx, "idx", (4,), False)
+    _flag(err_flag)
+    _room(idx, "idx", B * T * K)
     if workspace is None:
         workspace = torch.empty(max(1, csa2_index_topk_dense_workspace_bytes(B, T, N, K)), dtype=torch.uint8,
                                 device=idx.device)
@@ -229,6 +315,19 @@ def csa2_swa_attn_fp8(q, swa_kv, swa_len, out, sm_scale, o_sparse=None, lse_spar
     _cuda(q, swa_kv, swa_len, out, o_sparse, lse_sparse, lse, err_flag)
     B, T, H, D = q.shape
     W = swa_kv.shape[1]
+    dv = out.shape[-1]
+    _elem(q, "q", (2,))
+    _elem(swa_kv, "swa_kv", (1,))
+    _elem(swa_len, "swa_len", (4,), False)
+    for t, name in ((out, "out"), (o_sparse, "o_sparse"), (lse_sparse, "lse_sparse"), (lse, "lse")):
+        _elem(t, name, (4,), True)
+    _flag(err_flag)
+    _room(swa_kv, "swa_kv", B * W * D)
+    _room(swa_len, "swa_len", B * T)
+    _room(out, "out", B * T * H * dv)
+    _room(o_sparse, "o_sparse", B * T * H * dv)
+    _room(lse_sparse, "lse_sparse", B * T * H)
+    _room(lse, "lse", B * T * H)
     _check(_lib.csa2_swa_attn_fp8(B, T, H, D, out.shape[-1], _ptr(q), _ptr(swa_kv), W, _ptr(swa_len),
                                   float(sm_scale), _ptr(o_sparse), _ptr(lse_sparse), _ptr(out), _ptr(lse),
                                   _ptr(err_flag), _stream(stream)))
@@ -236,6 +335,23 @@ def csa2_swa_attn_fp8(q, swa_kv, swa_len, out, sm_scale, o_sparse=None, lse_spar
 
 def csa2_sparse_attn_workspace_bytes(B, T, H, D, dv, K) -> int:
     return int(_lib.csa2_sparse_attn_workspace_bytes(B, T, H, D, dv, K))
+
+
+def _attn_args(q, codes, scales, N, idx, out, kv_len, lse, err_flag, B, T, H, D, dv, K):
+    _elem(q, "q", (2,))
+    _elem(codes, "codes", (1,))
+    _elem(scales, "scales", (1,))
+    _elem(idx, "idx", (4,), False)
+    _elem(kv_len, "kv_len", (4,), False)
+    _elem(out, "out", (4,), True)
+    _elem(lse, "lse", (4,), True)
+    _flag(err_flag)
+    _room(codes, "codes", B * int(N) * (D // 2))
+    _room(scales, "scales", B * int(N) * (D // 16))
+    _room(idx, "idx", B * T * K)
+    _room(kv_len, "kv_len", B * T)
+    _room(out, "out", B * T * H * dv)
+    _room(lse, "lse", B * T * H)
 
 
 def csa2_sparse_attn_fp4(mode, q, codes, scales, N, idx, out, sm_scale, kv_len=None, lse=None, err_flag=None,
@@ -246,6 +362,7 @@ def csa2_sparse_attn_fp4(mode, q, codes, scales, N, idx, out, sm_scale, kv_len=N
     B, T, H, D = q.shape
     dv = out.shape[-1]
     K = idx.shape[-1]
+    _attn_args(q, codes, scales, N, idx, out, kv_len, lse, err_flag, B, T, H, D, dv, K)
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.csa2_sparse_attn_fp4(int(mode), B, T, H, D, dv, _ptr(q), _ptr(codes), _ptr(scales), int(N),
                                      _ptr(idx), K, _ptr(kv_len), float(sm_scale), _ptr(out), FP32, _ptr(lse),
@@ -266,6 +383,7 @@ def csa2_sparse_attn_fp4_noalloc(mode, q, codes, scales, N, idx, out, sm_scale, 
     B, T, H, D = q.shape
     dv = out.shape[-1]
     K = idx.shape[-1]
+    _attn_args(q, codes, scales, N, idx, out, kv_len, lse, err_flag, B, T, H, D, dv, K)
     _check(_lib.csa2_sparse_attn_fp4_noalloc(int(mode), B, T, H, D, dv, _ptr(q), _ptr(codes), _ptr(scales), int(N),
                                              _ptr(idx), K, _ptr(kv_len), float(sm_scale), _ptr(out), FP32,
                                              _ptr(lse), _ptr(err_flag), _stream(stream)))
