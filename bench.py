@@ -688,7 +688,7 @@ def cpu_baseline(budget_s=15.0):
     """Time the oracle as it stands (single-threaded C, fp64) on a bounded
     sample of the workload: whole sequences through the 20-layer schedule."""
     import oracle as orc
-    from sparse_attention_fp4_quantize_gb300.decode import DECODER_SCHEDULE
+    from gen import DECODER_SCHEDULE
     orc.build()
     s1 = _oracle_sample(1)
     t = time.perf_counter()
@@ -742,7 +742,7 @@ def cpu_baseline_all_cores(per_seq_s, budget_s=10.0, workers=None):
     start).  Processes are spawned, never forked, so no CUDA state is shared."""
     import multiprocessing as mp
     import oracle as orc
-    from sparse_attention_fp4_quantize_gb300.decode import DECODER_SCHEDULE
+    from gen import DECODER_SCHEDULE
     orc.build()
     n = int(workers or os.cpu_count() or 1)
     n_seq = int(max(1, min(4, budget_s // max(per_seq_s, 1e-3))))
@@ -785,7 +785,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle as orc
-    from sparse_attention_fp4_quantize_gb300.decode import DECODER_SCHEDULE
+    from gen import DECODER_SCHEDULE
     orc.build()
     s1 = _oracle_sample(1)
     t = time.perf_counter()

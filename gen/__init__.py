@@ -173,6 +173,13 @@ APPEND_POOL = Workload("append_1m_rows_d576_pool_b16_n65536", 4, B=16, T=1, N=65
 
 WORKLOADS = [TINY_FULL_DECODE, FULL_BATCHED_DECODE, REINDEX_REUSE_1M, PREFILL_CHUNK, APPEND_POOL]
 
+# The decoder's layer schedule ("DeepSeek-V4.1-Flash：把 KV Cache 压缩到极限的百万上下文
+# MoE", CSA2 section): 20 layers in 5 groups of 4, the first group 1 Full + 3
+# Reuse, the other four 1 Reindex + 3 Reuse.  A constant of the workload, kept
+# here so that the oracle's timing leg can use it without loading the CUDA
+# library.
+DECODER_SCHEDULE = ("full", "reuse", "reuse", "reuse") + ("reindex", "reuse", "reuse", "reuse") * 4
+
 
 def scaled(w: Workload, **changes) -> Workload:
     """A smaller copy of a workload (same distributions) for oracle-sized tests."""

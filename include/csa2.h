@@ -327,7 +327,9 @@ csa2_status csa2_swa_attn_fp8(int B, int T, int H, int D, int dv, const void *q,
  * Arguments, layouts, results and errors are those of csa2_sparse_attn_fp4
  * (minus workspace/ws_bytes); the call allocates nothing.  A shape whose
  * scratch (csa2_sparse_attn_workspace_bytes) exceeds the array returns
- * CSA2_ERR_WORKSPACE with an explanation.  The first call on each device
+ * CSA2_ERR_WORKSPACE with an explanation.  The array's device addresses are
+ * kept in a table of 64 devices: a call on a device ordinal of 64 or more
+ * that needs scratch returns CSA2_ERR_UNSUPPORTED.  The first call on each device
  * looks up the array's device address with that device current; make that
  * first call before any stream capture.  All calls on a device share the
  * array and it keeps the previous call's contents (each call overwrites every

@@ -112,9 +112,13 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError("indexer tensors must be FP8 E4M3 (uint8/float8_e4m3fn) or bf16 (bfloat16/int16 bits)")
 
 
+def _on_device(t) -> bool:
+    return t.is_cuda
+
+
 def _cuda(*ts):
     for t in ts:
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+        if t is not None and (not _on_device(t) or not t.is_contiguous()):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
@@ -125,6 +129,14 @@ def _elem(t, name, sizes, floating=None):
         return
     if t.element_size() not in sizes or (floating is not None and t.is_floating_point() != floating):
         raise TypeError("%s: %s elements do not fit this call" % (name, t.dtype))
+
+
+def _bf16(t, name):
+    """The C call reads t as bf16 values: only torch.bfloat16 or its int16
+    bit patterns are accepted (a float16 tensor has the same element size
+    but other values)."""
+    if t is not None and t.dtype not in (torch.bfloat16, torch.int16):
+        raise TypeError("%s: %s elements are not bf16 (pass torch.bfloat16 or int16 bit patterns)" % (name, t.dtype))
 
 
 def _room(t, name, n):
@@ -161,7 +173,7 @@ def version() -> int:
 
 
 def _plane_args(kv, codes, scales, dst_slot, err_flag, R, D, n_slots):
-    _elem(kv, "kv", (2,))
+    _bf16(kv, "kv")
     _elem(codes, "codes", (1,))
     _elem(scales, "scales", (1,))
     _elem(dst_slot, "dst_slot", (8,), False)
@@ -176,7 +188,7 @@ def csa2_quantize_kv_fp4(kv, codes, scales, dst_slot=None, err_flag=None, stream
     """kv bf16 [R, D] (or int16 bits) -> codes uint8 [S, D/2], scales uint8 [S, D/16]."""
     _cuda(codes, scales, dst_slot, err_flag)
     R, D = kv.shape
-    if not kv.is_cuda or kv.stride(1) != 1:
+    if not _on_device(kv) or kv.stride(1) != 1:
         raise ValueError("kv must be a CUDA tensor with contiguous rows (any row stride)")
     n_slots = codes.shape[0]
     _plane_args(kv, codes, scales, dst_slot, err_flag, R, D, n_slots)
@@ -316,7 +328,7 @@ def csa2_swa_attn_fp8(q, swa_kv, swa_len, out, sm_scale, o_sparse=None, lse_spar
     B, T, H, D = q.shape
     W = swa_kv.shape[1]
     dv = out.shape[-1]
-    _elem(q, "q", (2,))
+    _bf16(q, "q")
     _elem(swa_kv, "swa_kv", (1,))
     _elem(swa_len, "swa_len", (4,), False)
     for t, name in ((out, "out"), (o_sparse, "o_sparse"), (lse_sparse, "lse_sparse"), (lse, "lse")):
@@ -338,7 +350,7 @@ def csa2_sparse_attn_workspace_bytes(B, T, H, D, dv, K) -> int:
 
 
 def _attn_args(q, codes, scales, N, idx, out, kv_len, lse, err_flag, B, T, H, D, dv, K):
-    _elem(q, "q", (2,))
+    _bf16(q, "q")
     _elem(codes, "codes", (1,))
     _elem(scales, "scales", (1,))
     _elem(idx, "idx", (4,), False)

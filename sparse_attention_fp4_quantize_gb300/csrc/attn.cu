@@ -605,7 +605,15 @@ extern "C" csa2_status csa2_sparse_attn_fp4_noalloc(csa2_mode mode, int B, int T
         return CSA2_ERR_WORKSPACE;
     }
     void *scratch = nullptr;
-    if (need > 0) CSA2_CUDA_CALL(noalloc_scratch(&scratch), "sparse_attn_noalloc: scratch address");
+    if (need > 0) {
+        int dev = 0;
+        CSA2_CUDA_CALL(cudaGetDevice(&dev), "sparse_attn_noalloc: current device");
+        if (dev < 0 || dev >= 64) {
+            set_error("sparse_attn_noalloc: device ordinal %d; the scratch address table covers devices 0-63", dev);
+            return CSA2_ERR_UNSUPPORTED;
+        }
+        CSA2_CUDA_CALL(noalloc_scratch(&scratch), "sparse_attn_noalloc: scratch address");
+    }
     // Every split rewrites all of its partial rows (empty splits write zeros
     // and lse = -inf), so nothing in the array needs clearing between calls.
     return csa2_sparse_attn_fp4(mode, B, T, H, D, dv, q, codes, scales, N, idx, K, kv_len, sm_scale, out, out_dt,

@@ -26,10 +26,10 @@ from dataclasses import dataclass
 
 import torch
 
+from gen import DECODER_SCHEDULE  # the schedule as a workload constant (no arithmetic)
+
 from . import (MODE_FULL, MODE_REINDEX, MODE_REUSE, csa2_build_pool, csa2_index_score, csa2_index_topk,
                csa2_quantize_kv_fp4, csa2_sparse_attn_fp4, csa2_topk, workspace_for_attn)
-
-DECODER_SCHEDULE = ("full", "reuse", "reuse", "reuse") + ("reindex", "reuse", "reuse", "reuse") * 4
 
 
 @dataclass

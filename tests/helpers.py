@@ -5,7 +5,11 @@ same inputs):
   * FP4 codes and scale bytes: bit-exact.
   * indexer scores: |s_gpu - s_ref| <= 1e-4 * max(|s_ref|, sum_h |w_h| sum_d |q_hd k_d|)
     (the magnitude sum is the dot product's conditioning; a score near 0 after
-    ReLU has no meaningful pure relative error).
+    ReLU has no meaningful pure relative error).  This widens the plain
+    "1e-4 relative" of the specification where q.k cancels; the plain relative
+    error |s_gpu - s_ref| / |s_ref| <= 1e-4 is also required of every score
+    whose magnitude sum is at most COND_MAX times the score (no heavy
+    cancellation), and its worst value is returned.
   * Top-K / pool sets: equal, except members whose oracle score lies within
     1e-5 relative of the oracle's K-th score (the tie band).
   * attention: per (b, t, h) row, max_c |o_gpu - o_ref| / max_c |o_ref| <= 2e-3.
@@ -15,6 +19,7 @@ from __future__ import annotations
 import numpy as np
 
 SCORE_RTOL = 1e-4
+COND_MAX = 10.0
 TIE_RTOL = 1e-5
 ATTN_RTOL = 2e-3
 
@@ -29,7 +34,11 @@ def check_scores(got, ref, mag, what="scores"):
     bad = err > tol
     assert not bad.any(), "%s: %d of %d outside tolerance, worst err/tol %.3g" % (
         what, int(bad.sum()), bad.size, float((err / np.maximum(tol, 1e-300)).max()))
-    return float((err / np.maximum(tol, 1e-300)).max()) if err.size else 0.0
+    r, m = np.abs(ref[fin]), mag[fin]
+    wc = (r > 0) & (m <= COND_MAX * r)          # well-conditioned scores: the plain relative error
+    plain = float((err[wc] / r[wc]).max()) if wc.any() else 0.0
+    assert plain <= SCORE_RTOL, "%s: plain relative error %.3g on well-conditioned scores" % (what, plain)
+    return plain
 
 
 def kth_score(ref_row, K):

@@ -26,9 +26,8 @@ class _FakeLib:
 def fake(monkeypatch):
     lib = _FakeLib()
     monkeypatch.setattr(csa2, "_lib", lib)
-    monkeypatch.setattr(csa2, "_cuda", lambda *ts: None)
+    monkeypatch.setattr(csa2, "_on_device", lambda t: True)   # the binding's own device check only
     monkeypatch.setattr(csa2, "_stream", lambda s: None)
-    monkeypatch.setattr(torch.Tensor, "is_cuda", property(lambda self: True))
     return lib
 
 
@@ -67,6 +66,15 @@ def test_wrong_element_sizes_are_refused(fake):
         csa2.csa2_sparse_attn_fp4(0, q, codes, scales, N, idx.long(), out, 0.1)
     with pytest.raises(TypeError):                                       # fp32 query
         csa2.csa2_sparse_attn_fp4(0, q.float(), codes, scales, N, idx, out, 0.1)
+    with pytest.raises(TypeError):                                       # fp16 query: bf16's size, other values
+        csa2.csa2_sparse_attn_fp4(0, q.half(), codes, scales, N, idx, out, 0.1)
+    with pytest.raises(TypeError):                                       # fp16 query in the window branch
+        csa2.csa2_swa_attn_fp8(q.half(), _z(B, 128, D, dtype=u8), _z(B * T, dtype=i32), out, 0.1)
+    with pytest.raises(TypeError):                                       # fp16 kv rows
+        csa2.csa2_quantize_kv_fp4(_z(5, D, dtype=torch.float16), _z(5, D // 2, dtype=u8), _z(5, D // 16, dtype=u8))
+    with pytest.raises(TypeError):                                       # fp16 kv rows before RoPE
+        csa2.csa2_rope_quantize_kv_fp4(_z(5, D, dtype=torch.float16), _z(5, dtype=i32), _z(8, 32, 2),
+                                       _z(5, D // 2, dtype=u8), _z(5, D // 16, dtype=u8))
     with pytest.raises(TypeError):                                       # int64 kv_len
         csa2.csa2_topk(0, _z(B, T, N), idx, kv_len=_z(B * T, dtype=torch.int64))
     with pytest.raises(TypeError):                                       # fp32 kv rows
