@@ -287,6 +287,30 @@ csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H, int D, int
 size_t csa2_sparse_attn_workspace_bytes(int B, int T, int H, int D, int dv, int K);
 
 /*
+ * csa2_sparse_attn_fp4_prefetch -- csa2_sparse_attn_fp4, plus an L2 prefetch
+ * hint for the layer that attends next with the same indices.  In a CSA2
+ * group the Reuse layers attend with their source layer's idx ([ENG] CSA2
+ * section; [HUNT] CSA2 paragraph), so while this layer's attention computes
+ * (its HBM traffic is over once its own rows have landed) the rows that idx
+ * selects in the next layer's planes can already travel to L2, and the next
+ * launch gathers them from there.
+ *
+ * Arguments, results and errors are those of csa2_sparse_attn_fp4, plus
+ * next_codes / next_scales: FP4 planes of the same shape and layout as
+ * codes / scales (codes 16-byte, scales 4-byte aligned), or both NULL (then
+ * this is exactly csa2_sparse_attn_fp4).  They are only read as a hint: no
+ * result depends on them, nothing waits for them, and they may be written
+ * afterwards.  The hint is issued on the D = 576, K <= 512 path only.
+ */
+csa2_status csa2_sparse_attn_fp4_prefetch(csa2_mode mode, int B, int T, int H, int D, int dv,
+                                          const void *q, const uint8_t *codes, const uint8_t *scales,
+                                          int64_t N, const int32_t *idx, int K, const int32_t *kv_len,
+                                          float sm_scale, void *out, csa2_dtype out_dt, float *lse,
+                                          uint32_t *err_flag, void *workspace, size_t ws_bytes,
+                                          const uint8_t *next_codes, const uint8_t *next_scales,
+                                          csa2_stream_t stream);
+
+/*
  * csa2_swa_attn_fp8 -- the sliding-window branch over an FP8 window KV,
  * merged with the sparse branch.  [ENG] "效率组件四件" item 4 (the SWA KV stays
  * FP8); [HUNT] (every layer also has a sliding window).  The pages give neither

@@ -62,6 +62,8 @@ def _load() -> ctypes.CDLL:
         "csa2_sparse_attn_fp4": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P, P,
                                   P, u64, P], i32),
         "csa2_sparse_attn_workspace_bytes": ([i32, i32, i32, i32, i32, i32], u64),
+        "csa2_sparse_attn_fp4_prefetch": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P, P,
+                                           P, u64, P, P, P], i32),
         "csa2_swa_attn_fp8": ([i32, i32, i32, i32, i32, P, P, i32, P, f32, P, P, P, P, P, P], i32),
         "csa2_sparse_attn_fp4_noalloc": ([i32, i32, i32, i32, i32, i32, P, P, P, i64, P, i32, P, f32, P, i32, P,
                                           P, P], i32),
@@ -84,7 +86,8 @@ _lib = _load()
 def exported_symbols():
     return ["csa2_quantize_kv_fp4", "csa2_rope_quantize_kv_fp4", "csa2_index_score", "csa2_build_pool", "csa2_build_pool_workspace_bytes",
             "csa2_topk", "csa2_topk_workspace_bytes", "csa2_index_topk", "csa2_index_topk_dense",
-            "csa2_index_topk_dense_workspace_bytes", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes", "csa2_swa_attn_fp8",
+            "csa2_index_topk_dense_workspace_bytes", "csa2_sparse_attn_fp4", "csa2_sparse_attn_workspace_bytes",
+            "csa2_sparse_attn_fp4_prefetch", "csa2_swa_attn_fp8",
             "csa2_sparse_attn_fp4_noalloc", "csa2_sparse_attn_noalloc_max_scratch_bytes",
             "csa2_selftest_bounded_wait", "csa2_status_string", "csa2_last_error", "csa2_version"]
 
@@ -379,6 +382,30 @@ def csa2_sparse_attn_fp4(mode, q, codes, scales, N, idx, out, sm_scale, kv_len=N
     _check(_lib.csa2_sparse_attn_fp4(int(mode), B, T, H, D, dv, _ptr(q), _ptr(codes), _ptr(scales), int(N),
                                      _ptr(idx), K, _ptr(kv_len), float(sm_scale), _ptr(out), FP32, _ptr(lse),
                                      _ptr(err_flag), _ptr(workspace), ws, _stream(stream)))
+
+
+def csa2_sparse_attn_fp4_prefetch(mode, q, codes, scales, N, idx, out, sm_scale, next_codes=None, next_scales=None,
+                                  kv_len=None, lse=None, err_flag=None, workspace=None, stream=None):
+    """csa2_sparse_attn_fp4 plus an L2 prefetch hint: the rows idx selects in
+    (next_codes, next_scales), the planes of the layer that attends next with
+    the same indices."""
+    _cuda(q, codes, scales, idx, out, kv_len, lse, err_flag, workspace, next_codes, next_scales)
+    B, T, H, D = q.shape
+    dv = out.shape[-1]
+    K = idx.shape[-1]
+    _attn_args(q, codes, scales, N, idx, out, kv_len, lse, err_flag, B, T, H, D, dv, K)
+    if (next_codes is None) != (next_scales is None):
+        raise ValueError("next_codes and next_scales go together")
+    if next_codes is not None:
+        _elem(next_codes, "next_codes", (1,))
+        _elem(next_scales, "next_scales", (1,))
+        _room(next_codes, "next_codes", B * int(N) * (D // 2))
+        _room(next_scales, "next_scales", B * int(N) * (D // 16))
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.csa2_sparse_attn_fp4_prefetch(int(mode), B, T, H, D, dv, _ptr(q), _ptr(codes), _ptr(scales), int(N),
+                                              _ptr(idx), K, _ptr(kv_len), float(sm_scale), _ptr(out), FP32,
+                                              _ptr(lse), _ptr(err_flag), _ptr(workspace), ws, _ptr(next_codes),
+                                              _ptr(next_scales), _stream(stream)))
 
 
 def workspace_for_attn(B, T, H, D, dv, K, device="cuda"):

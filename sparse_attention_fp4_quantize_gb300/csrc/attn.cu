@@ -495,13 +495,13 @@ extern "C" size_t csa2_sparse_attn_workspace_bytes(int B, int T, int H, int D, i
     return (size_t)splits * rows * ((size_t)dv + 1) * sizeof(float) + 256;
 }
 
-extern "C" csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H, int D, int dv,
-                                            const void *q, const uint8_t *codes, const uint8_t *scales,
-                                            int64_t N, const int32_t *idx, int K, const int32_t *kv_len,
-                                            float sm_scale, void *out, csa2_dtype out_dt, float *lse,
-                                            uint32_t *err_flag, void *workspace, size_t ws_bytes,
-                                            csa2_stream_t stream) {
-    clear_error();
+// The attention of csa2_sparse_attn_fp4, with an optional L2 prefetch of the
+// selected rows of a second pair of planes (pf_codes / pf_scales).
+static csa2_status sparse_attn_impl(csa2_mode mode, int B, int T, int H, int D, int dv, const void *q,
+                                    const uint8_t *codes, const uint8_t *scales, int64_t N, const int32_t *idx,
+                                    int K, const int32_t *kv_len, float sm_scale, void *out, csa2_dtype out_dt,
+                                    float *lse, uint32_t *err_flag, void *workspace, size_t ws_bytes,
+                                    const uint8_t *pf_codes, const uint8_t *pf_scales, csa2_stream_t stream) {
     CSA2_REQUIRE(mode == CSA2_MODE_FULL || mode == CSA2_MODE_REINDEX || mode == CSA2_MODE_REUSE,
                  "sparse_attn: bad mode %d", (int)mode);
     CSA2_REQUIRE(B >= 0 && T >= 0 && H >= 0 && N >= 0, "sparse_attn: negative shape");
@@ -519,7 +519,7 @@ extern "C" csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H,
 
     if (sparse_attn_tc_supported(D, dv, H, K))
         return launch_sparse_attn_tc(B, T, H, K, N, q, codes, scales, idx, kv_len, sm_scale, (float *)out, lse,
-                                     err_flag, stream_of(stream));
+                                     err_flag, pf_codes, pf_scales, stream_of(stream));
 
     AttnArgs a = {};
     a.B = B; a.T = T; a.H = H; a.K = K; a.N = N;
@@ -540,6 +540,33 @@ extern "C" csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H,
     }
     if (D == 576) return launch_attn<576, 512, 4>(a, stream_of(stream));
     return launch_attn<128, 64, 1>(a, stream_of(stream));
+}
+
+extern "C" csa2_status csa2_sparse_attn_fp4(csa2_mode mode, int B, int T, int H, int D, int dv,
+                                            const void *q, const uint8_t *codes, const uint8_t *scales,
+                                            int64_t N, const int32_t *idx, int K, const int32_t *kv_len,
+                                            float sm_scale, void *out, csa2_dtype out_dt, float *lse,
+                                            uint32_t *err_flag, void *workspace, size_t ws_bytes,
+                                            csa2_stream_t stream) {
+    clear_error();
+    return sparse_attn_impl(mode, B, T, H, D, dv, q, codes, scales, N, idx, K, kv_len, sm_scale, out, out_dt, lse,
+                            err_flag, workspace, ws_bytes, nullptr, nullptr, stream);
+}
+
+extern "C" csa2_status csa2_sparse_attn_fp4_prefetch(csa2_mode mode, int B, int T, int H, int D, int dv,
+                                                     const void *q, const uint8_t *codes, const uint8_t *scales,
+                                                     int64_t N, const int32_t *idx, int K, const int32_t *kv_len,
+                                                     float sm_scale, void *out, csa2_dtype out_dt, float *lse,
+                                                     uint32_t *err_flag, void *workspace, size_t ws_bytes,
+                                                     const uint8_t *next_codes, const uint8_t *next_scales,
+                                                     csa2_stream_t stream) {
+    clear_error();
+    CSA2_REQUIRE((next_codes == nullptr) == (next_scales == nullptr),
+                 "sparse_attn_prefetch: next_codes and next_scales go together");
+    CSA2_REQUIRE(aligned(next_codes, 16) && aligned(next_scales, 4),
+                 "sparse_attn_prefetch: next_codes needs 16-byte, next_scales 4-byte alignment");
+    return sparse_attn_impl(mode, B, T, H, D, dv, q, codes, scales, N, idx, K, kv_len, sm_scale, out, out_dt, lse,
+                            err_flag, workspace, ws_bytes, next_codes, next_scales, stream);
 }
 
 // ---------------------------------------------------------------------------

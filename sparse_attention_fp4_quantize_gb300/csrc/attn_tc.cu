@@ -111,6 +111,9 @@ struct TcArgs {
     const int32_t *swa_len;
     const float *o_sparse;
     const float *lse_sparse;
+    // optional L2 prefetch: the same selected rows of another pair of FP4 planes
+    const uint8_t *pf_codes;
+    const uint8_t *pf_scales;
 };
 
 // 16 E4M3 bytes -> 16 f16 (exact), as 8 f16x2 words.
@@ -173,6 +176,12 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_remote, uint32_t src_local
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// L2 prefetch hints (no data is returned; nothing waits on them).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // FP8W = false: the sparse branch (FP4 entries gathered by idx).  FP8W = true:
@@ -400,6 +409,18 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     }
     ok = tc::mbar_wait(bar_s, 0, MAX_POLLS) && ok;
     tc::fence_after();
+    // This CTA's own rows have landed and HBM is idle for the rest of the launch:
+    // hint the same selected rows of the next planes (the layer that attends next
+    // with these indices) into L2, so that its launch gathers them from L2.
+    if constexpr (!FP8W) {
+        if (a.pf_codes && issuer && valid) {
+            const int64_t row = b * a.N + j;
+            bulk_prefetch_l2(a.pf_codes + row * (D / 2), D / 2);
+            const uint8_t *srow = a.pf_scales + row * (D / 16);
+            prefetch_l2(srow);
+            prefetch_l2(srow + D / 16 - 1);   // the 36 bytes may straddle two lines
+        }
+    }
 
     // ---- 4a. S^T -> shared memory, transposed to [head][entry] (the Q tile is free now)
     const int quarter = warp & 3, hh = warp >> 2;   // TMEM lane quarter, 16-column group
@@ -723,8 +744,10 @@ static csa2_status launch_tc(TcArgs &a, int B, int entries, cudaStream_t stream)
 
 csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const void *q, const uint8_t *codes,
                                   const uint8_t *scales, const int32_t *idx, const int32_t *kv_len, float sm_scale,
-                                  float *out, float *lse, uint32_t *err_flag, cudaStream_t stream) {
+                                  float *out, float *lse, uint32_t *err_flag, const uint8_t *pf_codes,
+                                  const uint8_t *pf_scales, cudaStream_t stream) {
     TcArgs a = {};
+    a.pf_codes = pf_codes; a.pf_scales = pf_scales;
     a.T = T; a.H = H; a.K = K; a.N = N;
     a.q = (const uint16_t *)q; a.codes = codes; a.scales = scales; a.idx = idx; a.kv_len = kv_len;
     a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.err_flag = err_flag;

@@ -62,9 +62,11 @@ static inline cudaStream_t stream_of(csa2_stream_t s) { return (cudaStream_t)s; 
 
 // tcgen05 sparse attention (attn_tc.cu): D = 576, dv = 512, 64-head blocks, K <= 1024.
 bool sparse_attn_tc_supported(int D, int dv, int H, int K);
+// pf_codes / pf_scales: optional planes whose selected rows are prefetched into L2 (may be NULL).
 csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const void *q, const uint8_t *codes,
                                   const uint8_t *scales, const int32_t *idx, const int32_t *kv_len, float sm_scale,
-                                  float *out, float *lse, uint32_t *err_flag, cudaStream_t stream);
+                                  float *out, float *lse, uint32_t *err_flag, const uint8_t *pf_codes,
+                                  const uint8_t *pf_scales, cudaStream_t stream);
 csa2_status launch_swa_attn_tc(int B, int T, int H, const void *q, const uint8_t *kv8, int W, const int32_t *swa_len,
                                float sm_scale, const float *o_sparse, const float *lse_sparse, float *out, float *lse,
                                uint32_t *err_flag, cudaStream_t stream);

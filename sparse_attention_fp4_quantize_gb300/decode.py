@@ -29,7 +29,8 @@ import torch
 from gen import DECODER_SCHEDULE  # the schedule as a workload constant (no arithmetic)
 
 from . import (MODE_FULL, MODE_REINDEX, MODE_REUSE, csa2_build_pool, csa2_index_score, csa2_index_topk,
-               csa2_quantize_kv_fp4, csa2_sparse_attn_fp4, csa2_topk, workspace_for_attn)
+               csa2_quantize_kv_fp4, csa2_sparse_attn_fp4, csa2_sparse_attn_fp4_prefetch, csa2_topk,
+               workspace_for_attn)
 
 
 @dataclass
@@ -44,6 +45,7 @@ class StepShape:
     idx_fp8: bool = True
     kv_per_layer: bool = True        # each layer attends over its own FP4 KV
     fused_indexer: bool = True       # FP8 only: csa2_index_topk instead of score + pool + topk
+    prefetch_next: bool = True       # a layer followed by a Reuse layer hints that layer's selected rows into L2
     schedule: tuple = DECODER_SCHEDULE
 
 
@@ -110,6 +112,7 @@ class DecoderStep:
                              stream=stream)
         gi = -1
         fused = s.fused_indexer and s.idx_fp8
+        L = len(s.schedule)
         for layer, mode in enumerate(s.schedule):
             if mode != "reuse" and fused:
                 gi += 1
@@ -136,9 +139,18 @@ class DecoderStep:
                 csa2_topk(MODE_REUSE, self.scores, self.idx[gi], stream=stream)
             codes, scales = self.kv_planes(layer)
             mode_id = {"full": MODE_FULL, "reindex": MODE_REINDEX, "reuse": MODE_REUSE}[mode]
-            csa2_sparse_attn_fp4(mode_id, x["q"][layer], codes, scales, s.N, self.idx[gi], self.out[layer],
-                                 self.sm_scale, kv_len=self.kv_len, lse=self.lse[layer], err_flag=self.err,
-                                 workspace=self.ws, stream=stream)
+            nxt = layer + 1
+            if s.prefetch_next and s.kv_per_layer and nxt < L and s.schedule[nxt] == "reuse":
+                # the next layer attends with this group's idx over its own planes
+                nc, ns = self.kv_planes(nxt)
+                csa2_sparse_attn_fp4_prefetch(mode_id, x["q"][layer], codes, scales, s.N, self.idx[gi],
+                                              self.out[layer], self.sm_scale, next_codes=nc, next_scales=ns,
+                                              kv_len=self.kv_len, lse=self.lse[layer], err_flag=self.err,
+                                              workspace=self.ws, stream=stream)
+            else:
+                csa2_sparse_attn_fp4(mode_id, x["q"][layer], codes, scales, s.N, self.idx[gi], self.out[layer],
+                                     self.sm_scale, kv_len=self.kv_len, lse=self.lse[layer], err_flag=self.err,
+                                     workspace=self.ws, stream=stream)
 
     def launches_per_step(self) -> int:
         """Kernel launches of one step (Reuse-mode scoring/selection launch nothing)."""
@@ -146,6 +158,7 @@ class DecoderStep:
         split = self.ws is not None
         n = 1                                              # quantise
         fused = s.fused_indexer and s.idx_fp8
+        L = len(s.schedule)
         for layer, mode in enumerate(s.schedule):
             if mode != "reuse" and fused:
                 n += 1                                     # fused score + (pool) + topk

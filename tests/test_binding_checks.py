@@ -110,6 +110,22 @@ def test_buffers_smaller_than_the_call_touches_are_refused(fake):
     assert fake.calls == []
 
 
+def test_prefetch_planes_are_checked(fake):
+    B, T, N, H, D, dv, K = 2, 1, 100, 64, 576, 512, 16
+    i32, u8, i16 = torch.int32, torch.uint8, torch.int16
+    q, idx, out = _z(B, T, H, D, dtype=i16), _z(B, T, K, dtype=i32), _z(B, T, H, dv)
+    codes, scales = _z(B * N, D // 2, dtype=u8), _z(B * N, D // 16, dtype=u8)
+    with pytest.raises(ValueError):                                      # next codes without next scales
+        csa2.csa2_sparse_attn_fp4_prefetch(0, q, codes, scales, N, idx, out, 0.1, next_codes=codes)
+    with pytest.raises(ValueError):                                      # next planes of one sequence for two
+        csa2.csa2_sparse_attn_fp4_prefetch(0, q, codes, scales, N, idx, out, 0.1, next_codes=codes[:N],
+                                           next_scales=scales[:N])
+    assert fake.calls == []
+    csa2.csa2_sparse_attn_fp4_prefetch(0, q, codes, scales, N, idx, out, 0.1, next_codes=codes, next_scales=scales)
+    csa2.csa2_sparse_attn_fp4_prefetch(0, q, codes, scales, N, idx, out, 0.1)
+    assert fake.calls == ["csa2_sparse_attn_fp4_prefetch"] * 2
+
+
 def test_reuse_calls_and_rejected_dtypes_pass_through_to_the_library(fake):
     # Reuse mode does no work, so its buffers are not checked; bf16 indexer tensors on the FP8-only
     # fused calls are the library's to reject (it returns a status)

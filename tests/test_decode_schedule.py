@@ -13,7 +13,8 @@ import sparse_attention_fp4_quantize_gb300 as csa2
 import sparse_attention_fp4_quantize_gb300.decode as dec
 
 CALLS = ["csa2_quantize_kv_fp4", "csa2_index_topk", "csa2_index_score", "csa2_build_pool", "csa2_topk",
-         "csa2_sparse_attn_fp4"]
+         "csa2_sparse_attn_fp4", "csa2_sparse_attn_fp4_prefetch"]
+ATTN = ("csa2_sparse_attn_fp4", "csa2_sparse_attn_fp4_prefetch")
 
 
 def test_schedule_is_the_pages_grouping():
@@ -43,7 +44,7 @@ def test_one_step_issues_the_calls_in_model_order(monkeypatch, fused):
     st = dec.DecoderStep(dec.StepShape(B=2, N=64, fused_indexer=fused), device="cpu")
     st.run()
     assert calls[0][0] == "csa2_quantize_kv_fp4"
-    attn = [c for c in calls if c[0] == "csa2_sparse_attn_fp4"]
+    attn = [c for c in calls if c[0] in ATTN]
     assert [c[1][0] for c in attn] == [{"full": csa2.MODE_FULL, "reindex": csa2.MODE_REINDEX,
                                          "reuse": csa2.MODE_REUSE}[m] for m in dec.DECODER_SCHEDULE]
     # every layer attends over its own KV planes; Reuse layers use their group's indices
@@ -53,9 +54,16 @@ def test_one_step_issues_the_calls_in_model_order(monkeypatch, fused):
     for layer in range(20):
         assert idx_ptrs[layer] == idx_ptrs[layer - layer % 4]
     assert len(set(idx_ptrs)) == 5
+    # a layer followed by a Reuse layer hints that layer's planes into L2; the group's last does not
+    for layer in range(20):
+        nxt_reuse = layer + 1 < 20 and dec.DECODER_SCHEDULE[layer + 1] == "reuse"
+        assert attn[layer][0] == ("csa2_sparse_attn_fp4_prefetch" if nxt_reuse else "csa2_sparse_attn_fp4")
+        if nxt_reuse:
+            assert attn[layer][2]["next_codes"].data_ptr() == code_ptrs[layer + 1]
+            assert attn[layer][2]["next_scales"].data_ptr() == attn[layer + 1][1][3].data_ptr()
     # each group's indexer runs before the group's first attention and after the previous layer's
     order = [c[0] for c in calls]
-    first_attn = [i for i, c in enumerate(calls) if c[0] == "csa2_sparse_attn_fp4"]
+    first_attn = [i for i, c in enumerate(calls) if c[0] in ATTN]
     sel = "csa2_index_topk" if fused else "csa2_topk"
     for g in range(5):
         i_attn = first_attn[4 * g]

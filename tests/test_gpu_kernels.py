@@ -431,3 +431,37 @@ def test_bounded_wait_times_out_and_the_context_stays_usable():
     torch.cuda.synchronize()
     want_c, want_s = oracle.quantize_kv_fp4(gen.as_numpy(rows).reshape(64, 128))
     assert (codes.cpu().numpy() == want_c).all() and (scales.cpu().numpy() == want_s).all()
+
+
+@pytest.mark.parametrize("B,N,K,H", [(4, 16384, 512, 64), (3, 3000, 300, 128), (2, 5000, 1024, 64)])
+def test_sparse_attn_prefetch_variant_is_the_same_attention(csa2, B, N, K, H):
+    """csa2_sparse_attn_fp4_prefetch only adds an L2 hint for another pair of
+    planes: its output and lse are bitwise those of csa2_sparse_attn_fp4, the
+    hinted planes are left untouched, and on the split-KV path (K > 512) the
+    hint is simply not issued."""
+    w = gen.scaled(gen.FULL_BATCHED_DECODE, B=B, N=N, K=K, H=H)
+    kv_len = gen.kv_lengths(w).clamp(max=N)
+    codes, scales = gen.fp4_planes(5, 1, B * N, 576, device=DEV)
+    nc, ns = gen.fp4_planes(5, 2, B * N, 576, device=DEV)
+    nc0, ns0 = nc.clone(), ns.clone()
+    idx = gen.random_indices(w, kv_len, frac_pad=0.05).to(DEV)
+    q = gen.normal_bf16(5, 3, (B, 1, H, 576), device=DEV)
+    kl = kv_len.to(DEV)
+    ws = csa2.workspace_for_attn(B, 1, H, 576, 512, K, device=DEV)
+    outs = []
+    for pf in (False, True):
+        out = torch.full((B, 1, H, 512), 7.0, device=DEV)
+        lse = torch.full((B, 1, H), 7.0, device=DEV)
+        flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+        if pf:
+            csa2.csa2_sparse_attn_fp4_prefetch(csa2.MODE_REUSE, q, codes, scales, N, idx, out, 1 / 24.0,
+                                               next_codes=nc, next_scales=ns, kv_len=kl, lse=lse, err_flag=flag,
+                                               workspace=ws)
+        else:
+            csa2.csa2_sparse_attn_fp4(csa2.MODE_REUSE, q, codes, scales, N, idx, out, 1 / 24.0, kv_len=kl, lse=lse,
+                                      err_flag=flag, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(flag.item()) == 0
+        outs.append((out, lse))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(nc, nc0) and torch.equal(ns, ns0)
