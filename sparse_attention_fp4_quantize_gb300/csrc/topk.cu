@@ -497,7 +497,16 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
     const int nm4 = (nm + 3) >> 2;
 
     // ---------------------------------------------------------------- pool (Full, optional)
-    if (a.pool_out) {
+    if (a.pool_out && (len + 7) / 8 <= a.P_out) {
+        // every block with a valid position is in the pool: this CTA's blocks [beg/8, beg/8 + nb)
+        // go to the same slots (the slices are contiguous and 8-aligned), the last CTA pads
+        const int nb = (nm + 7) / 8;
+        const int64_t b0 = beg / 8, nbt = (len + 7) / 8;
+        int32_t *prow = a.pool_out + row * (int64_t)a.P_out;
+        for (int ib = tid; ib < nb; ib += kThreads) prow[b0 + ib] = (int32_t)(b0 + ib);
+        if (cta == C - 1)
+            for (int64_t s2 = nbt + tid; s2 < a.P_out; s2 += kThreads) prow[s2] = -1;
+    } else if (a.pool_out) {
         const int nb = (nm + 7) / 8, nb4 = (nb + 3) >> 2;
         for (int ib = tid; ib < 4 * nb4; ib += kThreads) {
             uint32_t m = 0u;
@@ -519,14 +528,15 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
     }
 
     // ---------------------------------------------------------------- Top-K
+    auto global_id = [&](int64_t li) -> int32_t {   // candidate li of the row -> entry position
+        if (full) return (int32_t)li;
+        return (int32_t)((int64_t)__ldg(a.pool_in + row * a.P + li / 8) * 8 + (li & 7));
+    };
     uint32_t T, kk;
     cluster_select<C>(cluster, cta, sm, keys, nm4, full ? len : a.M, a.K, T, kk);
     pdl_launch_dependents();
-    cluster_compact<C>(cluster, cta, sm, keys, nm, T, kk, a.K, a.idx + row * (int64_t)a.K, [&](int i) {
-        const int64_t li = beg + i;
-        if (full) return (int32_t)li;
-        return (int32_t)((int64_t)__ldg(a.pool_in + row * a.P + li / 8) * 8 + (li & 7));
-    });
+    cluster_compact<C>(cluster, cta, sm, keys, nm, T, kk, a.K, a.idx + row * (int64_t)a.K,
+                       [&](int i) { return global_id(beg + i); });
 }
 
 // Keys per CTA and dynamic shared memory for a split of the rows over C CTAs.
