@@ -701,6 +701,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         }
         if (rank == 0 && a.lse && tid < HB) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
     }
+    tc::fence_before();   // every warp's TMEM loads are done before the columns are freed
+    __syncthreads();
     tc::fence_after();
     if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
