@@ -34,6 +34,7 @@
 // Waits on the mbarriers are bounded; on timeout the kernel sets
 // CSA2_FLAG_TIMEOUT and still runs every cluster barrier, so it always ends.
 #include <cooperative_groups.h>
+#include <type_traits>
 
 #include "common.cuh"
 #include "tc.cuh"
@@ -707,6 +708,372 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
+
+// ---------------------------------------------------------------------------
+// Many query tokens: one CTA per (token, 64 heads) over all of its K <= 512
+// selected entries, in two passes and with no cluster merge (used when a
+// launch has enough (token, head-block) items to fill the GPU on its own,
+// e.g. a prefill chunk).  512 threads; the same 128-entry tile and MMA shapes
+// as above.
+//  Pass 1, per 128-entry tile t: the code rows by TMA bulk copies, all 576
+//   channels dequantised into the Khat tile, S^T_t = Khat . Q^T into TMEM
+//   columns [64 t, 64 t + 64); once those MMAs have released the tile the next
+//   tile's rows are copied in, while the per-head maxima of tile t are taken
+//   straight from TMEM (a butterfly over the 32 lanes of each warp).
+//  Pass 2, per tile: the rows again (now from L2; the next tile's land in the
+//   dead Q region meanwhile), the value channels into the Khat tile,
+//   P_t = exp2(z - M) from TMEM into an f16 tile laid out MN-major, and
+//   O^T += Vhat_t^T . P_t^T into TMEM columns [256, 512).
+//  Finally out = O / L and lse = (M + log2 L) ln 2 per head, L summed over the
+//  f16-rounded P as the MMAs consumed it.
+constexpr uint32_t TK_OFF_K = 0;
+constexpr uint32_t TK_OFF_Q = KT_BYTES;                        // Q tile (pass 1)
+constexpr uint32_t TK_OFF_STAGE2 = TK_OFF_Q;                   // pass 2: code rows of the next tile
+constexpr uint32_t TK_P_SBO = (TM / 8) * 128;                  // MN-major P: 2048 bytes per 8-head group
+constexpr uint32_t TK_P_BYTES = (HB / 8) * TK_P_SBO;           // 16384
+constexpr uint32_t TK_OFF_P = TK_OFF_Q + Q_BYTES - TK_P_BYTES; // pass 2: P tile
+constexpr uint32_t TK_OFF_BAR = TK_OFF_Q + Q_BYTES;            // mbarriers: Q rows, code rows, S, P V
+constexpr uint32_t TK_OFF_TMEM = TK_OFF_BAR + 32;
+constexpr uint32_t TK_OFF_ROW = TK_OFF_TMEM + 16;              // int64[512] KV row of each selected entry, -1 if none
+constexpr uint32_t TK_OFF_QMAX = TK_OFF_ROW + MAX_S * TM * 8;  // uint[64] per-head max |q| (bits)
+constexpr uint32_t TK_OFF_CS = TK_OFF_QMAX + HB * 4;           // float[64] logit factor per head
+constexpr uint32_t TK_OFF_PART = TK_OFF_CS + HB * 4;           // float[4][64] per lane quarter
+constexpr uint32_t TK_OFF_M = TK_OFF_PART + 4 * HB * 4;        // float[64] row max (log2 domain)
+constexpr uint32_t TK_OFF_L = TK_OFF_M + HB * 4;               // float[64] row sum
+constexpr uint32_t TK_SMEM = TK_OFF_L + HB * 4;
+constexpr uint32_t TK_S_COL = 0, TK_O_COL = MAX_S * HB;        // S^T tiles: 4 x 64 columns; O^T: 4 x 64
+static_assert(TM * CRAW_STRIDE <= Q_BYTES - TK_P_BYTES, "pass-2 staging must fit below the P tile");
+static_assert(TK_O_COL + (DV / 128) * HB <= TMEM_COLS, "TMEM columns");
+static_assert(TK_SMEM <= 227 * 1024, "shared memory");
+
+// Reduce-scatter of 16 values over the 32 lanes of a warp: afterwards lanes l
+// and l ^ 1 both hold the reduction over all lanes of value (l >> 1) & 15.
+template <bool MAX>
+__device__ __forceinline__ float lane_reduce16(float (&v)[16], int lane) {
+    auto op = [](float x, float y) { return MAX ? fmaxf(x, y) : x + y; };
+    auto step = [&](auto half_c, int d) {
+        constexpr int half = decltype(half_c)::value;
+        const bool up = (lane & d) != 0;
+#pragma unroll
+        for (int j = 0; j < half; ++j) {
+            const float send = up ? v[j] : v[j + half];
+            const float keep = up ? v[j + half] : v[j];
+            v[j] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, send, d));
+        }
+    };
+    step(std::integral_constant<int, 8>{}, 16);
+    step(std::integral_constant<int, 4>{}, 8);
+    step(std::integral_constant<int, 2>{}, 4);
+    step(std::integral_constant<int, 1>{}, 2);
+    return op(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 1));
+}
+
+__global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t bt = blockIdx.x / a.hblocks;
+    const int hblk = (int)(blockIdx.x - bt * a.hblocks);
+    const int64_t b = bt / a.T;
+    const int h0 = hblk * HB;
+    const int ntiles = (a.K + TM - 1) / TM;
+
+    uint8_t *sK = smem + TK_OFF_K;
+    uint8_t *sQ = smem + TK_OFF_Q;
+    uint8_t *sP = smem + TK_OFF_P;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + TK_OFF_TMEM);
+    int64_t *sRow = reinterpret_cast<int64_t *>(smem + TK_OFF_ROW);
+    uint32_t *sQmax = reinterpret_cast<uint32_t *>(smem + TK_OFF_QMAX);
+    float *sCs = reinterpret_cast<float *>(smem + TK_OFF_CS);
+    float *sPart = reinterpret_cast<float *>(smem + TK_OFF_PART);
+    float *sM = reinterpret_cast<float *>(smem + TK_OFF_M);
+    float *sL = reinterpret_cast<float *>(smem + TK_OFF_L);
+    const uint32_t bar_q = tc::smem_u32(smem + TK_OFF_BAR);   // Q rows landed
+    const uint32_t bar_ld = bar_q + 8;                          // a tile's code rows landed (one phase per tile and pass)
+    const uint32_t bar_s = bar_q + 16;                          // S MMAs of a tile done
+    const uint32_t bar_o = bar_q + 24;                          // P V MMAs of a tile done
+
+    const int e = tid & (TM - 1), qt = tid >> 7;   // entry of this thread in a tile, channel quarter
+    const bool issuer = qt == ((e >> 3) & 3);        // one thread per entry, spread over all 16 warps
+    const int quarter = warp & 3, hh = warp >> 2;    // TMEM lane quarter, 16-column group
+
+    if (tid == 0) {
+        tc::mbar_init(bar_q, HB);    // one arrival per head row
+        tc::mbar_init(bar_ld, TM);   // one arrival per entry of a tile
+        tc::mbar_init(bar_s, 1);
+        tc::mbar_init(bar_o, 1);
+        tc::mbar_init_fence();
+    }
+    if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
+    if (tid < HB) {
+        sQmax[tid] = 0u;
+        sM[tid] = -INFINITY;
+        sL[tid] = 0.f;
+    }
+    __syncthreads();
+    pdl_wait();   // the set-up above overlaps the previous kernel's tail
+
+    // the Q rows (no index needed) first, then every selected entry's row
+    if (issuer && e < HB) {
+        mbar_arrive_expect_tx(bar_q, D * 2);
+        bulk_g2s(tc::smem_u32(smem + OFF_QRAW + e * QRAW_STRIDE), a.q + ((bt * a.H) + h0 + e) * (int64_t)D, D * 2,
+                 bar_q);
+    }
+    {
+        int64_t len = a.kv_len ? (int64_t)a.kv_len[bt] : a.N;
+        len = len < a.N ? len : a.N;
+        for (int i = tid; i < ntiles * TM; i += THREADS) {
+            const int64_t j = (i < a.K) ? (int64_t)__ldg(a.idx + bt * a.K + i) : -1;
+            const bool v = j >= 0 && j < len;
+            if (!v && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
+            sRow[i] = v ? b * a.N + j : -1;
+        }
+    }
+    __syncthreads();
+    auto issue_codes = [&](int t, uint32_t stage) {   // the issuers: one row each, on bar_ld
+        if (issuer) {
+            const int64_t r = sRow[t * TM + e];
+            mbar_arrive_expect_tx(bar_ld, r >= 0 ? D / 2 : 0);
+            if (r >= 0) bulk_g2s(stage + e * CRAW_STRIDE, a.codes + r * (D / 2), D / 2, bar_ld);
+        }
+    };
+    auto load_scales = [&](int t, uint32_t (&sw)[9]) {   // the entry's 36 scale bytes as 9 words
+        const int64_t r = sRow[t * TM + e];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) sw[i] = 0u;
+        if (r >= 0) {
+            const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + r * (D / 16));
+#pragma unroll
+            for (int i = 0; i < 9; ++i) sw[i] = __ldg(srow + i);
+        }
+    };
+    const uint32_t stage1 = tc::smem_u32(smem + OFF_CRAW), stage2 = tc::smem_u32(smem + TK_OFF_STAGE2);
+    issue_codes(0, stage1);
+    uint32_t sw[9];
+    load_scales(0, sw);
+
+    // ---- Q -> registers -> per-head power-of-two scale -> f16 core-matrix tile (as the cluster kernel)
+    bool ok = tc::mbar_wait(bar_q, 0, MAX_POLLS);
+    {
+        const int hq = 8 * (warp & 7) + (lane & 7), cpos = lane >> 3, c0 = 36 * (warp >> 3);
+        const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE + (c0 + cpos) * 16;
+        uint4 qv[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + i * 64);
+        float mx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 9; ++i) {
+            const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+        if (cpos == 0) atomicMax(sQmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
+        __syncthreads();
+        mx = __uint_as_float(sQmax[hq]);
+        const int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
+        int sh = 14 - e2;   // max |q| * 2^sh in [2^14, 2^15)
+        sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
+        const float up = ldexpf(1.0f, sh);
+        uint8_t *qdst = sQ + (hq >> 3) * Q_SBO + (hq & 7) * 16 + (c0 + cpos) * 128;
+#pragma unroll
+        for (int i = 0; i < 9; ++i) {
+            const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
+            *reinterpret_cast<uint4 *>(qdst + i * 512) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
+    }
+
+    // staged codes of entry e -> registers: in half h the groups 18 h + qh + 4 i with qh = (qt + 2 h) mod 4
+    uint2 cw[2][5];
+    auto read_codes = [&](uint32_t stage_off, bool valid) {
+        const uint8_t *craw = smem + stage_off + e * CRAW_STRIDE;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int qh = (qt + 2 * h) & 3, nh = qh < 2 ? 5 : 4;
+#pragma unroll
+            for (int i = 0; i < 5; ++i)
+                cw[h][i] = (valid && i < nh) ? *reinterpret_cast<const uint2 *>(craw + 8 * (18 * h + qh + 4 * i))
+                                              : make_uint2(0, 0);
+        }
+    };
+    // dequantise half h of this thread's groups into the Khat tile (values_only: the 32 value groups)
+    auto dequant_half = [&](const int h, bool valid, bool values_only) {
+        const int qh = (qt + 2 * h) & 3, nh = qh < 2 ? 5 : 4;
+        uint8_t *kbase = sK + (e >> 3) * KT_SBO + (e & 7) * 16;
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            const int g = 18 * h + qh + 4 * i;   // group of the entry
+            if (i < nh && (!values_only || g < DV / 16)) {
+                const uint32_t word = h == 0 ? sw[i] : ((qh >> 1) ? sw[i < 4 ? 5 + i : 8] : sw[4 + i]);
+                const int byte = h == 0 ? qh : ((2 + qh) & 3);
+                uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                if (valid) {
+                    const uint32_t sc = e4m3_to_f16x2_bcast((word >> (8 * byte)) & 0xFFu);
+#pragma unroll
+                    for (int bb = 0; bb < 4; ++bb) {
+                        r[bb] = hmul2(e2m1x2_to_f16x2((cw[h][i].x >> (8 * bb)) & 0xFF), sc);
+                        r[4 + bb] = hmul2(e2m1x2_to_f16x2((cw[h][i].y >> (8 * bb)) & 0xFF), sc);
+                    }
+                }
+                *reinterpret_cast<uint4 *>(kbase + (2 * g) * 128) = make_uint4(r[0], r[1], r[2], r[3]);
+                *reinterpret_cast<uint4 *>(kbase + (2 * g + 1) * 128) = make_uint4(r[4], r[5], r[6], r[7]);
+            }
+        }
+    };
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t a0s = tc::smem_u32(sK), b0s = tc::smem_u32(sQ);
+    constexpr uint32_t idesc_s = tc::idesc_f16_f32(TM, HB, false, false);
+    uint32_t ld_phase = 0;
+
+    // ---- pass 1: S^T of every tile, per-head maxima
+    for (int t = 0; t < ntiles; ++t) {
+        ok = tc::mbar_wait(bar_ld, ld_phase & 1, MAX_POLLS) && ok;
+        ++ld_phase;
+        const bool valid = sRow[t * TM + e] >= 0;
+        read_codes(OFF_CRAW, valid);
+        __syncthreads();   // staging and Q-staging reads done: the Khat tile may overwrite them
+        dequant_half(0, valid, false);
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        if (tid == 0)
+            for (int ks = 0; ks < D / 32; ++ks)
+                tc::mma_f16(tmem + TK_S_COL + HB * t, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
+                            tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, ks > 0);
+        dequant_half(1, valid, false);
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        if (tid == 0) {
+            for (int ks = D / 32; ks < D / 16; ++ks)
+                tc::mma_f16(tmem + TK_S_COL + HB * t, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
+                            tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, true);
+            tc::commit(bar_s);
+        }
+        if (t + 1 < ntiles) load_scales(t + 1, sw);
+        ok = tc::mbar_wait(bar_s, t & 1, MAX_POLLS) && ok;
+        tc::fence_after();
+        if (t + 1 < ntiles) issue_codes(t + 1, stage1);   // the MMAs have released the Khat tile
+        // per-head maximum of this tile's logits
+        uint32_t r[16];
+        tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + TK_S_COL + HB * t + 16 * hh, r);
+        tc::tmem_ld_wait();
+        const bool v = ok && sRow[t * TM + 32 * quarter + lane] >= 0;
+        float z[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) z[jj] = v ? __uint_as_float(r[jj]) * sCs[16 * hh + jj] : -INFINITY;
+        const float m = lane_reduce16<true>(z, lane);
+        if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = m;
+        __syncthreads();
+        if (tid < HB)
+            sM[tid] = fmaxf(fmaxf(sM[tid], fmaxf(sPart[tid], sPart[HB + tid])),
+                            fmaxf(sPart[2 * HB + tid], sPart[3 * HB + tid]));
+    }
+
+    // ---- pass 2: P V of every tile
+    load_scales(0, sw);
+    issue_codes(0, stage2);   // the Q tile is dead: its region stages the rows
+    const uint32_t p0 = tc::smem_u32(sP);
+    constexpr uint32_t idesc_o = tc::idesc_f16_f32(TM, HB, true, true);
+    for (int t = 0; t < ntiles; ++t) {
+        ok = tc::mbar_wait(bar_ld, ld_phase & 1, MAX_POLLS) && ok;
+        ++ld_phase;
+        const bool valid = sRow[t * TM + e] >= 0;
+        read_codes(TK_OFF_STAGE2, valid);
+        if (t > 0) ok = tc::mbar_wait(bar_o, (t - 1) & 1, MAX_POLLS) && ok;   // the previous P V released the tiles
+        tc::fence_after();
+        __syncthreads();   // staging reads done; sM (after pass 1) visible
+        if (t + 1 < ntiles) issue_codes(t + 1, stage2);
+        dequant_half(0, valid, true);
+        dequant_half(1, valid, true);
+        if (t + 1 < ntiles) load_scales(t + 1, sw);
+        // P_t = exp2(z - M) in f16, MN-major [entry][head] core matrices; partial row sums
+        {
+            uint32_t r[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + TK_S_COL + HB * t + 16 * hh, r);
+            tc::tmem_ld_wait();
+            const int ee = 32 * quarter + lane;
+            const bool v = ok && sRow[t * TM + ee] >= 0;
+            float pf[16];
+            uint32_t pk[8];
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 2) {
+                float p2[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int hd = 16 * hh + jj + u;
+                    const float mx = sM[hd];
+                    const float zz = __uint_as_float(r[jj + u]) * sCs[hd];
+                    p2[u] = (!v || mx == -INFINITY) ? 0.f : ex2(zz - mx);
+                }
+                const __half2 hp = __floats2half2_rn(p2[0], p2[1]);
+                pk[jj / 2] = *reinterpret_cast<const uint32_t *>(&hp);
+                const float2 back = __half22float2(hp);
+                pf[jj] = back.x;
+                pf[jj + 1] = back.y;
+            }
+            uint8_t *pdst = sP + (ee >> 3) * 128 + (ee & 7) * 16;
+            *reinterpret_cast<uint4 *>(pdst + (2 * hh) * TK_P_SBO) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4 *>(pdst + (2 * hh + 1) * TK_P_SBO) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            const float sum = lane_reduce16<false>(pf, lane);
+            if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = sum;
+        }
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        if (tid < HB) sL[tid] += (sPart[tid] + sPart[HB + tid]) + (sPart[2 * HB + tid] + sPart[3 * HB + tid]);
+        if (tid == 0) {
+            for (int mb = 0; mb < DV / 128; ++mb)
+#pragma unroll
+                for (int ks = 0; ks < TM / 16; ++ks)
+                    tc::mma_f16(tmem + TK_O_COL + mb * HB,
+                                tc::desc_noswizzle(a0s + ks * 2 * KT_SBO + mb * 16 * 128, KT_SBO, 128),
+                                tc::desc_noswizzle(p0 + ks * 256, 128, TK_P_SBO), idesc_o, t > 0 || ks > 0);
+            tc::commit(bar_o);
+        }
+    }
+    ok = tc::mbar_wait(bar_o, (ntiles - 1) & 1, MAX_POLLS) && ok;
+    tc::fence_after();
+    __syncthreads();   // sL complete
+    if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
+
+    // ---- out = O / L (lanes = 32 consecutive channels of one head per store), lse
+    {
+        float il[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const float l = sL[16 * hh + jj];
+            il[jj] = l > 0.f ? 1.f / l : 0.f;
+        }
+        const int64_t hbase = (bt * a.H) + h0 + 16 * hh;
+#pragma unroll 1
+        for (int mb = 0; mb < DV / 128; ++mb) {
+            uint32_t r[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + TK_O_COL + mb * HB + 16 * hh, r);
+            tc::tmem_ld_wait();
+            const int c = mb * 128 + 32 * quarter + lane;
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) a.out[(hbase + jj) * (int64_t)DV + c] = __uint_as_float(r[jj]) * il[jj];
+        }
+        if (a.lse && tid < HB) {
+            const float l = sL[tid], mx = sM[tid];
+            a.lse[(bt * a.H) + h0 + tid] = (l > 0.f && mx != -INFINITY) ? (mx + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
 }  // namespace
 
 bool sparse_attn_tc_supported(int D_, int dv, int H, int K) {
@@ -744,6 +1111,27 @@ static csa2_status launch_tc(TcArgs &a, int B, int entries, cudaStream_t stream)
     return CSA2_OK;
 }
 
+static csa2_status launch_tc_tokens(TcArgs &a, int B, cudaStream_t stream) {
+    static bool smem_set[64];
+    CSA2_CUDA_CALL(ensure_smem_limit((const void *)sparse_attn_tc_tokens_kernel, (int)TK_SMEM, smem_set),
+                   "sparse_attn_tc_tokens: smem attribute");
+    a.hblocks = a.H / HB;
+    a.csize = 1;
+    const int64_t grid = (int64_t)B * a.T * a.hblocks;
+    if (grid > 0x7FFFFFFF) {
+        set_error("sparse_attn_tc_tokens: grid too large");
+        return CSA2_ERR_UNSUPPORTED;
+    }
+    CSA2_CUDA_CALL(launch_pdl(sparse_attn_tc_tokens_kernel, dim3((unsigned)grid), dim3(THREADS), TK_SMEM, stream, a),
+                   "sparse_attn_tc_tokens_kernel launch");
+    CSA2_LAUNCH_CHECK("sparse_attn_tc_tokens_kernel");
+    return CSA2_OK;
+}
+
+// Many (token, 64-head) items: more than a quarter of the SMs, i.e. the cluster
+// kernel's grid (up to four CTAs per item) would exceed one wave.
+bool use_token_kernel(int64_t items) { return items * 4 > (int64_t)num_sms(); }
+
 csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const void *q, const uint8_t *codes,
                                   const uint8_t *scales, const int32_t *idx, const int32_t *kv_len, float sm_scale,
                                   float *out, float *lse, uint32_t *err_flag, const uint8_t *pf_codes,
@@ -753,6 +1141,7 @@ csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const v
     a.T = T; a.H = H; a.K = K; a.N = N;
     a.q = (const uint16_t *)q; a.codes = codes; a.scales = scales; a.idx = idx; a.kv_len = kv_len;
     a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.err_flag = err_flag;
+    if (use_token_kernel((int64_t)B * T * (H / HB))) return launch_tc_tokens(a, B, stream);
     return launch_tc<false>(a, B, K, stream);
 }
 

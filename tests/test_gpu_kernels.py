@@ -340,6 +340,11 @@ def _attn_gpu(csa2, q, codes, scales, N, idx, kv_len, sm, dv, flag=None):
     ("full", 3, 1, 4000, 1024, 64, 0.1),      # K > 512: the mma.sync kernel
     ("full", 2, 2, 3000, 700, 64, 0.0),       # K > 512, not a multiple of the entry tile
     ("full", 1, 1, 3000, 1500, 64, 0.0),      # one row, K = 1500: split-KV partials + combine
+    # enough (token, 64-head) items for the one-CTA-per-item two-pass kernel (more than a quarter of the SMs)
+    ("full", 48, 1, 3000, 512, 64, 0.1),      # four tiles, padded rows
+    ("full", 24, 2, 2000, 300, 64, 0.0),      # three tiles, the last one ragged, two tokens per row
+    ("full", 40, 1, 900, 100, 128, 0.2),      # one tile, two head blocks
+    ("full", 20, 1, 5000, 257, 128, 0.0),     # three tiles, one entry in the last
 ])
 def test_sparse_attn_matches_oracle(csa2, base, B, T, N, K, H, pad):
     w0 = gen.TINY_FULL_DECODE if base == "tiny" else gen.FULL_BATCHED_DECODE
