@@ -836,6 +836,20 @@ def run_profile_case(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile_case": "append_quantize_1m_rows", "calls": 2}))
         return
+    if case == "prefill_attn":
+        # the many-token attention kernel on 1024 of the prefill chunk's queries, twice (about 0.3 GB)
+        w4 = gen.scaled(gen.PREFILL_CHUNK, T=1024)
+        kl4 = gen.kv_lengths(w4).to("cuda")
+        c4, s4 = gen.fp4_planes(3, 1, w4.N, D, device="cuda")
+        idx4 = gen.random_indices(w4, kl4.cpu()).to("cuda")
+        qa4 = gen.normal_bf16(3, 2, (1, w4.T, H, D), device="cuda")
+        oa4 = torch.empty(1, w4.T, H, DV, device="cuda")
+        flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            csa2.csa2_sparse_attn_fp4(0, qa4, c4, s4, w4.N, idx4, oa4, 1 / D ** 0.5, kv_len=kl4, err_flag=flag)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": "prefill_attention_t1024_k512", "calls": 2, "error_flag": int(flag.item())}))
+        return
     if case == "prefill":
         w4 = gen.PREFILL_CHUNK
         q4, ww4, k4 = gen.indexer_inputs(w4, device="cuda")
@@ -870,8 +884,9 @@ def main():
     ap.add_argument("--cpu-workers", type=int, default=0,
                     help="processes for the all-cores oracle baseline (0: one per host core; 1: skip it)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' timings")
-    ap.add_argument("--profile-case", nargs="?", const="decode", default=None, choices=["decode", "append", "prefill"],
-                    help="a small case for ncu: 3 eager decode steps (default), the 1M-row append, or the prefill indexer")
+    ap.add_argument("--profile-case", nargs="?", const="decode", default=None, choices=["decode", "append", "prefill", "prefill_attn"],
+                    help="a small case for ncu: 3 eager decode steps (default), the 1M-row append, the prefill indexer, "
+                         "or the many-token attention on 1024 prefill queries")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
