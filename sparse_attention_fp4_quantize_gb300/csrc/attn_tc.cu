@@ -127,12 +127,6 @@ __device__ __forceinline__ void e4m3x16_to_f16(const uint4 v, uint32_t (&r)[8]) 
     }
 }
 
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-    uint32_t r;
-    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t byte) {
     uint32_t r;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)(byte | (byte << 8))));
@@ -143,6 +137,25 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
+}
+
+// Eight E2M1 codes (one word; byte i holds codes 2i (low nibble) and 2i + 1)
+// -> four f16x2 words times the f16x2 scale sc (exact: at most 6 significant
+// bits).  The word is split into its bytes by a vector move, not by shifts.
+__device__ __forceinline__ void e2m1x8_scaled(uint32_t w, uint32_t sc, uint32_t *r) {
+    uint32_t h0, h1, h2, h3;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w));
+    r[0] = hmul2(h0, sc);
+    r[1] = hmul2(h1, sc);
+    r[2] = hmul2(h2, sc);
+    r[3] = hmul2(h3, sc);
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -355,11 +368,12 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     }
     __syncthreads();
     // ---- 2c. dequantise one half of this thread's groups into the Khat tile
-    auto dequant_half = [&](const int h) {
+    auto dequant_half = [&](const int h, auto &&before_group) {
         const int qh = (qt + 2 * h) & 3, nh = qh < 2 ? 5 : 4;
         uint8_t *kbase = sK + (e >> 3) * KT_SBO + (e & 7) * 16;
 #pragma unroll
         for (int i = 0; i < 5; ++i) {
+            before_group(i);
             if (i < nh) {
                 const int g = 18 * h + qh + 4 * i;   // group of the entry
                 // scale byte g: word g / 4, byte g % 4 (compile-time word choice by a select)
@@ -370,11 +384,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
                     e4m3x16_to_f16(w8[h][i], r);   // zero bytes for an invalid entry
                 } else if (valid) {
                     const uint32_t sc = e4m3_to_f16x2_bcast((word >> (8 * byte)) & 0xFFu);
-#pragma unroll
-                    for (int bb = 0; bb < 4; ++bb) {
-                        r[bb] = hmul2(e2m1x2_to_f16x2((cw[h][i].x >> (8 * bb)) & 0xFF), sc);
-                        r[4 + bb] = hmul2(e2m1x2_to_f16x2((cw[h][i].y >> (8 * bb)) & 0xFF), sc);
-                    }
+                    e2m1x8_scaled(cw[h][i].x, sc, r);
+                    e2m1x8_scaled(cw[h][i].y, sc, r + 4);
                 }
                 *reinterpret_cast<uint4 *>(kbase + (2 * g) * 128) = make_uint4(r[0], r[1], r[2], r[3]);
                 *reinterpret_cast<uint4 *>(kbase + (2 * g + 1) * 128) = make_uint4(r[4], r[5], r[6], r[7]);
@@ -384,19 +395,21 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     // ---- 3. S^T = Khat . Q^T  (M = 128 entries, N = 64 heads, K = 576): 18 k-steps per half
     const uint32_t a0s = tc::smem_u32(sK), b0s = tc::smem_u32(sQ);
     constexpr uint32_t idesc_s = tc::idesc_f16_f32(TM, HB, false, false);
-    dequant_half(0);
+    dequant_half(0, [](int) {});
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    if (tid == 0) {
-#pragma unroll 2
-        for (int ks = 0; ks < D / 32; ++ks)
-            tc::mma_f16(tmem + S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
-                        tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, ks > 0);
-    }
-    dequant_half(1);
+    // the first half's 18 MMAs, issued by thread 0 a few at a time between its
+    // own second-half groups (four of them), so that the issue does not hold
+    // its warp back while the tensor pipe drains
+    dequant_half(1, [&](int i) {
+        if (tid == 0 && i < 4)
+            for (int ks = (D / 32) * i / 4; ks < (D / 32) * (i + 1) / 4; ++ks)
+                tc::mma_f16(tmem + S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
+                            tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, ks > 0);
+    });
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
@@ -711,40 +724,46 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
 
 // ---------------------------------------------------------------------------
 // Many query tokens: one CTA per (token, 64 heads) over all of its K <= 512
-// selected entries, in two passes and with no cluster merge (used when a
-// launch has enough (token, head-block) items to fill the GPU on its own,
-// e.g. a prefill chunk).  512 threads; the same 128-entry tile and MMA shapes
-// as above.
-//  Pass 1, per 128-entry tile t: the code rows by TMA bulk copies, all 576
-//   channels dequantised into the Khat tile, S^T_t = Khat . Q^T into TMEM
-//   columns [64 t, 64 t + 64); once those MMAs have released the tile the next
-//   tile's rows are copied in, while the per-head maxima of tile t are taken
-//   straight from TMEM (a butterfly over the 32 lanes of each warp).
-//  Pass 2, per tile: the rows again (now from L2; the next tile's land in the
-//   dead Q region meanwhile), the value channels into the Khat tile,
-//   P_t = exp2(z - M) from TMEM into an f16 tile laid out MN-major, and
-//   O^T += Vhat_t^T . P_t^T into TMEM columns [256, 512).
-//  Finally out = O / L and lse = (M + log2 L) ln 2 per head, L summed over the
-//  f16-rounded P as the MMAs consumed it.
+// selected entries in one pass with an online softmax, no cluster merge (used
+// when a launch has enough (token, head-block) items to fill the GPU on its
+// own, e.g. a prefill chunk).  512 threads; the same 128-entry tile and MMA
+// shapes as above.  Per 128-entry tile t:
+//  - the entry's 288 code bytes and 36 scale bytes were loaded into registers
+//    while tile t-1 was computed (tile 0: while Q was converted), 8 bytes of
+//    codes per thread and load, four lanes per entry, so one warp load touches
+//    8 rows with one 32-byte sector each;
+//  - the 576 channels are dequantised into the Khat tile in two parts:
+//    channels 0..255 once P V of tile t-1 has read its first two channel
+//    blocks (its last two still running), the rest once it is done, the first
+//    part's S MMAs running meanwhile: S^T_t = Khat . Q^T into TMEM columns
+//    [0, 64);
+//  - z = S * c per head; the running maximum M moves only when a tile's
+//    maximum exceeds it by more than 8 (log2 units), and then O^T and the
+//    running sum are scaled by 2^(M_old - M_new), so P = 2^(z - M) <= 256;
+//  - P_t in f16, laid out MN-major in the Khat tile's rotary channels (dead
+//    once S_t is done); O^T += Vhat_t^T . P_t^T into TMEM columns [64, 320)
+//    is issued at the start of tile t+1, ahead of its dequantisation.
+// Finally out = O / L and lse = (M + log2 L) ln 2 per head, L summed over the
+// f16-rounded P as the MMAs consumed it.
 constexpr uint32_t TK_OFF_K = 0;
-constexpr uint32_t TK_OFF_Q = KT_BYTES;                        // Q tile (pass 1)
-constexpr uint32_t TK_OFF_STAGE2 = TK_OFF_Q;                   // pass 2: code rows of the next tile
-constexpr uint32_t TK_P_SBO = (TM / 8) * 128;                  // MN-major P: 2048 bytes per 8-head group
-constexpr uint32_t TK_P_BYTES = (HB / 8) * TK_P_SBO;           // 16384
-constexpr uint32_t TK_OFF_P = TK_OFF_Q + Q_BYTES - TK_P_BYTES; // pass 2: P tile
-constexpr uint32_t TK_OFF_BAR = TK_OFF_Q + Q_BYTES;            // mbarriers: Q rows, code rows, S, P V
+constexpr uint32_t TK_OFF_Q = KT_BYTES;                        // Q tile
+constexpr uint32_t TK_P_IN_GROUP = (DV / 8) * 128;             // P: the rotary core matrices of each 8-entry group
+constexpr uint32_t TK_OFF_BAR = TK_OFF_Q + Q_BYTES;            // mbarriers: Q rows, S, P V
 constexpr uint32_t TK_OFF_TMEM = TK_OFF_BAR + 32;
 constexpr uint32_t TK_OFF_ROW = TK_OFF_TMEM + 16;              // int64[512] KV row of each selected entry, -1 if none
 constexpr uint32_t TK_OFF_QMAX = TK_OFF_ROW + MAX_S * TM * 8;  // uint[64] per-head max |q| (bits)
 constexpr uint32_t TK_OFF_CS = TK_OFF_QMAX + HB * 4;           // float[64] logit factor per head
 constexpr uint32_t TK_OFF_PART = TK_OFF_CS + HB * 4;           // float[4][64] per lane quarter
-constexpr uint32_t TK_OFF_M = TK_OFF_PART + 4 * HB * 4;        // float[64] row max (log2 domain)
-constexpr uint32_t TK_OFF_L = TK_OFF_M + HB * 4;               // float[64] row sum
-constexpr uint32_t TK_SMEM = TK_OFF_L + HB * 4;
-constexpr uint32_t TK_S_COL = 0, TK_O_COL = MAX_S * HB;        // S^T tiles: 4 x 64 columns; O^T: 4 x 64
-static_assert(TM * CRAW_STRIDE <= Q_BYTES - TK_P_BYTES, "pass-2 staging must fit below the P tile");
+constexpr uint32_t TK_OFF_M = TK_OFF_PART + 4 * HB * 4;        // float[64] running max (log2 domain)
+constexpr uint32_t TK_OFF_L = TK_OFF_M + HB * 4;               // float[64] running sum
+constexpr uint32_t TK_OFF_ALPHA = TK_OFF_L + HB * 4;           // float[64] rescale factor of this tile
+constexpr uint32_t TK_SMEM = TK_OFF_ALPHA + HB * 4;
+constexpr uint32_t TK_S_COL = 0, TK_O_COL = HB;                // S^T: 64 columns; O^T: 4 x 64
+constexpr float TK_MAX_SLACK = 8.f;                            // P <= 2^8 between rescales
+static_assert((HB / 8) * 128 == KT_SBO - TK_P_IN_GROUP, "P fills the rotary channels of an 8-entry group");
 static_assert(TK_O_COL + (DV / 128) * HB <= TMEM_COLS, "TMEM columns");
 static_assert(TK_SMEM <= 227 * 1024, "shared memory");
+static_assert(HB * QRAW_STRIDE <= KT_BYTES, "Q staging fits in the Khat region");
 
 // Reduce-scatter of 16 values over the 32 lanes of a warp: afterwards lanes l
 // and l ^ 1 both hold the reduction over all lanes of value (l >> 1) & 15.
@@ -768,6 +787,16 @@ __device__ __forceinline__ float lane_reduce16(float (&v)[16], int lane) {
     return op(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 1));
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -779,7 +808,6 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
 
     uint8_t *sK = smem + TK_OFF_K;
     uint8_t *sQ = smem + TK_OFF_Q;
-    uint8_t *sP = smem + TK_OFF_P;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + TK_OFF_TMEM);
     int64_t *sRow = reinterpret_cast<int64_t *>(smem + TK_OFF_ROW);
     uint32_t *sQmax = reinterpret_cast<uint32_t *>(smem + TK_OFF_QMAX);
@@ -787,20 +815,21 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
     float *sPart = reinterpret_cast<float *>(smem + TK_OFF_PART);
     float *sM = reinterpret_cast<float *>(smem + TK_OFF_M);
     float *sL = reinterpret_cast<float *>(smem + TK_OFF_L);
+    float *sAlpha = reinterpret_cast<float *>(smem + TK_OFF_ALPHA);
     const uint32_t bar_q = tc::smem_u32(smem + TK_OFF_BAR);   // Q rows landed
-    const uint32_t bar_ld = bar_q + 8;                          // a tile's code rows landed (one phase per tile and pass)
-    const uint32_t bar_s = bar_q + 16;                          // S MMAs of a tile done
-    const uint32_t bar_o = bar_q + 24;                          // P V MMAs of a tile done
+    const uint32_t bar_s = bar_q + 8;                           // S MMAs of a tile done
+    const uint32_t bar_o = bar_q + 16;                          // P V MMAs of a tile done
+    const uint32_t bar_o1 = bar_q + 24;                         // its first two channel blocks done
 
-    const int e = tid & (TM - 1), qt = tid >> 7;   // entry of this thread in a tile, channel quarter
-    const bool issuer = qt == ((e >> 3) & 3);        // one thread per entry, spread over all 16 warps
-    const int quarter = warp & 3, hh = warp >> 2;    // TMEM lane quarter, 16-column group
+    // dequantisation: entry de of a tile, lane dq of its four; channel groups dq + 4 j
+    const int de = 8 * warp + (lane >> 2), dq = lane & 3;
+    const int quarter = warp & 3, hh = warp >> 2;    // TMEM lane quarter, 16-head group
 
     if (tid == 0) {
         tc::mbar_init(bar_q, HB);    // one arrival per head row
-        tc::mbar_init(bar_ld, TM);   // one arrival per entry of a tile
         tc::mbar_init(bar_s, 1);
         tc::mbar_init(bar_o, 1);
+        tc::mbar_init(bar_o1, 1);
         tc::mbar_init_fence();
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -812,10 +841,11 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
     __syncthreads();
     pdl_wait();   // the set-up above overlaps the previous kernel's tail
 
-    // the Q rows (no index needed) first, then every selected entry's row
-    if (issuer && e < HB) {
+    // the Q rows (one bulk copy per head row, issuers spread over the warps), then the entries' rows
+    if ((tid & 7) == 0) {
+        const int hr = tid >> 3;
         mbar_arrive_expect_tx(bar_q, D * 2);
-        bulk_g2s(tc::smem_u32(smem + OFF_QRAW + e * QRAW_STRIDE), a.q + ((bt * a.H) + h0 + e) * (int64_t)D, D * 2,
+        bulk_g2s(tc::smem_u32(smem + OFF_QRAW + hr * QRAW_STRIDE), a.q + ((bt * a.H) + h0 + hr) * (int64_t)D, D * 2,
                  bar_q);
     }
     {
@@ -829,27 +859,28 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
         }
     }
     __syncthreads();
-    auto issue_codes = [&](int t, uint32_t stage) {   // the issuers: one row each, on bar_ld
-        if (issuer) {
-            const int64_t r = sRow[t * TM + e];
-            mbar_arrive_expect_tx(bar_ld, r >= 0 ? D / 2 : 0);
-            if (r >= 0) bulk_g2s(stage + e * CRAW_STRIDE, a.codes + r * (D / 2), D / 2, bar_ld);
-        }
-    };
-    auto load_scales = [&](int t, uint32_t (&sw)[9]) {   // the entry's 36 scale bytes as 9 words
-        const int64_t r = sRow[t * TM + e];
-#pragma unroll
-        for (int i = 0; i < 9; ++i) sw[i] = 0u;
+
+    // this thread's code and scale bytes of one tile, straight into registers
+    uint2 cw[9];
+    uint32_t sw[9];
+    auto load_tile = [&](int t) {
+        const int64_t r = sRow[t * TM + de];
         if (r >= 0) {
+            const uint2 *crow = reinterpret_cast<const uint2 *>(a.codes + r * (D / 2));
             const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + r * (D / 16));
 #pragma unroll
-            for (int i = 0; i < 9; ++i) sw[i] = __ldg(srow + i);
+            for (int j = 0; j < 9; ++j) cw[j] = __ldg(crow + dq + 4 * j);
+#pragma unroll
+            for (int j = 0; j < 9; ++j) sw[j] = __ldg(srow + j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 9; ++j) {
+                cw[j] = make_uint2(0u, 0u);
+                sw[j] = 0u;
+            }
         }
     };
-    const uint32_t stage1 = tc::smem_u32(smem + OFF_CRAW), stage2 = tc::smem_u32(smem + TK_OFF_STAGE2);
-    issue_codes(0, stage1);
-    uint32_t sw[9];
-    load_scales(0, sw);
+    load_tile(0);
 
     // ---- Q -> registers -> per-head power-of-two scale -> f16 core-matrix tile (as the cluster kernel)
     bool ok = tc::mbar_wait(bar_q, 0, MAX_POLLS);
@@ -870,7 +901,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
         if (cpos == 0) atomicMax(sQmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
-        __syncthreads();
+        __syncthreads();   // also: every read of the Q staging (in the Khat region) is done
         mx = __uint_as_float(sQmax[hq]);
         const int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
         int sh = 14 - e2;   // max |q| * 2^sh in [2^14, 2^15)
@@ -889,119 +920,130 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
         if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
     }
 
-    // staged codes of entry e -> registers: in half h the groups 18 h + qh + 4 i with qh = (qt + 2 h) mod 4
-    uint2 cw[2][5];
-    auto read_codes = [&](uint32_t stage_off, bool valid) {
-        const uint8_t *craw = smem + stage_off + e * CRAW_STRIDE;
+    // dequantise channel groups dq + 4 j, j in [j0, j1), of entry de into the Khat tile
+    uint8_t *kbase = sK + warp * KT_SBO + (lane >> 2) * 16;   // (de >> 3) == warp
+    auto dequant = [&](auto j0_c, auto j1_c, bool valid, auto &&before_group) {
+        constexpr int j0 = decltype(j0_c)::value, j1 = decltype(j1_c)::value;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int qh = (qt + 2 * h) & 3, nh = qh < 2 ? 5 : 4;
-#pragma unroll
-            for (int i = 0; i < 5; ++i)
-                cw[h][i] = (valid && i < nh) ? *reinterpret_cast<const uint2 *>(craw + 8 * (18 * h + qh + 4 * i))
-                                              : make_uint2(0, 0);
-        }
-    };
-    // dequantise half h of this thread's groups into the Khat tile (values_only: the 32 value groups)
-    auto dequant_half = [&](const int h, bool valid, bool values_only) {
-        const int qh = (qt + 2 * h) & 3, nh = qh < 2 ? 5 : 4;
-        uint8_t *kbase = sK + (e >> 3) * KT_SBO + (e & 7) * 16;
-#pragma unroll
-        for (int i = 0; i < 5; ++i) {
-            const int g = 18 * h + qh + 4 * i;   // group of the entry
-            if (i < nh && (!values_only || g < DV / 16)) {
-                const uint32_t word = h == 0 ? sw[i] : ((qh >> 1) ? sw[i < 4 ? 5 + i : 8] : sw[4 + i]);
-                const int byte = h == 0 ? qh : ((2 + qh) & 3);
-                uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                if (valid) {
-                    const uint32_t sc = e4m3_to_f16x2_bcast((word >> (8 * byte)) & 0xFFu);
-#pragma unroll
-                    for (int bb = 0; bb < 4; ++bb) {
-                        r[bb] = hmul2(e2m1x2_to_f16x2((cw[h][i].x >> (8 * bb)) & 0xFF), sc);
-                        r[4 + bb] = hmul2(e2m1x2_to_f16x2((cw[h][i].y >> (8 * bb)) & 0xFF), sc);
-                    }
-                }
-                *reinterpret_cast<uint4 *>(kbase + (2 * g) * 128) = make_uint4(r[0], r[1], r[2], r[3]);
-                *reinterpret_cast<uint4 *>(kbase + (2 * g + 1) * 128) = make_uint4(r[4], r[5], r[6], r[7]);
+        for (int j = j0; j < j1; ++j) {
+            before_group(j - j0);
+            const int g = dq + 4 * j;
+            uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (valid) {
+                const uint32_t sc = e4m3_to_f16x2_bcast((sw[j] >> (8 * dq)) & 0xFFu);
+                e2m1x8_scaled(cw[j].x, sc, r);
+                e2m1x8_scaled(cw[j].y, sc, r + 4);
             }
+            *reinterpret_cast<uint4 *>(kbase + (2 * g) * 128) = make_uint4(r[0], r[1], r[2], r[3]);
+            *reinterpret_cast<uint4 *>(kbase + (2 * g + 1) * 128) = make_uint4(r[4], r[5], r[6], r[7]);
         }
     };
     const uint32_t tmem = *tmem_slot;
     const uint32_t a0s = tc::smem_u32(sK), b0s = tc::smem_u32(sQ);
     constexpr uint32_t idesc_s = tc::idesc_f16_f32(TM, HB, false, false);
-    uint32_t ld_phase = 0;
+    constexpr uint32_t idesc_o = tc::idesc_f16_f32(TM, HB, true, true);
+    constexpr int KS_A = 16;   // groups 0..15 (channels 0..255: the value blocks P V reads first) go first
+    const uint32_t s_lane = tmem + ((uint32_t)(32 * quarter) << 16);
 
-    // ---- pass 1: S^T of every tile, per-head maxima
+    // P V of tile tp, value channel block mb, entry steps [ks0, ks1): O^T += Vhat^T . P^T
+    auto pv_mmas = [&](int tp, int mb, int ks0, int ks1) {
+        for (int ks = ks0; ks < ks1; ++ks)
+            tc::mma_f16(tmem + TK_O_COL + mb * HB, tc::desc_noswizzle(a0s + ks * 2 * KT_SBO + mb * 16 * 128, KT_SBO, 128),
+                        tc::desc_noswizzle(a0s + ks * 2 * KT_SBO + TK_P_IN_GROUP, KT_SBO, 128), idesc_o,
+                        tp > 0 || ks > 0);
+    };
+
     for (int t = 0; t < ntiles; ++t) {
-        ok = tc::mbar_wait(bar_ld, ld_phase & 1, MAX_POLLS) && ok;
-        ++ld_phase;
-        const bool valid = sRow[t * TM + e] >= 0;
-        read_codes(OFF_CRAW, valid);
-        __syncthreads();   // staging and Q-staging reads done: the Khat tile may overwrite them
-        dequant_half(0, valid, false);
+        // P V of tile t-1 is issued here: its first two channel blocks, then the
+        // other two a few MMAs at a time between thread 0's first groups (the issue
+        // waits on the tensor pipe).  Channels 0..255 are dequantised once the
+        // first two blocks have read them, the rest once all of it is done.
+        if (t > 0) {
+            if (tid == 0) {
+                pv_mmas(t - 1, 0, 0, TM / 16);
+                pv_mmas(t - 1, 1, 0, TM / 16);
+                tc::commit(bar_o1);
+            }
+            ok = tc::mbar_wait(bar_o1, (t - 1) & 1, MAX_POLLS) && ok;
+        }
+        tc::fence_after();
+        const bool valid = sRow[t * TM + de] >= 0;
+        dequant(std::integral_constant<int, 0>{}, std::integral_constant<int, 4>{}, valid, [&](int i) {
+            if (t > 0 && tid == 0) pv_mmas(t - 1, 2 + (i >> 1), (i & 1) * (TM / 32), ((i & 1) + 1) * (TM / 32));
+        });
+        if (t > 0 && tid == 0) tc::commit(bar_o);
         tc::fence_async_smem();
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
-        if (tid == 0)
-            for (int ks = 0; ks < D / 32; ++ks)
-                tc::mma_f16(tmem + TK_S_COL + HB * t, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
-                            tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, ks > 0);
-        dequant_half(1, valid, false);
+        if (t > 0) ok = tc::mbar_wait(bar_o, (t - 1) & 1, MAX_POLLS) && ok;
+        tc::fence_after();
+        // the first part's 16 MMAs, four before each of thread 0's first four later groups
+        dequant(std::integral_constant<int, 4>{}, std::integral_constant<int, 9>{}, valid, [&](int i) {
+            if (tid == 0 && i < 4)
+                for (int ks = KS_A * i / 4; ks < KS_A * (i + 1) / 4; ++ks)
+                    tc::mma_f16(tmem + TK_S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
+                                tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, ks > 0);
+        });
         tc::fence_async_smem();
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
         if (tid == 0) {
-            for (int ks = D / 32; ks < D / 16; ++ks)
-                tc::mma_f16(tmem + TK_S_COL + HB * t, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
+            for (int ks = KS_A; ks < D / 16; ++ks)
+                tc::mma_f16(tmem + TK_S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
                             tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, true);
             tc::commit(bar_s);
         }
-        if (t + 1 < ntiles) load_scales(t + 1, sw);
+        if (t + 1 < ntiles) load_tile(t + 1);   // lands while this tile is finished
         ok = tc::mbar_wait(bar_s, t & 1, MAX_POLLS) && ok;
         tc::fence_after();
-        if (t + 1 < ntiles) issue_codes(t + 1, stage1);   // the MMAs have released the Khat tile
-        // per-head maximum of this tile's logits
-        uint32_t r[16];
-        tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + TK_S_COL + HB * t + 16 * hh, r);
-        tc::tmem_ld_wait();
-        const bool v = ok && sRow[t * TM + 32 * quarter + lane] >= 0;
-        float z[16];
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) z[jj] = v ? __uint_as_float(r[jj]) * sCs[16 * hh + jj] : -INFINITY;
-        const float m = lane_reduce16<true>(z, lane);
-        if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = m;
-        __syncthreads();
-        if (tid < HB)
-            sM[tid] = fmaxf(fmaxf(sM[tid], fmaxf(sPart[tid], sPart[HB + tid])),
-                            fmaxf(sPart[2 * HB + tid], sPart[3 * HB + tid]));
-    }
 
-    // ---- pass 2: P V of every tile
-    load_scales(0, sw);
-    issue_codes(0, stage2);   // the Q tile is dead: its region stages the rows
-    const uint32_t p0 = tc::smem_u32(sP);
-    constexpr uint32_t idesc_o = tc::idesc_f16_f32(TM, HB, true, true);
-    for (int t = 0; t < ntiles; ++t) {
-        ok = tc::mbar_wait(bar_ld, ld_phase & 1, MAX_POLLS) && ok;
-        ++ld_phase;
-        const bool valid = sRow[t * TM + e] >= 0;
-        read_codes(TK_OFF_STAGE2, valid);
-        if (t > 0) ok = tc::mbar_wait(bar_o, (t - 1) & 1, MAX_POLLS) && ok;   // the previous P V released the tiles
-        tc::fence_after();
-        __syncthreads();   // staging reads done; sM (after pass 1) visible
-        if (t + 1 < ntiles) issue_codes(t + 1, stage2);
-        dequant_half(0, valid, true);
-        dequant_half(1, valid, true);
-        if (t + 1 < ntiles) load_scales(t + 1, sw);
-        // P_t = exp2(z - M) in f16, MN-major [entry][head] core matrices; partial row sums
+        // logits of this warp's 32 entries x 16 heads; the tile's per-head maximum
+        uint32_t r[16];
+        tc::tmem_ld16(s_lane + TK_S_COL + 16 * hh, r);
+        tc::tmem_ld_wait();
+        const int ee = 32 * quarter + lane;
+        const bool v = ok && sRow[t * TM + ee] >= 0;
         {
-            uint32_t r[16];
-            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + TK_S_COL + HB * t + 16 * hh, r);
-            tc::tmem_ld_wait();
-            const int ee = 32 * quarter + lane;
-            const bool v = ok && sRow[t * TM + ee] >= 0;
+            float z[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) z[jj] = v ? __uint_as_float(r[jj]) * sCs[16 * hh + jj] : -INFINITY;
+            const float m = lane_reduce16<true>(z, lane);
+            if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = m;
+        }
+        __syncthreads();
+        bool resc = false;
+        if (tid < HB) {
+            const float mt = fmaxf(fmaxf(sPart[tid], sPart[HB + tid]), fmaxf(sPart[2 * HB + tid], sPart[3 * HB + tid]));
+            const float mo = sM[tid];
+            float al = 1.f;
+            if (mt > mo + TK_MAX_SLACK) {   // also the first finite maximum (mo = -inf)
+                resc = mo != -INFINITY;
+                al = resc ? ex2(mo - mt) : 0.f;
+                sM[tid] = mt;
+                sL[tid] *= al;
+            }
+            sAlpha[tid] = al;
+        }
+        tc::fence_before();
+        const bool any_resc = __syncthreads_or(resc) != 0;
+        tc::fence_after();
+        if (any_resc) {   // O^T *= alpha per head column (P V of t-1 is complete)
+#pragma unroll 1
+            for (int mb = 0; mb < DV / 128; ++mb) {
+                uint32_t o[16];
+                const uint32_t ta = s_lane + TK_O_COL + mb * HB + 16 * hh;
+                tc::tmem_ld16(ta, o);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) o[jj] = __float_as_uint(__uint_as_float(o[jj]) * sAlpha[16 * hh + jj]);
+                tmem_st16(ta, o);
+            }
+            tmem_st_wait();
+        }
+        // P_t = 2^(z - M) in f16 into the rotary channels of the Khat tile (MN-major: 8 heads per 16 bytes); row sums
+        {
             float pf[16];
             uint32_t pk[8];
 #pragma unroll
@@ -1020,9 +1062,9 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
                 pf[jj] = back.x;
                 pf[jj + 1] = back.y;
             }
-            uint8_t *pdst = sP + (ee >> 3) * 128 + (ee & 7) * 16;
-            *reinterpret_cast<uint4 *>(pdst + (2 * hh) * TK_P_SBO) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4 *>(pdst + (2 * hh + 1) * TK_P_SBO) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            uint8_t *pdst = sK + (ee >> 3) * KT_SBO + TK_P_IN_GROUP + (ee & 7) * 16;
+            *reinterpret_cast<uint4 *>(pdst + (2 * hh) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4 *>(pdst + (2 * hh + 1) * 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             const float sum = lane_reduce16<false>(pf, lane);
             if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = sum;
         }
@@ -1031,15 +1073,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
         __syncthreads();
         tc::fence_after();
         if (tid < HB) sL[tid] += (sPart[tid] + sPart[HB + tid]) + (sPart[2 * HB + tid] + sPart[3 * HB + tid]);
-        if (tid == 0) {
-            for (int mb = 0; mb < DV / 128; ++mb)
-#pragma unroll
-                for (int ks = 0; ks < TM / 16; ++ks)
-                    tc::mma_f16(tmem + TK_O_COL + mb * HB,
-                                tc::desc_noswizzle(a0s + ks * 2 * KT_SBO + mb * 16 * 128, KT_SBO, 128),
-                                tc::desc_noswizzle(p0 + ks * 256, 128, TK_P_SBO), idesc_o, t > 0 || ks > 0);
-            tc::commit(bar_o);
-        }
+    }
+    if (tid == 0) {   // P V of the last tile
+        for (int mb = 0; mb < DV / 128; ++mb) pv_mmas(ntiles - 1, mb, 0, TM / 16);
+        tc::commit(bar_o);
     }
     ok = tc::mbar_wait(bar_o, (ntiles - 1) & 1, MAX_POLLS) && ok;
     tc::fence_after();
@@ -1058,7 +1095,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
 #pragma unroll 1
         for (int mb = 0; mb < DV / 128; ++mb) {
             uint32_t r[16];
-            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + TK_O_COL + mb * HB + 16 * hh, r);
+            tc::tmem_ld16(s_lane + TK_O_COL + mb * HB + 16 * hh, r);
             tc::tmem_ld_wait();
             const int c = mb * 128 + 32 * quarter + lane;
 #pragma unroll

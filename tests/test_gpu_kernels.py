@@ -340,7 +340,7 @@ def _attn_gpu(csa2, q, codes, scales, N, idx, kv_len, sm, dv, flag=None):
     ("full", 3, 1, 4000, 1024, 64, 0.1),      # K > 512: the mma.sync kernel
     ("full", 2, 2, 3000, 700, 64, 0.0),       # K > 512, not a multiple of the entry tile
     ("full", 1, 1, 3000, 1500, 64, 0.0),      # one row, K = 1500: split-KV partials + combine
-    # enough (token, 64-head) items for the one-CTA-per-item two-pass kernel (more than a quarter of the SMs)
+    # enough (token, 64-head) items for the one-CTA-per-item kernel (more than a quarter of the SMs)
     ("full", 48, 1, 3000, 512, 64, 0.1),      # four tiles, padded rows
     ("full", 24, 2, 2000, 300, 64, 0.0),      # three tiles, the last one ragged, two tokens per row
     ("full", 40, 1, 900, 100, 128, 0.2),      # one tile, two head blocks
@@ -358,6 +358,46 @@ def test_sparse_attn_matches_oracle(csa2, base, B, T, N, K, H, pad):
     got, glse = _attn_gpu(csa2, q, codes, scales, N, idx, kl, sm, w.dv)
     ref, rlse, bad = oracle.sparse_attn(gen.as_numpy(q), codes, scales, N, idx, kl, sm, w.dv)
     assert bad == 0
+    check_attn(got, ref)
+    check_lse(glse, rlse)
+
+
+def test_sparse_attn_many_tokens_running_max_moves(csa2):
+    """Launches with many (token, 64-head) items take one CTA per item and an
+    online softmax over its 128-entry tiles, whose running maximum moves only
+    when a tile's maximum exceeds it by a wide margin.  Entries 2000.. of every
+    sequence get scale bytes 16x larger (four more exponent steps), so their
+    logits are about 16x wider: tokens whose large entries sit in the last two
+    tiles raise the maximum after two tiles (the partial output is rescaled),
+    the others meet them in the first two tiles (later tiles add almost
+    nothing), and one token alternates them.  Against the oracle."""
+    B, N, K = 48, 3000, 512
+    w = gen.scaled(gen.FULL_BATCHED_DECODE, B=B, T=1, N=N, K=K, H=64)
+    codes, scales = _kv_planes(gen.FULL_BATCHED_DECODE, B, N)
+    scales = scales.copy()
+    big = np.zeros(B * N, bool)
+    for bb in range(B):
+        big[bb * N + 2000:(bb + 1) * N] = True
+    sc = scales[big].astype(np.int32)
+    scales[big] = np.where(sc == 0, 0, np.minimum(sc + 0x20, 0x7E)).astype(np.uint8)
+    rng = np.random.default_rng(7)
+    idx = np.empty((B, 1, K), np.int32)
+    for bb in range(B):
+        small = rng.choice(2000, 256, replace=False)
+        large = 2000 + rng.choice(N - 2000, 256, replace=False)
+        if bb % 2 == 0:
+            row = np.concatenate([small, large])
+        else:
+            row = np.concatenate([large, small])
+        if bb == 1:
+            row = np.stack([small, large], 1).reshape(-1)
+        idx[bb, 0] = row
+    q = gen.attn_query(w)
+    sm = gen.softmax_scale(w.D)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got, glse = _attn_gpu(csa2, q, codes, scales, N, idx, None, sm, w.dv, flag=flag)
+    ref, rlse, bad = oracle.sparse_attn(gen.as_numpy(q), codes, scales, N, idx, None, sm, w.dv)
+    assert bad == 0 and int(flag.item()) == 0
     check_attn(got, ref)
     check_lse(glse, rlse)
 
