@@ -6,28 +6,38 @@
 //
 // With thousands of query tokens per sequence the scores are a dense
 // contraction: [T x 4 heads, 64] x [64, N keys].  Work item = (sequence b,
-// 64-query tile, range of 128-key tiles).  A persistent CTA per SM:
-//  - keeps the query tile (256 query-head rows x 64 B, FP8) in shared memory
-//    as the MMA B operand (K-major, no-swizzle core matrices);
-//  - streams key tiles (128 keys x 64 B) through an 8-stage cp.async ring,
-//    remapping each 16-byte chunk into the core-matrix layout;
-//  - issues S^T [128 keys x 256 query-heads] = K . Q^T as two tcgen05.mma
-//    kind::f8f6f4 (E4M3 x E4M3, K = 32 each) into one of two TMEM
-//    accumulators, so the MMA of tile i+1 overlaps the epilogue of tile i;
-//  - epilogue (16 warps): TMEM lane = key, 4 consecutive columns = the 4
-//    heads of one query, so score = sum_h w_h * max(x_h, 0) stays inside a
-//    thread;
-//    keys at or beyond the query's kv_len become -inf; each warp store writes
-//    32 consecutive keys of one query (128 B).
-// Key tiles beyond every query's kv_len skip the MMA and store -inf.  The
-// scores are fp32 [B, T, N]: this kernel is bound by writing them.
-//
-// The same main loop has a second epilogue, the first pass of the fused dense
-// indexer (csa2_index_topk_dense) that never writes the score matrix:
-// BLOCKMAX keeps the order-preserving key of each 8-key block's maximum
-// score.  Three xor-shuffle steps reduce over the 8 lanes (= keys) of a block
-// and transpose at the same time (each step keeps half of the queries), so
-// one 32-lane store writes the 8 queries x 4 blocks of a warp.
+// 64-query tile, range of 128-key tiles), taken by a persistent CTA per SM in
+// a static order.  The CTA is warp-specialised:
+//  - warp 16 (producer) streams the operand tiles with TMA tensor copies into
+//    shared memory, 64-byte swizzled (the layout tcgen05 reads directly): the
+//    item's query tile (256 query-head rows x 64 B, FP8) into one of two Q
+//    buffers, then its key tiles (128 keys x 64 B) through an 8-stage ring;
+//    full / empty mbarriers per buffer;
+//  - warp 17 (MMA) issues S^T [128 keys x 256 query-heads] = K . Q^T as two
+//    tcgen05.mma kind::f8f6f4 (E4M3 x E4M3, K = 32 each) into one of two TMEM
+//    accumulators and commits the key stage (empty) and the accumulator
+//    (full) to mbarriers;
+//  - warps 0..15 (epilogue) drain an accumulator while the next one fills:
+//    TMEM lane = key, 4 consecutive columns = the 4 heads of one query, so
+//    score = sum_h w_h * max(x_h, 0) stays inside a thread; keys at or beyond
+//    the query's kv_len become -inf.  Each warp owns a TMEM lane quarter and
+//    16 queries, read 8 queries (32 columns) at a time.
+// Key tiles at or beyond every query's kv_len are neither loaded nor
+// multiplied (SCORES writes -inf there).  Two epilogues share the pipeline:
+//  SCORES   writes fp32 [B, T, N]; each warp store covers 32 consecutive keys
+//           of one query (128 B);
+//  BLOCKMAX (first pass of the fused dense indexer csa2_index_topk_dense,
+//           which never writes the score matrix) keeps the order-preserving
+//           key of each 8-key block's maximum score.  Three xor-shuffle steps
+//           reduce over the 8 lanes (= keys) of a block and transpose at the
+//           same time (each step keeps half of the queries), so one 32-lane
+//           store writes the 8 queries x 4 blocks of a warp.
+// Every mbarrier wait is bounded; a thread that gives up raises a shared
+// abort word that every other wait polls, so all roles leave their loops,
+// the producer waits (bounded) for the copies it issued, and the CTA frees
+// its TMEM and returns with CSA2_FLAG_TIMEOUT set.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "tc.cuh"
 
@@ -40,31 +50,34 @@ constexpr int QT = 64;                 // queries per tile
 constexpr int QR = QT * 4;             // query-head rows (MMA N)
 constexpr int KT = 128;                // keys per tile (MMA M)
 constexpr int KTILES_PER_ITEM = 16;    // key tiles per work item
-constexpr int STAGES = 8;
-constexpr int THREADS = 512;             // 16 warps: 4 per TMEM lane quarter
+constexpr int STAGES = 8;              // key-tile ring
+constexpr int EPI_WARPS = 16;          // 4 per TMEM lane quarter
+constexpr int PRODUCER_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
+constexpr int THREADS = (EPI_WARPS + 2) * 32;
 constexpr uint32_t Q_BYTES = QR * 64;           // 16 KB
 constexpr uint32_t K_BYTES = KT * 64;           // 8 KB per stage
-constexpr uint32_t SBO = 4 * 128;               // 8-row group stride (64 B rows = 4 core matrices)
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-constexpr uint32_t OFF_W = OFF_K + STAGES * K_BYTES;  // float[QT][4]
-constexpr uint32_t OFF_LT = OFF_W + QT * 16;          // int2[QT]: (kv_len clamped to N, 0)
-constexpr uint32_t OFF_BAR = OFF_LT + QT * 8;         // 2 mbarriers
-constexpr uint32_t OFF_TMEM = OFF_BAR + 16;
-constexpr uint32_t OFF_SMAX = OFF_TMEM + 8;              // int[2]: longest kv_len of the tile's queries
-constexpr uint32_t SMEM_USED = OFF_SMAX + 8;
-// request more than half of the SM's shared memory: one CTA per SM, so the
-// CTA's 512 TMEM columns are never contended
-constexpr uint32_t SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+constexpr uint32_t SW_SBO = 8 * 64;             // 64-byte swizzle: 8-row atoms of 512 bytes
+// shared memory, from a 1024-byte aligned base
+constexpr uint32_t OFF_K = 0;
+constexpr uint32_t OFF_Q = OFF_K + STAGES * K_BYTES;     // 2 query tiles
+constexpr uint32_t OFF_W = OFF_Q + 2 * Q_BYTES;          // float[QT][4]
+constexpr uint32_t OFF_LT = OFF_W + QT * 16;             // int2[QT]: (kv_len clamped to N, 0)
+constexpr uint32_t OFF_BAR = OFF_LT + QT * 8;            // mbarriers, see below
+constexpr int NBARS = 2 * STAGES + 8;
+constexpr uint32_t OFF_TMEM = OFF_BAR + NBARS * 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM + 4;
+constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
+// Ask for more than half of the SM's shared memory: one CTA per SM, so the
+// CTA's 512 TMEM columns are never contended.  +1024 for the base alignment.
+constexpr uint32_t SMEM = (SMEM_USED + 1024) > 120 * 1024 ? (SMEM_USED + 1024) : 120 * 1024;
 constexpr uint32_t TMEM_COLS = 512;                   // 2 accumulators x 256 columns
 constexpr uint32_t MAX_POLLS = 1u << 22;
+static_assert(OFF_Q % 1024 == 0 && K_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzled tiles are 1024-aligned");
 
 struct PrefillArgs {
     int B, T;
     int64_t N;
-    const uint8_t *q;
     const float *w;
-    const uint8_t *k;
     const int32_t *kv_len;
     float *scores;
     uint32_t *err_flag;
@@ -75,38 +88,137 @@ struct PrefillArgs {
     int64_t nblk;
 };
 
-// sum_h w_h * max(x_h, 0) with every rounding spelled out, so that each pass
-// computes the same fp32 value.
-__device__ __forceinline__ float head_sum(const float4 wq, const uint32_t *r) {
-    float s = __fmul_rn(wq.x, fmaxf(__uint_as_float(r[0]), 0.f));
-    s = __fmaf_rn(wq.y, fmaxf(__uint_as_float(r[1]), 0.f), s);
-    s = __fmaf_rn(wq.z, fmaxf(__uint_as_float(r[2]), 0.f), s);
-    return __fmaf_rn(wq.w, fmaxf(__uint_as_float(r[3]), 0.f), s);
+// Twice sum_h w_h * max(x_h, 0), rounding step by step in the order
+// w_0 m_0, + w_1 m_1, + w_2 m_2, + w_3 m_3.  x + |x| is exactly 2 max(x, 0)
+// (one add with an absolute-value operand, off the integer/compare pipe), and
+// scaling every operand of a rounding by 2 scales its result by 2 exactly
+// (short of overflow or subnormal results), so half of this is that sum.
+__device__ __forceinline__ float head_sum2(const float4 wq, const uint32_t *r) {
+    auto relu2 = [](uint32_t v) { const float x = __uint_as_float(v); return __fadd_rn(x, fabsf(x)); };
+    float s = __fmul_rn(wq.x, relu2(r[0]));
+    s = __fmaf_rn(wq.y, relu2(r[1]), s);
+    s = __fmaf_rn(wq.z, relu2(r[2]), s);
+    return __fmaf_rn(wq.w, relu2(r[3]), s);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0));
+// K-major operand tile in the 64-byte swizzled canonical layout (rows of 64
+// bytes, 8-row atoms of 512 bytes, as the TMA writes it with SWIZZLE_64B).
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;                        // leading byte offset: unused for swizzled K-major
+    d |= (uint64_t)((SW_SBO >> 4) & 0x3FFF) << 32;  // stride byte offset: one 8-row atom
+    d |= (uint64_t)1 << 46;                        // descriptor version for sm_100-family
+    d |= (uint64_t)4 << 61;                        // swizzle mode: 64-byte
+    return d;
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Named barrier over the 16 epilogue warps only.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory"); }
+
+// Bounded wait that also gives up once another thread has raised the abort word.
+// sleep_ns > 0 backs off between polls, so that a waiting producer or MMA warp
+// leaves the issue slots of its scheduler to the epilogue warps that share it.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_word,
+                                              uint32_t sleep_ns = 0) {
+    for (uint32_t i = 0; i < MAX_POLLS; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (sleep_ns) __nanosleep(sleep_ns);
+        if ((i & 63) == 63 && *abort_word) return false;
+    }
+    *abort_word = 1;
+    return false;
+}
+
+// Work item -> (sequence, query tile, key-tile range) and the longest visible
+// prefix among the tile's queries (one warp; every lane gets the result).
+struct Item {
+    int64_t b;
+    int t0, kt0, kt1, ntiles;   // ntiles: key tiles [kt0, kt0 + ntiles) hold a visible key
+    int minlen;                 // shortest visible prefix (0 if the tile has fewer than 64 queries)
+};
+__device__ __forceinline__ Item item_of(const PrefillArgs &a, int64_t item, int lane) {
+    Item it;
+    const int kr = (int)(item % a.kranges);
+    const int64_t rest = item / a.kranges;
+    const int qt = (int)(rest % a.qtiles);
+    it.b = rest / a.qtiles;
+    it.t0 = qt * QT;
+    it.kt0 = kr * KTILES_PER_ITEM;
+    it.kt1 = min(a.ktiles, it.kt0 + KTILES_PER_ITEM);
+    int m = 0, mn = 0x7FFFFFFF;
+#pragma unroll
+    for (int u = 0; u < QT / 32; ++u) {
+        const int tq = it.t0 + lane + 32 * u;
+        int l = 0;
+        if (tq < a.T) {
+            const int64_t len = (int64_t)a.kv_len[it.b * a.T + tq];
+            l = (int)(len < 0 ? 0 : (len < a.N ? len : a.N));
+        }
+        m = max(m, l);
+        mn = min(mn, l);
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    it.minlen = __reduce_min_sync(0xFFFFFFFFu, mn);
+    const int vis = (m + KT - 1) / KT;   // key tiles with a visible key
+    it.ntiles = max(0, min(it.kt1, vis) - it.kt0);
+    return it;
+}
 
 template <int EPI>
-__global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(PrefillArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(THREADS, 1)
+    index_score_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                                  PrefillArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float *sW = reinterpret_cast<float *>(smem + OFF_W);
     const float4 *sW4 = reinterpret_cast<const float4 *>(smem + OFF_W);
+    float *sW = reinterpret_cast<float *>(smem + OFF_W);
     int2 *sLT = reinterpret_cast<int2 *>(smem + OFF_LT);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
-    int *sMax = reinterpret_cast<int *>(smem + OFF_SMAX);
-    const uint32_t bar0 = tc::smem_u32(smem + OFF_BAR);
-    const uint32_t sq = tc::smem_u32(smem + OFF_Q), sk = tc::smem_u32(smem + OFF_K);
+    volatile int *abort_word = reinterpret_cast<volatile int *>(smem + OFF_ABORT);
+    const uint32_t sbase = tc::smem_u32(smem);
+    const uint32_t bar0 = sbase + OFF_BAR;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull = [&](int j) { return bar0 + 8u * (2 * STAGES + j); };
+    auto tempty = [&](int j) { return bar0 + 8u * (2 * STAGES + 2 + j); };
+    auto qfull = [&](int j) { return bar0 + 8u * (2 * STAGES + 4 + j); };
+    auto qempty = [&](int j) { return bar0 + 8u * (2 * STAGES + 6 + j); };
     const float NEG_INF = __int_as_float(0xff800000);
 
     if (tid == 0) {
-        tc::mbar_init(bar0, 1);
-        tc::mbar_init(bar0 + 8, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(full(s), 1);
+            tc::mbar_init(empty(s), 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            tc::mbar_init(tfull(j), 1);
+            tc::mbar_init(tempty(j), EPI_WARPS);
+            tc::mbar_init(qfull(j), 1);
+            tc::mbar_init(qempty(j), 1);
+        }
+        *abort_word = 0;
         tc::mbar_init_fence();
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -116,172 +228,170 @@ __global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(Pref
     const uint32_t tmem = *tmem_slot;
     pdl_wait();
     pdl_launch_dependents();
-    uint32_t uses0 = 0, uses1 = 0;   // completed phases of the two accumulator barriers
-    bool ok = true;
 
-    for (int64_t item = blockIdx.x; item < a.items; item += gridDim.x) {
-        const int kr = (int)(item % a.kranges);
-        const int64_t rest = item / a.kranges;
-        const int qt = (int)(rest % a.qtiles);
-        const int64_t b = rest / a.qtiles;
-        const int t0 = qt * QT;
-        const int kt0 = kr * KTILES_PER_ITEM;
-        const int kt1 = min(a.ktiles, kt0 + KTILES_PER_ITEM);
-
-        // ---- query tile (rows r = 4*query + head) and its w / kv_len
-        __syncthreads();   // the previous item's epilogue reads of sW / sLT are done
-        for (int c = tid; c < QR * 4; c += THREADS) {
-            const int r = c >> 2, ch = c & 3, tq = t0 + (r >> 2);
-            const bool v = tq < a.T;
-            const uint8_t *src = a.q + ((b * a.T + (v ? tq : 0)) * 4 + (r & 3)) * 64 + ch * 16;
-            cp_async16(sq + (r >> 3) * SBO + ch * 128 + (r & 7) * 16, src, v);
-        }
-        if (tid < QT) {   // warps 0 and 1
-            const int tq = t0 + tid;
-            const bool v = tq < a.T;
-            const int64_t row = b * a.T + (v ? tq : 0);
-            for (int h = 0; h < 4; ++h) sW[tid * 4 + h] = v ? a.w[row * 4 + h] : 0.f;
-            int64_t len = v ? (int64_t)a.kv_len[row] : 0;
-            const int lc = (int)(len < 0 ? 0 : (len < a.N ? len : a.N));
-            sLT[tid] = make_int2(lc, 0);
-            const int m = __reduce_max_sync(0xFFFFFFFFu, lc);
-            if (lane == 0) sMax[warp] = m;
-        }
-        cp_commit();
-        int maxlen = 0;   // longest visible prefix among the tile's queries, read after the first barrier
-
-        auto load_ktile = [&](int kt, int stage) {
-            for (int c = tid; c < KT * 4; c += THREADS) {
-                const int r = c >> 2, ch = c & 3;
-                const int64_t key = (int64_t)kt * KT + r;
-                const bool v = key < a.N;
-                const uint8_t *src = a.k + ((b * a.N + (v ? key : 0)) * 64) + ch * 16;
-                cp_async16(sk + stage * K_BYTES + (r >> 3) * SBO + ch * 128 + (r & 7) * 16, src, v);
+    if (warp == PRODUCER_WARP) {
+        // ---- TMA: the item's query tile, then its visible key tiles through the ring
+        uint32_t kcount = 0, qcount = 0;
+        bool run = true;
+        for (int64_t item = blockIdx.x; run && item < a.items; item += gridDim.x) {
+            const Item it = item_of(a, item, lane);
+            const int qb = qcount & 1;
+            if (!wait_or_abort(qempty(qb), ((qcount >> 1) & 1) ^ 1, abort_word, 256)) break;
+            if (lane == 0) {
+                mbar_expect_tx(qfull(qb), Q_BYTES);
+                tma_load_2d(sbase + OFF_Q + qb * Q_BYTES, &qmap, 0, (int)((it.b * a.T + it.t0) * 4), qfull(qb));
             }
-            cp_commit();
-        };
-        // prologue: STAGES-1 key tiles in flight
-        for (int i = 0; i < STAGES - 1; ++i) {
-            if (kt0 + i < kt1) load_ktile(kt0 + i, i);
-            else cp_commit();
+            ++qcount;
+            for (int i = 0; i < it.ntiles; ++i) {
+                const int s = kcount % STAGES;
+                if (!wait_or_abort(empty(s), ((kcount / STAGES) & 1) ^ 1, abort_word, 256)) {
+                    run = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_expect_tx(full(s), K_BYTES);
+                    tma_load_2d(sbase + OFF_K + s * K_BYTES, &kmap, 0, (int)(it.b * a.N + (int64_t)(it.kt0 + i) * KT),
+                                full(s));
+                }
+                ++kcount;
+            }
         }
-
-        int prev_tile = -1, prev_buf = 0;
-        bool prev_mma = false;
-        // Epilogue of one key tile: warp w reads TMEM lane quarter w & 3 (32
-        // keys, lane = key) and the columns of queries 16 (w >> 2) .. +15.
-        auto epilogue = [&](int tile, int buf, bool did_mma) {
-            const int lq = warp & 3, qg = warp >> 2;
-            const int64_t key = (int64_t)tile * KT + 32 * lq + lane;
-            const int64_t row0 = b * a.T + t0 + 16 * qg;
-            if (did_mma) {
-                const uint32_t u = buf ? uses1 : uses0;
-                ok = tc::mbar_wait(bar0 + 8 * buf, u & 1, MAX_POLLS) && ok;
-                if (buf) ++uses1; else ++uses0;
+        if (*abort_word) {
+            // copies still in flight land before the CTA leaves (bounded)
+            for (uint32_t c = kcount > STAGES ? kcount - STAGES : 0; c < kcount; ++c)
+                tc::mbar_wait(full(c % STAGES), (c / STAGES) & 1, MAX_POLLS);
+            for (uint32_t c = qcount > 2 ? qcount - 2 : 0; c < qcount; ++c)
+                tc::mbar_wait(qfull(c & 1), (c >> 1) & 1, MAX_POLLS);
+        }
+    } else if (warp == MMA_WARP) {
+        // ---- tcgen05: two K = 32 MMAs per key tile into alternating accumulators
+        constexpr uint32_t idesc = tc::idesc_e4m3_f32(KT, QR, false, false);
+        uint32_t kcount = 0, qcount = 0, acount = 0;
+        bool run = true;
+        for (int64_t item = blockIdx.x; run && item < a.items; item += gridDim.x) {
+            const Item it = item_of(a, item, lane);
+            const int qb = qcount & 1;
+            if (!wait_or_abort(qfull(qb), (qcount >> 1) & 1, abort_word, 64)) break;
+            tc::fence_after();
+            const uint32_t qaddr = sbase + OFF_Q + qb * Q_BYTES;
+            for (int i = 0; i < it.ntiles; ++i) {
+                const int s = kcount % STAGES, buf = acount & 1;
+                if (!wait_or_abort(full(s), (kcount / STAGES) & 1, abort_word, 64) ||
+                    !wait_or_abort(tempty(buf), ((acount >> 1) & 1) ^ 1, abort_word, 64)) {
+                    run = false;
+                    break;
+                }
                 tc::fence_after();
+                if (lane == 0) {
+                    const uint32_t kaddr = sbase + OFF_K + s * K_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks)
+                        tc::mma_f8(tmem + buf * 256, desc_sw64(kaddr + ks * 32), desc_sw64(qaddr + ks * 32), idesc,
+                                   ks > 0);
+                    tc::commit(empty(s));
+                    tc::commit(tfull(buf));
+                }
+                __syncwarp();
+                ++kcount;
+                ++acount;
             }
-            // A skipped tile has no visible key for any query of the tile:
-            // nothing to write for the block maxima.
-            if (EPI != EPI_SCORES && !did_mma) return;
-            const uint32_t ta = tmem + ((uint32_t)(32 * lq) << 16) + buf * 256 + 64 * qg;
-            // eight queries of this warp's sixteen, from 32 TMEM columns.
-            // Straight-line over the eight (queries past T have kv_len 0 in
-            // sLT, so they are invalid without a branch): the independent
-            // chains interleave.
-            auto eight = [&](const uint32_t (&r)[32], int h) {
-                const int q0 = 16 * qg + 8 * h;
-                float s[8];
-#pragma unroll
-                for (int qq = 0; qq < 8; ++qq) {
-                    const float4 wq = sW4[q0 + qq];
-                    const int2 lt = sLT[q0 + qq];
-                    s[qq] = (did_mma && key < lt.x) ? head_sum(wq, r + 4 * qq) : NEG_INF;
+            if (lane == 0) tc::commit(qempty(qb));   // the query tile is free once these MMAs are done
+            __syncwarp();
+            ++qcount;
+        }
+    } else {
+        // ---- epilogue: warp w reads TMEM lane quarter w & 3 (32 keys, lane =
+        // key) and the columns of queries 16 (w >> 2) .. +15, eight at a time
+        const int lq = warp & 3, qg = warp >> 2;
+        uint32_t acount = 0;
+        bool run = true;
+        for (int64_t item = blockIdx.x; run && item < a.items; item += gridDim.x) {
+            const Item it = item_of(a, item, lane);
+            epi_sync();   // the previous item's reads of sW / sLT are done
+            if (tid < QT) {
+                const int tq = it.t0 + tid;
+                const bool v = tq < a.T;
+                const int64_t row = it.b * a.T + (v ? tq : 0);
+                for (int h = 0; h < 4; ++h) sW[tid * 4 + h] = v ? a.w[row * 4 + h] : 0.f;
+                const int64_t len = v ? (int64_t)a.kv_len[row] : 0;
+                sLT[tid] = make_int2((int)(len < 0 ? 0 : (len < a.N ? len : a.N)), 0);
+            }
+            epi_sync();
+            const int64_t row0 = it.b * a.T + it.t0 + 16 * qg;
+            for (int kt = it.kt0; kt < it.kt1; ++kt) {
+                const bool did = kt - it.kt0 < it.ntiles;
+                // a tile past every query's kv_len has nothing for the block maxima
+                if (EPI != EPI_SCORES && !did) continue;
+                const int buf = acount & 1;
+                if (did) {
+                    if (!wait_or_abort(tfull(buf), (acount >> 1) & 1, abort_word)) {
+                        run = false;
+                        break;
+                    }
+                    tc::fence_after();
                 }
-                const int64_t rowh = row0 + 8 * h;
-                const int nq = a.T - (t0 + q0);   // queries of these eight that exist
-                if constexpr (EPI == EPI_SCORES) {
-                    if (key < a.N) {
-#pragma unroll
-                        for (int qq = 0; qq < 8; ++qq)
-                            if (qq < nq) a.scores[(rowh + qq) * a.N + key] = s[qq];
-                    }
-                } else if constexpr (EPI == EPI_BLOCKMAX) {
-                    // Max over the 8 keys of each block, transposed on the way:
-                    // at each xor step a lane keeps half of its queries and
-                    // takes the partner's values for them.  Lane l ends with
-                    // the block max of query 4 b0 + 2 b1 + b2 (b = bits of l)
-                    // over keys 8 (l >> 3) .. +7 of its 32: one store for all.
-                    const bool b0 = lane & 1, b1 = (lane >> 1) & 1, b2 = (lane >> 2) & 1;
-                    float x[4], y[2];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float send = b0 ? s[j] : s[4 + j], keep = b0 ? s[4 + j] : s[j];
-                        x[j] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 1));
-                    }
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const float send = b1 ? x[j] : x[2 + j], keep = b1 ? x[2 + j] : x[j];
-                        y[j] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2));
-                    }
-                    const float send = b2 ? y[0] : y[1], keep = b2 ? y[1] : y[0];
-                    const float m = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 4));
-                    const int qs = 4 * b0 + 2 * b1 + b2;
-                    const int64_t blk = (key - lane + 8 * (lane >> 3)) >> 3;   // this lane's block
-                    if (qs < nq && 8 * blk < a.N) a.bmax[(rowh + qs) * a.nblk + blk] = score_key(m);
-                }
-            };
-            if constexpr (EPI == EPI_SCORES) {
-                // one half at a time: the store addresses need the registers
+                const int64_t key = (int64_t)kt * KT + 32 * lq + lane;
+                // every key of the tile is below every query's kv_len (<= N): no mask
+                const bool whole = did && (int64_t)(kt + 1) * KT <= it.minlen;
+                const uint32_t ta = tmem + ((uint32_t)(32 * lq) << 16) + buf * 256 + 64 * qg;
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     uint32_t r[32];
-                    if (did_mma) {
+                    if (did) {
                         tc::tmem_ld32(ta + 32 * h, r);
                         tc::tmem_ld_wait();
+                        if (h == 1) {   // both halves are in registers: the accumulator is free
+                            tc::fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(tempty(buf));
+                        }
                     }
-                    eight(r, h);
-                }
-            } else {
-                uint32_t r0[32], r1[32];
-                tc::tmem_ld32(ta, r0);
-                tc::tmem_ld32(ta + 32, r1);
-                tc::tmem_ld_wait();
-                eight(r0, 0);
-                eight(r1, 1);
-            }
-        };
-
-        for (int kt = kt0; kt < kt1; ++kt) {
-            const int i = kt - kt0;
-            cp_wait<STAGES - 2>();      // tile kt (and the query tile) have landed
-            tc::fence_async_smem();
-            tc::fence_before();
-            __syncthreads();
-            tc::fence_after();
-            const int buf = i & 1;
-            if (i == 0) maxlen = max(sMax[0], sMax[1]);
-            const bool do_mma = (int64_t)kt * KT < maxlen;
-            if (tid == 0 && do_mma) {
-                constexpr uint32_t idesc = tc::idesc_e4m3_f32(KT, QR, false, false);
-                const uint32_t ka = sk + (i % STAGES) * K_BYTES;
+                    const int q0 = 16 * qg + 8 * h;
+                    float s[8];   // twice the scores (halved below: at the store, or once per block maximum)
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-                    tc::mma_f8(tmem + buf * 256, tc::desc_noswizzle(ka + ks * 256, 128, SBO),
-                               tc::desc_noswizzle(sq + ks * 256, 128, SBO), idesc, ks > 0);
-                tc::commit(bar0 + 8 * buf);
+                    for (int qq = 0; qq < 8; ++qq) {
+                        float v = head_sum2(sW4[q0 + qq], r + 4 * qq);
+                        if (!whole && !(did && key < sLT[q0 + qq].x)) v = NEG_INF;
+                        s[qq] = v;
+                    }
+                    const int64_t rowh = row0 + 8 * h;
+                    const int nq = a.T - (it.t0 + q0);   // queries of these eight that exist
+                    if constexpr (EPI == EPI_SCORES) {
+                        if (key < a.N) {
+#pragma unroll
+                            for (int qq = 0; qq < 8; ++qq)
+                                if (qq < nq) a.scores[(rowh + qq) * a.N + key] = 0.5f * s[qq];
+                        }
+                    } else {
+                        // Max over the 8 keys of each block, transposed on the way:
+                        // at each xor step a lane keeps half of its queries and
+                        // takes the partner's values for them.  Lane l ends with
+                        // the block max of query 4 b0 + 2 b1 + b2 (b = bits of l)
+                        // over keys 8 (l >> 3) .. +7 of its 32: one store for all.
+                        const bool b0 = lane & 1, b1 = (lane >> 1) & 1, b2 = (lane >> 2) & 1;
+                        float x[4], y[2];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float send = b0 ? s[j] : s[4 + j], keep = b0 ? s[4 + j] : s[j];
+                            x[j] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 1));
+                        }
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const float send = b1 ? x[j] : x[2 + j], keep = b1 ? x[2 + j] : x[j];
+                            y[j] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2));
+                        }
+                        const float send = b2 ? y[0] : y[1], keep = b2 ? y[1] : y[0];
+                        const float m = 0.5f * fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 4));
+                        const int qs = 4 * b0 + 2 * b1 + b2;
+                        const int64_t blk = (key - lane + 8 * (lane >> 3)) >> 3;   // this lane's block
+                        if (qs < nq && 8 * blk < a.N) a.bmax[(rowh + qs) * a.nblk + blk] = score_key(m);
+                    }
+                }
+                if (did) ++acount;
             }
-            if (prev_tile >= 0) epilogue(prev_tile, prev_buf, prev_mma);   // also frees stage (i-1)%STAGES
-            __syncthreads();
-            if (kt + STAGES - 1 < kt1) load_ktile(kt + STAGES - 1, (i + STAGES - 1) % STAGES);
-            else cp_commit();
-            prev_tile = kt;
-            prev_buf = buf;
-            prev_mma = do_mma;
         }
-        if (prev_tile >= 0) epilogue(prev_tile, prev_buf, prev_mma);
-        cp_wait<0>();
     }
-    if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
+    if (*abort_word && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -292,11 +402,50 @@ __global__ void __launch_bounds__(THREADS, 1) index_score_prefill_tc_kernel(Pref
 
 bool index_score_prefill_tc_supported(int T, csa2_dtype dt) { return dt == CSA2_FP8_E4M3 && T >= 64; }
 
-static PrefillArgs prefill_args(int B, int T, int64_t N, const void *q, const float *w, const void *k,
-                                const int32_t *kv_len, uint32_t *err_flag) {
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// A tensor map over `rows` rows of 64 bytes (FP8 vectors of the indexer) with
+// boxes of box_rows rows, 64-byte swizzled in shared memory; rows past the end
+// read as zero.
+static csa2_status rows64_map(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_rows, const char *what) {
+    const EncodeTiledFn f = encode_tiled();
+    if (!f) {
+        set_error("%s: cuTensorMapEncodeTiled is not available from the driver", what);
+        return CSA2_ERR_CUDA;
+    }
+    const cuuint64_t dims[2] = {64, rows};
+    const cuuint64_t strides[1] = {64};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("%s: cuTensorMapEncodeTiled failed (%d)", what, (int)r);
+        return CSA2_ERR_CUDA;
+    }
+    return CSA2_OK;
+}
+
+static PrefillArgs prefill_args(int B, int T, int64_t N, const float *w, const int32_t *kv_len, uint32_t *err_flag) {
     PrefillArgs a = {};
     a.B = B; a.T = T; a.N = N;
-    a.q = (const uint8_t *)q; a.w = w; a.k = (const uint8_t *)k; a.kv_len = kv_len;
+    a.w = w; a.kv_len = kv_len;
     a.err_flag = err_flag;
     a.qtiles = (T + QT - 1) / QT;
     a.ktiles = (int)((N + KT - 1) / KT);
@@ -306,13 +455,24 @@ static PrefillArgs prefill_args(int B, int T, int64_t N, const void *q, const fl
 }
 
 template <int EPI>
-static csa2_status launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
+static csa2_status launch_prefill(const PrefillArgs &a, const void *q, const void *k, cudaStream_t stream) {
+    if (a.items == 0) return CSA2_OK;
+    // TMA row coordinates are 32-bit
+    if ((int64_t)a.B * a.T * 4 + QR > 0x7FFFFFFF || (int64_t)a.B * a.N + KT > 0x7FFFFFFF) {
+        set_error("index_score_prefill_tc: B*T*4 or B*N beyond 2^31 rows");
+        return CSA2_ERR_UNSUPPORTED;
+    }
+    CUtensorMap qm, km;
+    csa2_status st = rows64_map(&qm, q, (uint64_t)a.B * a.T * 4, QR, "index_score_prefill_tc (q)");
+    if (st != CSA2_OK) return st;
+    st = rows64_map(&km, k, (uint64_t)a.B * a.N, KT, "index_score_prefill_tc (k)");
+    if (st != CSA2_OK) return st;
     static bool smem_set[64];
     CSA2_CUDA_CALL(ensure_smem_limit((const void *)index_score_prefill_tc_kernel<EPI>, (int)SMEM, smem_set),
                    "index_score_prefill_tc: smem attribute");
-    int64_t grid = a.items < num_sms() ? a.items : num_sms();
+    const int64_t grid = a.items < num_sms() ? a.items : num_sms();
     CSA2_CUDA_CALL(launch_pdl(index_score_prefill_tc_kernel<EPI>, dim3((unsigned)grid), dim3(THREADS), SMEM, stream,
-                              a),
+                              qm, km, a),
                    "index_score_prefill_tc_kernel launch");
     CSA2_LAUNCH_CHECK("index_score_prefill_tc_kernel");
     return CSA2_OK;
@@ -321,19 +481,18 @@ static csa2_status launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
 csa2_status launch_index_score_prefill_tc(int B, int T, int64_t N, const void *q, const float *w, const void *k,
                                           const int32_t *kv_len, float *scores, uint32_t *err_flag,
                                           cudaStream_t stream) {
-    PrefillArgs a = prefill_args(B, T, N, q, w, k, kv_len, err_flag);
+    PrefillArgs a = prefill_args(B, T, N, w, kv_len, err_flag);
     a.scores = scores;
-    return launch_prefill<EPI_SCORES>(a, stream);
+    return launch_prefill<EPI_SCORES>(a, q, k, stream);
 }
 
 csa2_status launch_prefill_block_max(int B, int T, int64_t N, const void *q, const float *w, const void *k,
                                      const int32_t *kv_len, uint32_t *bmax, int64_t nblk, uint32_t *err_flag,
                                      cudaStream_t stream) {
-    PrefillArgs a = prefill_args(B, T, N, q, w, k, kv_len, err_flag);
+    PrefillArgs a = prefill_args(B, T, N, w, kv_len, err_flag);
     a.bmax = bmax;
     a.nblk = nblk;
-    return launch_prefill<EPI_BLOCKMAX>(a, stream);
+    return launch_prefill<EPI_BLOCKMAX>(a, q, k, stream);
 }
-
 
 }  // namespace csa2
