@@ -115,6 +115,7 @@ struct TcArgs {
     // optional L2 prefetch: the same selected rows of another pair of FP4 planes
     const uint8_t *pf_codes;
     const uint8_t *pf_scales;
+    int64_t items;   // token kernel: (token, 64-head block) items, taken in turn by persistent CTAs
 };
 
 // 16 E4M3 bytes -> 16 f16 (exact), as 8 f16x2 words.
@@ -757,7 +758,8 @@ constexpr uint32_t TK_OFF_PART = TK_OFF_CS + HB * 4;           // float[4][64] p
 constexpr uint32_t TK_OFF_M = TK_OFF_PART + 4 * HB * 4;        // float[64] running max (log2 domain)
 constexpr uint32_t TK_OFF_L = TK_OFF_M + HB * 4;               // float[64] running sum
 constexpr uint32_t TK_OFF_ALPHA = TK_OFF_L + HB * 4;           // float[64] rescale factor of this tile
-constexpr uint32_t TK_SMEM = TK_OFF_ALPHA + HB * 4;
+constexpr uint32_t TK_OFF_ILP = TK_OFF_ALPHA + HB * 4;         // float[64] 1 / L of the previous item
+constexpr uint32_t TK_SMEM = TK_OFF_ILP + HB * 4;
 constexpr uint32_t TK_S_COL = 0, TK_O_COL = HB;                // S^T: 64 columns; O^T: 4 x 64
 constexpr float TK_MAX_SLACK = 8.f;                            // P <= 2^8 between rescales
 static_assert((HB / 8) * 128 == KT_SBO - TK_P_IN_GROUP, "P fills the rotary channels of an 8-entry group");
@@ -800,10 +802,6 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t bt = blockIdx.x / a.hblocks;
-    const int hblk = (int)(blockIdx.x - bt * a.hblocks);
-    const int64_t b = bt / a.T;
-    const int h0 = hblk * HB;
     const int ntiles = (a.K + TM - 1) / TM;
 
     uint8_t *sK = smem + TK_OFF_K;
@@ -816,6 +814,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
     float *sM = reinterpret_cast<float *>(smem + TK_OFF_M);
     float *sL = reinterpret_cast<float *>(smem + TK_OFF_L);
     float *sAlpha = reinterpret_cast<float *>(smem + TK_OFF_ALPHA);
+    float *sILp = reinterpret_cast<float *>(smem + TK_OFF_ILP);
     const uint32_t bar_q = tc::smem_u32(smem + TK_OFF_BAR);   // Q rows landed
     const uint32_t bar_s = bar_q + 8;                           // S MMAs of a tile done
     const uint32_t bar_o = bar_q + 16;                          // P V MMAs of a tile done
@@ -841,23 +840,35 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
     __syncthreads();
     pdl_wait();   // the set-up above overlaps the previous kernel's tail
 
-    // the Q rows (one bulk copy per head row, issuers spread over the warps), then the entries' rows
-    if ((tid & 7) == 0) {
-        const int hr = tid >> 3;
-        mbar_arrive_expect_tx(bar_q, D * 2);
-        bulk_g2s(tc::smem_u32(smem + OFF_QRAW + hr * QRAW_STRIDE), a.q + ((bt * a.H) + h0 + hr) * (int64_t)D, D * 2,
-                 bar_q);
-    }
-    {
-        int64_t len = a.kv_len ? (int64_t)a.kv_len[bt] : a.N;
-        len = len < a.N ? len : a.N;
-        for (int i = tid; i < ntiles * TM; i += THREADS) {
-            const int64_t j = (i < a.K) ? (int64_t)__ldg(a.idx + bt * a.K + i) : -1;
-            const bool v = j >= 0 && j < len;
-            if (!v && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
-            sRow[i] = v ? b * a.N + j : -1;
+    // item -> (token bt, sequence b, first head h0)
+    int64_t item = blockIdx.x, bt, b;
+    int h0;
+    auto coords = [&](int64_t it, int64_t &bt_, int64_t &b_, int &h0_) {
+        bt_ = it / a.hblocks;
+        h0_ = (int)(it - bt_ * a.hblocks) * HB;
+        b_ = bt_ / a.T;
+    };
+    // the Q rows of an item: one bulk copy per head row, issuers spread over the warps
+    auto issue_q = [&](int64_t bt_, int h0_) {
+        if ((tid & 7) == 0) {
+            const int hr = tid >> 3;
+            mbar_arrive_expect_tx(bar_q, D * 2);
+            bulk_g2s(tc::smem_u32(smem + OFF_QRAW + hr * QRAW_STRIDE), a.q + ((bt_ * a.H) + h0_ + hr) * (int64_t)D,
+                     D * 2, bar_q);
         }
-    }
+    };
+    // the KV row of this thread's selected entry (entry tid < ntiles * TM <= THREADS), -1 if none
+    auto row_of = [&](int64_t bt_, int64_t b_) -> int64_t {
+        int64_t len = a.kv_len ? (int64_t)a.kv_len[bt_] : a.N;
+        len = len < a.N ? len : a.N;
+        const int64_t j = (tid < a.K) ? (int64_t)__ldg(a.idx + bt_ * a.K + tid) : -1;
+        const bool v = j >= 0 && j < len;
+        if (!v && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
+        return v ? b_ * a.N + j : -1;
+    };
+    coords(item, bt, b, h0);
+    issue_q(bt, h0);
+    if (tid < ntiles * TM) sRow[tid] = row_of(bt, b);
     __syncthreads();
 
     // this thread's code and scale bytes of one tile, straight into registers
@@ -880,46 +891,6 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
             }
         }
     };
-    load_tile(0);
-
-    // ---- Q -> registers -> per-head power-of-two scale -> f16 core-matrix tile (as the cluster kernel)
-    bool ok = tc::mbar_wait(bar_q, 0, MAX_POLLS);
-    {
-        const int hq = 8 * (warp & 7) + (lane & 7), cpos = lane >> 3, c0 = 36 * (warp >> 3);
-        const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE + (c0 + cpos) * 16;
-        uint4 qv[9];
-#pragma unroll
-        for (int i = 0; i < 9; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + i * 64);
-        float mx = 0.f;
-#pragma unroll
-        for (int i = 0; i < 9; ++i) {
-            const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-        if (cpos == 0) atomicMax(sQmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
-        __syncthreads();   // also: every read of the Q staging (in the Khat region) is done
-        mx = __uint_as_float(sQmax[hq]);
-        const int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
-        int sh = 14 - e2;   // max |q| * 2^sh in [2^14, 2^15)
-        sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
-        const float up = ldexpf(1.0f, sh);
-        uint8_t *qdst = sQ + (hq >> 3) * Q_SBO + (hq & 7) * 16 + (c0 + cpos) * 128;
-#pragma unroll
-        for (int i = 0; i < 9; ++i) {
-            const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-            uint32_t o[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
-            *reinterpret_cast<uint4 *>(qdst + i * 512) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
-    }
-
     // dequantise channel groups dq + 4 j, j in [j0, j1), of entry de into the Khat tile
     uint8_t *kbase = sK + warp * KT_SBO + (lane >> 2) * 16;   // (de >> 3) == warp
     auto dequant = [&](auto j0_c, auto j1_c, bool valid, auto &&before_group) {
@@ -953,159 +924,242 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
                         tp > 0 || ks > 0);
     };
 
-    for (int t = 0; t < ntiles; ++t) {
-        // P V of tile t-1 is issued here: its first two channel blocks, then the
-        // other two a few MMAs at a time between thread 0's first groups (the issue
-        // waits on the tensor pipe).  Channels 0..255 are dequantised once the
-        // first two blocks have read them, the rest once all of it is done.
-        if (t > 0) {
-            if (tid == 0) {
-                pv_mmas(t - 1, 0, 0, TM / 16);
-                pv_mmas(t - 1, 1, 0, TM / 16);
-                tc::commit(bar_o1);
-            }
-            ok = tc::mbar_wait(bar_o1, (t - 1) & 1, MAX_POLLS) && ok;
-        }
-        tc::fence_after();
-        const bool valid = sRow[t * TM + de] >= 0;
-        dequant(std::integral_constant<int, 0>{}, std::integral_constant<int, 4>{}, valid, [&](int i) {
-            if (t > 0 && tid == 0) pv_mmas(t - 1, 2 + (i >> 1), (i & 1) * (TM / 32), ((i & 1) + 1) * (TM / 32));
-        });
-        if (t > 0 && tid == 0) tc::commit(bar_o);
-        tc::fence_async_smem();
-        tc::fence_before();
-        __syncthreads();
-        tc::fence_after();
-        if (t > 0) ok = tc::mbar_wait(bar_o, (t - 1) & 1, MAX_POLLS) && ok;
-        tc::fence_after();
-        // the first part's 16 MMAs, four before each of thread 0's first four later groups
-        dequant(std::integral_constant<int, 4>{}, std::integral_constant<int, 9>{}, valid, [&](int i) {
-            if (tid == 0 && i < 4)
-                for (int ks = KS_A * i / 4; ks < KS_A * (i + 1) / 4; ++ks)
-                    tc::mma_f16(tmem + TK_S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
-                                tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, ks > 0);
-        });
-        tc::fence_async_smem();
-        tc::fence_before();
-        __syncthreads();
-        tc::fence_after();
-        if (tid == 0) {
-            for (int ks = KS_A; ks < D / 16; ++ks)
-                tc::mma_f16(tmem + TK_S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
-                            tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, true);
-            tc::commit(bar_s);
-        }
-        if (t + 1 < ntiles) load_tile(t + 1);   // lands while this tile is finished
-        ok = tc::mbar_wait(bar_s, t & 1, MAX_POLLS) && ok;
-        tc::fence_after();
-
-        // logits of this warp's 32 entries x 16 heads; the tile's per-head maximum
-        uint32_t r[16];
-        tc::tmem_ld16(s_lane + TK_S_COL + 16 * hh, r);
-        tc::tmem_ld_wait();
-        const int ee = 32 * quarter + lane;
-        const bool v = ok && sRow[t * TM + ee] >= 0;
-        {
-            float z[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) z[jj] = v ? __uint_as_float(r[jj]) * sCs[16 * hh + jj] : -INFINITY;
-            const float m = lane_reduce16<true>(z, lane);
-            if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = m;
-        }
-        __syncthreads();
-        bool resc = false;
-        if (tid < HB) {
-            const float mt = fmaxf(fmaxf(sPart[tid], sPart[HB + tid]), fmaxf(sPart[2 * HB + tid], sPart[3 * HB + tid]));
-            const float mo = sM[tid];
-            float al = 1.f;
-            if (mt > mo + TK_MAX_SLACK) {   // also the first finite maximum (mo = -inf)
-                resc = mo != -INFINITY;
-                al = resc ? ex2(mo - mt) : 0.f;
-                sM[tid] = mt;
-                sL[tid] *= al;
-            }
-            sAlpha[tid] = al;
-        }
-        tc::fence_before();
-        const bool any_resc = __syncthreads_or(resc) != 0;
-        tc::fence_after();
-        if (any_resc) {   // O^T *= alpha per head column (P V of t-1 is complete)
-#pragma unroll 1
-            for (int mb = 0; mb < DV / 128; ++mb) {
-                uint32_t o[16];
-                const uint32_t ta = s_lane + TK_O_COL + mb * HB + 16 * hh;
-                tc::tmem_ld16(ta, o);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) o[jj] = __float_as_uint(__uint_as_float(o[jj]) * sAlpha[16 * hh + jj]);
-                tmem_st16(ta, o);
-            }
-            tmem_st_wait();
-        }
-        // P_t = 2^(z - M) in f16 into the rotary channels of the Khat tile (MN-major: 8 heads per 16 bytes); row sums
-        {
-            float pf[16];
-            uint32_t pk[8];
-#pragma unroll
-            for (int jj = 0; jj < 16; jj += 2) {
-                float p2[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int hd = 16 * hh + jj + u;
-                    const float mx = sM[hd];
-                    const float zz = __uint_as_float(r[jj + u]) * sCs[hd];
-                    p2[u] = (!v || mx == -INFINITY) ? 0.f : ex2(zz - mx);
-                }
-                const __half2 hp = __floats2half2_rn(p2[0], p2[1]);
-                pk[jj / 2] = *reinterpret_cast<const uint32_t *>(&hp);
-                const float2 back = __half22float2(hp);
-                pf[jj] = back.x;
-                pf[jj + 1] = back.y;
-            }
-            uint8_t *pdst = sK + (ee >> 3) * KT_SBO + TK_P_IN_GROUP + (ee & 7) * 16;
-            *reinterpret_cast<uint4 *>(pdst + (2 * hh) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4 *>(pdst + (2 * hh + 1) * 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            const float sum = lane_reduce16<false>(pf, lane);
-            if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = sum;
-        }
-        tc::fence_async_smem();
-        tc::fence_before();
-        __syncthreads();
-        tc::fence_after();
-        if (tid < HB) sL[tid] += (sPart[tid] + sPart[HB + tid]) + (sPart[2 * HB + tid] + sPart[3 * HB + tid]);
-    }
-    if (tid == 0) {   // P V of the last tile
-        for (int mb = 0; mb < DV / 128; ++mb) pv_mmas(ntiles - 1, mb, 0, TM / 16);
-        tc::commit(bar_o);
-    }
-    ok = tc::mbar_wait(bar_o, (ntiles - 1) & 1, MAX_POLLS) && ok;
-    tc::fence_after();
-    __syncthreads();   // sL complete
-    if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
-
-    // ---- out = O / L (lanes = 32 consecutive channels of one head per store), lse
-    {
-        float il[16];
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-            const float l = sL[16 * hh + jj];
-            il[jj] = l > 0.f ? 1.f / l : 0.f;
-        }
-        const int64_t hbase = (bt * a.H) + h0 + 16 * hh;
-#pragma unroll 1
-        for (int mb = 0; mb < DV / 128; ++mb) {
+    uint32_t cnt_q = 0, cnt_s = 0, cnt_o = 0, cnt_o1 = 0;   // completed phases waited on, per barrier
+    bool ok = true;
+    // out = O / L of the previous item, channel blocks [mb0, mb1) (lanes = 32
+    // consecutive channels of one head per store).  O stays in TMEM until the
+    // next item's first P V, so the stores of one item are spread over the
+    // next item's first tile.
+    int64_t prev_hbase = -1;   // first (token, head) row of the previous item, -1 if none
+    auto emit_out = [&](int mb0, int mb1) {
+        for (int mb = mb0; mb < mb1; ++mb) {
             uint32_t r[16];
             tc::tmem_ld16(s_lane + TK_O_COL + mb * HB + 16 * hh, r);
             tc::tmem_ld_wait();
             const int c = mb * 128 + 32 * quarter + lane;
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) a.out[(hbase + jj) * (int64_t)DV + c] = __uint_as_float(r[jj]) * il[jj];
+            for (int jj = 0; jj < 16; ++jj)
+                a.out[(prev_hbase + 16 * hh + jj) * (int64_t)DV + c] = __uint_as_float(r[jj]) * sILp[16 * hh + jj];
         }
-        if (a.lse && tid < HB) {
+    };
+    auto convert_q = [&]() {
+    // ---- Q -> registers -> per-head power-of-two scale -> f16 core-matrix tile (as the cluster kernel)
+        ok = tc::mbar_wait(bar_q, cnt_q & 1, MAX_POLLS) && ok;
+        ++cnt_q;
+        {
+            const int hq = 8 * (warp & 7) + (lane & 7), cpos = lane >> 3, c0 = 36 * (warp >> 3);
+            const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE + (c0 + cpos) * 16;
+            uint4 qv[9];
+#pragma unroll
+            for (int i = 0; i < 9; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + i * 64);
+            float mx = 0.f;
+#pragma unroll
+            for (int i = 0; i < 9; ++i) {
+                const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+            if (cpos == 0) atomicMax(sQmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
+            __syncthreads();   // also: every read of the Q staging (in the Khat region) is done
+            mx = __uint_as_float(sQmax[hq]);
+            const int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
+            int sh = 14 - e2;   // max |q| * 2^sh in [2^14, 2^15)
+            sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
+            const float up = ldexpf(1.0f, sh);
+            uint8_t *qdst = sQ + (hq >> 3) * Q_SBO + (hq & 7) * 16 + (c0 + cpos) * 128;
+#pragma unroll
+            for (int i = 0; i < 9; ++i) {
+                const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
+                *reinterpret_cast<uint4 *>(qdst + i * 512) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
+        }
+    };
+    for (;;) {   // the items of this CTA: blockIdx.x, + gridDim.x, ...
+        load_tile(0);
+        convert_q();
+        for (int t = 0; t < ntiles; ++t) {
+            // P V of tile t-1 is issued here: its first two channel blocks, then the
+            // other two a few MMAs at a time between thread 0's first groups (the issue
+            // waits on the tensor pipe).  Channels 0..255 are dequantised once the
+            // first two blocks have read them, the rest once all of it is done.
+            if (t > 0) {
+                if (tid == 0) {
+                    pv_mmas(t - 1, 0, 0, TM / 16);
+                    pv_mmas(t - 1, 1, 0, TM / 16);
+                    tc::commit(bar_o1);
+                }
+                ok = tc::mbar_wait(bar_o1, cnt_o1 & 1, MAX_POLLS) && ok;
+                ++cnt_o1;
+            }
+            tc::fence_after();
+            const bool valid = sRow[t * TM + de] >= 0;
+            if (t == 0 && prev_hbase >= 0) emit_out(0, 2);
+            dequant(std::integral_constant<int, 0>{}, std::integral_constant<int, 4>{}, valid, [&](int i) {
+                if (t > 0 && tid == 0) pv_mmas(t - 1, 2 + (i >> 1), (i & 1) * (TM / 32), ((i & 1) + 1) * (TM / 32));
+            });
+            if (t > 0 && tid == 0) tc::commit(bar_o);
+            tc::fence_async_smem();
+            tc::fence_before();
+            __syncthreads();
+            tc::fence_after();
+            if (t > 0) {
+                ok = tc::mbar_wait(bar_o, cnt_o & 1, MAX_POLLS) && ok;
+                ++cnt_o;
+            }
+            tc::fence_after();
+            if (t == 0 && prev_hbase >= 0) emit_out(2, 4);
+            // the first part's 16 MMAs, four before each of thread 0's first four later groups
+            dequant(std::integral_constant<int, 4>{}, std::integral_constant<int, 9>{}, valid, [&](int i) {
+                if (tid == 0 && i < 4)
+                    for (int ks = KS_A * i / 4; ks < KS_A * (i + 1) / 4; ++ks)
+                        tc::mma_f16(tmem + TK_S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
+                                    tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, ks > 0);
+            });
+            tc::fence_async_smem();
+            tc::fence_before();
+            __syncthreads();
+            tc::fence_after();
+            if (tid == 0) {
+                for (int ks = KS_A; ks < D / 16; ++ks)
+                    tc::mma_f16(tmem + TK_S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
+                                tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, true);
+                tc::commit(bar_s);
+            }
+            if (t + 1 < ntiles) load_tile(t + 1);   // lands while this tile is finished
+            ok = tc::mbar_wait(bar_s, cnt_s & 1, MAX_POLLS) && ok;
+            ++cnt_s;
+            tc::fence_after();
+
+
+            // logits of this warp's 32 entries x 16 heads; the tile's per-head maximum
+            uint32_t r[16];
+            tc::tmem_ld16(s_lane + TK_S_COL + 16 * hh, r);
+            tc::tmem_ld_wait();
+            const int ee = 32 * quarter + lane;
+            const bool v = ok && sRow[t * TM + ee] >= 0;
+            {
+                float z[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) z[jj] = v ? __uint_as_float(r[jj]) * sCs[16 * hh + jj] : -INFINITY;
+                const float m = lane_reduce16<true>(z, lane);
+                if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = m;
+            }
+            __syncthreads();
+            bool resc = false;
+            if (tid < HB) {
+                const float mt = fmaxf(fmaxf(sPart[tid], sPart[HB + tid]), fmaxf(sPart[2 * HB + tid], sPart[3 * HB + tid]));
+                const float mo = sM[tid];
+                float al = 1.f;
+                if (mt > mo + TK_MAX_SLACK) {   // also the first finite maximum (mo = -inf)
+                    resc = mo != -INFINITY;
+                    al = resc ? ex2(mo - mt) : 0.f;
+                    sM[tid] = mt;
+                    sL[tid] *= al;
+                }
+                sAlpha[tid] = al;
+            }
+            tc::fence_before();
+            const bool any_resc = __syncthreads_or(resc) != 0;
+            tc::fence_after();
+            if (any_resc) {   // O^T *= alpha per head column (P V of t-1 is complete)
+#pragma unroll 1
+                for (int mb = 0; mb < DV / 128; ++mb) {
+                    uint32_t o[16];
+                    const uint32_t ta = s_lane + TK_O_COL + mb * HB + 16 * hh;
+                    tc::tmem_ld16(ta, o);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) o[jj] = __float_as_uint(__uint_as_float(o[jj]) * sAlpha[16 * hh + jj]);
+                    tmem_st16(ta, o);
+                }
+                tmem_st_wait();
+            }
+            // P_t = 2^(z - M) in f16 into the rotary channels of the Khat tile (MN-major: 8 heads per 16 bytes); row sums
+            {
+                float pf[16];
+                uint32_t pk[8];
+#pragma unroll
+                for (int jj = 0; jj < 16; jj += 2) {
+                    float p2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int hd = 16 * hh + jj + u;
+                        const float mx = sM[hd];
+                        const float zz = __uint_as_float(r[jj + u]) * sCs[hd];
+                        p2[u] = (!v || mx == -INFINITY) ? 0.f : ex2(zz - mx);
+                    }
+                    const __half2 hp = __floats2half2_rn(p2[0], p2[1]);
+                    pk[jj / 2] = *reinterpret_cast<const uint32_t *>(&hp);
+                    const float2 back = __half22float2(hp);
+                    pf[jj] = back.x;
+                    pf[jj + 1] = back.y;
+                }
+                uint8_t *pdst = sK + (ee >> 3) * KT_SBO + TK_P_IN_GROUP + (ee & 7) * 16;
+                *reinterpret_cast<uint4 *>(pdst + (2 * hh) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(pdst + (2 * hh + 1) * 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                const float sum = lane_reduce16<false>(pf, lane);
+                if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = sum;
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            __syncthreads();
+            tc::fence_after();
+            if (tid < HB) sL[tid] += (sPart[tid] + sPart[HB + tid]) + (sPart[2 * HB + tid] + sPart[3 * HB + tid]);
+        }
+        if (tid == 0) {   // P V of the last tile
+            for (int mb = 0; mb < DV / 128; ++mb) pv_mmas(ntiles - 1, mb, 0, TM / 16);
+            tc::commit(bar_o);
+        }
+        ok = tc::mbar_wait(bar_o, cnt_o & 1, MAX_POLLS) && ok;
+        ++cnt_o;
+        tc::fence_after();
+        // 1 / L and lse of this item; its O is stored during the next item's first tile
+        if (tid < HB) {
             const float l = sL[tid], mx = sM[tid];
-            a.lse[(bt * a.H) + h0 + tid] = (l > 0.f && mx != -INFINITY) ? (mx + log2f(l)) * 0.6931471805599453f : -INFINITY;
+            sILp[tid] = l > 0.f ? 1.f / l : 0.f;
+            if (a.lse)
+                a.lse[(bt * a.H) + h0 + tid] = (l > 0.f && mx != -INFINITY) ? (mx + log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
+        prev_hbase = (bt * a.H) + h0;
+        // the next item's Q rows and indices are fetched now (the Khat region, which
+        // stages Q, is free once P V is done)
+        const int64_t nitem = item + gridDim.x;
+        const bool more = ok && nitem < a.items;
+        int64_t nbt = 0, nb = 0, nrow = -1;
+        int nh0 = 0;
+        if (more) {
+            coords(nitem, nbt, nb, nh0);
+            issue_q(nbt, nh0);
+            if (tid < ntiles * TM) nrow = row_of(nbt, nb);
+        }
+        tc::fence_before();
+        __syncthreads();   // sILp complete; every read of this item's sL and sM is done
+        tc::fence_after();
+        if (!more) {
+            emit_out(0, DV / 128);
+            break;
+        }
+        if (tid < ntiles * TM) sRow[tid] = nrow;
+        if (tid < HB) {
+            sQmax[tid] = 0u;
+            sM[tid] = -INFINITY;
+            sL[tid] = 0.f;
+        }
+        __syncthreads();
+        item = nitem;
+        bt = nbt;
+        b = nb;
+        h0 = nh0;
     }
+    if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -1154,11 +1208,8 @@ static csa2_status launch_tc_tokens(TcArgs &a, int B, cudaStream_t stream) {
                    "sparse_attn_tc_tokens: smem attribute");
     a.hblocks = a.H / HB;
     a.csize = 1;
-    const int64_t grid = (int64_t)B * a.T * a.hblocks;
-    if (grid > 0x7FFFFFFF) {
-        set_error("sparse_attn_tc_tokens: grid too large");
-        return CSA2_ERR_UNSUPPORTED;
-    }
+    a.items = (int64_t)B * a.T * a.hblocks;
+    const int64_t grid = a.items < num_sms() ? a.items : num_sms();   // persistent: one CTA per SM at most
     CSA2_CUDA_CALL(launch_pdl(sparse_attn_tc_tokens_kernel, dim3((unsigned)grid), dim3(THREADS), TK_SMEM, stream, a),
                    "sparse_attn_tc_tokens_kernel launch");
     CSA2_LAUNCH_CHECK("sparse_attn_tc_tokens_kernel");

@@ -345,6 +345,9 @@ def _attn_gpu(csa2, q, codes, scales, N, idx, kv_len, sm, dv, flag=None):
     ("full", 24, 2, 2000, 300, 64, 0.0),      # three tiles, the last one ragged, two tokens per row
     ("full", 40, 1, 900, 100, 128, 0.2),      # one tile, two head blocks
     ("full", 20, 1, 5000, 257, 128, 0.0),     # three tiles, one entry in the last
+    # more items than SMs: each persistent CTA takes several in turn
+    ("full", 320, 1, 3000, 300, 64, 0.1),
+    ("full", 160, 1, 2000, 200, 128, 0.0),
 ])
 def test_sparse_attn_matches_oracle(csa2, base, B, T, N, K, H, pad):
     w0 = gen.TINY_FULL_DECODE if base == "tiny" else gen.FULL_BATCHED_DECODE
