@@ -436,6 +436,13 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
     // 0-15: chunk warp, lanes 16-31: chunk warp + kWarps), off the chain of
     // dependent loads of each chunk
     const int32_t pre_blk = full ? -1 : pool_ids(warp + (lane >= 16 ? kWarps : 0), lane & 15);
+    // Reindex: the slice's checked pool block ids are kept in shared memory (the
+    // block-key area, unused without a pool to build), for the output ids
+    int32_t *sBlk = reinterpret_cast<int32_t *>(bkeys);
+    if (!full) {
+        const int cb = warp + (lane >= 16 ? kWarps : 0);
+        if (cb < nchunks) sBlk[cb * 16 + (lane & 15)] = pre_blk;
+    }
     // A warp scores its chunks (cb = warp, warp + kWarps, ...) in halves of 4
     // groups (64 candidates), software-pipelined over two register buffers:
     // the loads of half k + 1 are in flight while half k is scored.
@@ -443,7 +450,10 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
     int32_t chunk_blk = -1;   // Reindex, chunks past the first two: ids reloaded per chunk
     auto load_half = [&](int k, uint4 (&raw)[4][2], bool (&v)[4][2]) {
         const int it = k >> 1, cb = warp + kWarps * it, i0 = cb * 128 + 64 * (k & 1);
-        if (!full && it >= 2 && (k & 1) == 0) chunk_blk = lane < 16 ? pool_ids(cb, lane) : -1;
+        if (!full && it >= 2 && (k & 1) == 0) {
+            chunk_blk = lane < 16 ? pool_ids(cb, lane) : -1;
+            if (lane < 16 && cb < nchunks) sBlk[cb * 16 + lane] = chunk_blk;
+        }
         const int32_t ids = it < 2 ? pre_blk : chunk_blk;
         const int base_lane = (it < 2 ? 16 * (it & 1) : 0) + 8 * (k & 1);
 #pragma unroll
@@ -528,15 +538,15 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
     }
 
     // ---------------------------------------------------------------- Top-K
-    auto global_id = [&](int64_t li) -> int32_t {   // candidate li of the row -> entry position
-        if (full) return (int32_t)li;
-        return (int32_t)((int64_t)__ldg(a.pool_in + row * a.P + li / 8) * 8 + (li & 7));
+    auto global_id = [&](int i) -> int32_t {   // candidate beg + i of the row -> entry position
+        if (full) return (int32_t)(beg + i);
+        return sBlk[i >> 3] * 8 + (i & 7);      // beg is a multiple of 128
     };
     uint32_t T, kk;
     cluster_select<C>(cluster, cta, sm, keys, nm4, full ? len : a.M, a.K, T, kk);
     pdl_launch_dependents();
     cluster_compact<C>(cluster, cta, sm, keys, nm, T, kk, a.K, a.idx + row * (int64_t)a.K,
-                       [&](int i) { return global_id(beg + i); });
+                       [&](int i) { return global_id(i); });
 }
 
 // Keys per CTA and dynamic shared memory for a split of the rows over C CTAs.
