@@ -402,24 +402,24 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint64_t da_s = tc::desc_noswizzle(a0s, 128, KT_SBO), db_s = tc::desc_noswizzle(b0s, 128, Q_SBO);
     // the first half's 18 MMAs, issued by thread 0 a few at a time between its
     // own second-half groups (four of them), so that the issue does not hold
     // its warp back while the tensor pipe drains
     dequant_half(1, [&](int i) {
         if (tid == 0 && i < 4)
+#pragma unroll
             for (int ks = (D / 32) * i / 4; ks < (D / 32) * (i + 1) / 4; ++ks)
-                tc::mma_f16(tmem + S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
-                            tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, ks > 0);
+                tc::mma_f16(tmem + S_COL, tc::desc_at(da_s, ks * 256), tc::desc_at(db_s, ks * 256), idesc_s, ks > 0);
     });
     tc::fence_async_smem();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     if (tid == 0) {
-#pragma unroll 2
+#pragma unroll
         for (int ks = D / 32; ks < D / 16; ++ks)
-            tc::mma_f16(tmem + S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
-                        tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, true);
+            tc::mma_f16(tmem + S_COL, tc::desc_at(da_s, ks * 256), tc::desc_at(db_s, ks * 256), idesc_s, true);
         tc::commit(bar_s);
     }
     ok = tc::mbar_wait(bar_s, 0, MAX_POLLS) && ok;
@@ -494,13 +494,15 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     const int W = DV / S;                      // channels per owner
     const int bpo = W / 128;                   // blocks per owner
     if (tid == 0) {
-        const uint32_t a0 = tc::smem_u32(sK), b0 = tc::smem_u32(sP);
+        const uint64_t da = tc::desc_noswizzle(tc::smem_u32(sK), KT_SBO, 128),
+                       db = tc::desc_noswizzle(tc::smem_u32(sP), 128, P_SBO);
         constexpr uint32_t idesc = tc::idesc_f16_f32(TM, HB, true, false);
+#pragma unroll
         for (int mb = 0; mb < DV / 128; ++mb)
 #pragma unroll
             for (int ks = 0; ks < TM / 16; ++ks)
-                tc::mma_f16(tmem + O_COL + mb * HB, tc::desc_noswizzle(a0 + ks * 2 * KT_SBO + mb * 16 * 128, KT_SBO, 128),
-                            tc::desc_noswizzle(b0 + ks * 256, 128, P_SBO), idesc, ks > 0);
+                tc::mma_f16(tmem + O_COL + mb * HB, tc::desc_at(da, ks * 2 * KT_SBO + mb * 16 * 128),
+                            tc::desc_at(db, ks * 256), idesc, ks > 0);
         tc::commit(bar_o);
     }
     if (S > 1) {   // every CTA runs: publish this CTA's (max, sum) per head in every CTA of the cluster
@@ -916,12 +918,15 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
     constexpr int KS_A = 16;   // groups 0..15 (channels 0..255: the value blocks P V reads first) go first
     const uint32_t s_lane = tmem + ((uint32_t)(32 * quarter) << 16);
 
+    // operand descriptors: one base each, advanced by constant offsets per MMA
+    const uint64_t da_s = tc::desc_noswizzle(a0s, 128, KT_SBO), db_s = tc::desc_noswizzle(b0s, 128, Q_SBO);
+    const uint64_t da_o = tc::desc_noswizzle(a0s, KT_SBO, 128), db_o = tc::desc_noswizzle(a0s + TK_P_IN_GROUP, KT_SBO, 128);
     // P V of tile tp, value channel block mb, entry steps [ks0, ks1): O^T += Vhat^T . P^T
     auto pv_mmas = [&](int tp, int mb, int ks0, int ks1) {
+#pragma unroll
         for (int ks = ks0; ks < ks1; ++ks)
-            tc::mma_f16(tmem + TK_O_COL + mb * HB, tc::desc_noswizzle(a0s + ks * 2 * KT_SBO + mb * 16 * 128, KT_SBO, 128),
-                        tc::desc_noswizzle(a0s + ks * 2 * KT_SBO + TK_P_IN_GROUP, KT_SBO, 128), idesc_o,
-                        tp > 0 || ks > 0);
+            tc::mma_f16(tmem + TK_O_COL + mb * HB, tc::desc_at(da_o, ks * 2 * KT_SBO + mb * 16 * 128),
+                        tc::desc_at(db_o, ks * 2 * KT_SBO), idesc_o, tp > 0 || ks > 0);
     };
 
     uint32_t cnt_q = 0, cnt_s = 0, cnt_o = 0, cnt_o1 = 0;   // completed phases waited on, per barrier
@@ -1019,18 +1024,19 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
             // the first part's 16 MMAs, four before each of thread 0's first four later groups
             dequant(std::integral_constant<int, 4>{}, std::integral_constant<int, 9>{}, valid, [&](int i) {
                 if (tid == 0 && i < 4)
+#pragma unroll
                     for (int ks = KS_A * i / 4; ks < KS_A * (i + 1) / 4; ++ks)
-                        tc::mma_f16(tmem + TK_S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
-                                    tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, ks > 0);
+                        tc::mma_f16(tmem + TK_S_COL, tc::desc_at(da_s, ks * 256), tc::desc_at(db_s, ks * 256), idesc_s,
+                                    ks > 0);
             });
             tc::fence_async_smem();
             tc::fence_before();
             __syncthreads();
             tc::fence_after();
             if (tid == 0) {
+#pragma unroll
                 for (int ks = KS_A; ks < D / 16; ++ks)
-                    tc::mma_f16(tmem + TK_S_COL, tc::desc_noswizzle(a0s + ks * 256, 128, KT_SBO),
-                                tc::desc_noswizzle(b0s + ks * 256, 128, Q_SBO), idesc_s, true);
+                    tc::mma_f16(tmem + TK_S_COL, tc::desc_at(da_s, ks * 256), tc::desc_at(db_s, ks * 256), idesc_s, true);
                 tc::commit(bar_s);
             }
             if (t + 1 < ntiles) load_tile(t + 1);   // lands while this tile is finished
