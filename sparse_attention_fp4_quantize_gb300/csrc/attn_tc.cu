@@ -957,14 +957,18 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
             uint4 qv[9];
 #pragma unroll
             for (int i = 0; i < 9; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + i * 64);
-            float mx = 0.f;
+            // max |q| on the bf16 bit patterns: a finite magnitude orders as its 15 low bits
+            // (two per word, compared as unsigned 16-bit halves); four independent chains
+            uint32_t m4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int i = 0; i < 9; ++i) {
                 const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
+                for (int k = 0; k < 4; ++k) m4[k] = __vmaxu2(m4[k], w4[k] & 0x7FFF7FFFu);
             }
+            uint32_t mb2 = __vmaxu2(__vmaxu2(m4[0], m4[1]), __vmaxu2(m4[2], m4[3]));
+            mb2 = max(mb2 & 0xFFFFu, mb2 >> 16);
+            float mx = __uint_as_float(mb2 << 16);
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
             if (cpos == 0) atomicMax(sQmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
