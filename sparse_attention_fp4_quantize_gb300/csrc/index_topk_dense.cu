@@ -64,8 +64,10 @@ __device__ __forceinline__ uint32_t warp_suffix(uint32_t v) {   // sum over lane
 // three radix passes over the digits [31:21], [20:10], [9:0].  Each pass
 // histograms the keys that share the prefix found so far (2048 shared bins,
 // shared atomics), then the thread whose 8 bins hold the K-th key from the
-// top publishes the bin.  scratch: at least RS_WARPS + 2 words.
-__device__ uint32_t block_kth_largest(const uint32_t *keys, int n, int K, uint32_t *hist, uint32_t *scratch) {
+// top publishes the bin.  scratch: at least RS_WARPS + 2 words.  n_greater:
+// the number of keys > the result (K less the keys equal to it that are needed).
+__device__ uint32_t block_kth_largest(const uint32_t *keys, int n, int K, uint32_t *hist, uint32_t *scratch,
+                                      uint32_t &n_greater) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t prefix = 0u, mask = 0u, k = (uint32_t)K;
 #pragma unroll 1
@@ -111,22 +113,24 @@ __device__ uint32_t block_kth_largest(const uint32_t *keys, int n, int K, uint32
         __syncthreads();   // scratch and the histogram are reused
         // the boundary bin is taken whole: exactly K keys are >= its lower
         // edge, so every key above edge - 1 is selected (prefix >= 2^21 here)
-        if (inbin == k) return prefix - 1u;
+        if (inbin == k) {
+            n_greater = (uint32_t)K;
+            return prefix - 1u;
+        }
     }
+    n_greater = (uint32_t)K - k;   // k keys equal to the result complete the K
     return prefix;
 }
 
 // Writes to out[0, K): every i < n with keys[i] > T, then keys[i] == T until K
 // are taken (T = 0: every nonzero key), then -1; pos(i) gives the output id.
+// above = the number of keys > T (known to the caller from the selection).
 // Slots come from one shared atomic per warp and 32 keys (ballots order the
 // lanes), so the writes never contend on a single counter lane by lane.
 template <typename PosFn>
-__device__ void block_emit(const uint32_t *keys, int n, uint32_t T, int K, int32_t *out, PosFn pos,
+__device__ void block_emit(const uint32_t *keys, int n, uint32_t T, uint32_t above, int K, int32_t *out, PosFn pos,
                            uint32_t *scratch) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t c = 0;
-    for (int i = tid; i < n; i += RS_THREADS) c += (keys[i] > T) ? 1u : 0u;
-    const uint32_t above = block_sum(c, scratch);   // < K unless T = 0 or the boundary bin was taken whole
     if (tid == 0) {
         scratch[RS_WARPS] = 0u;
         scratch[RS_WARPS + 1] = 0u;
@@ -199,8 +203,9 @@ __global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArg
         for (int i = tid; 4 * i < nb; i += RS_THREADS) cp_async16((uint32_t)__cvta_generic_to_shared(sBm + 4 * i), row + 4 * i);
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         __syncthreads();
-        const uint32_t tau = block_kth_largest(sBm, nb, a.K, hist, scratch);
-        block_emit(sBm, nb, tau, a.K, sBlk, [](int i) { return (int32_t)i; }, scratch);
+        uint32_t above;
+        const uint32_t tau = block_kth_largest(sBm, nb, a.K, hist, scratch, above);
+        block_emit(sBm, nb, tau, above, a.K, sBlk, [](int i) { return (int32_t)i; }, scratch);
         nsel = a.K;
     }
     __syncthreads();
@@ -252,8 +257,9 @@ __global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArg
     uint32_t nv = 0;
     for (int i = tid; i < m; i += RS_THREADS) nv += sSc[i] != 0u ? 1u : 0u;
     nv = block_sum(nv, scratch);
-    const uint32_t T = nv <= (uint32_t)a.K ? 0u : block_kth_largest(sSc, m, a.K, hist, scratch);
-    block_emit(sSc, m, T, a.K, out, [&](int i) { return sBlk[i >> 3] * 8 + (i & 7); }, scratch);
+    uint32_t above = nv;   // at most K candidates: every nonzero key
+    const uint32_t T = nv <= (uint32_t)a.K ? 0u : block_kth_largest(sSc, m, a.K, hist, scratch, above);
+    block_emit(sSc, m, T, above, a.K, out, [&](int i) { return sBlk[i >> 3] * 8 + (i & 7); }, scratch);
 }
 
 }  // namespace
