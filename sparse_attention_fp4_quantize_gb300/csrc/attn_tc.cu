@@ -873,9 +873,11 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
     if (tid < ntiles * TM) sRow[tid] = row_of(bt, b);
     __syncthreads();
 
-    // this thread's code and scale bytes of one tile, straight into registers
+    // this thread's code bytes of one tile, straight into registers, and three of
+    // the entry's nine scale words (dq, dq + 4 and, for dq = 0, 8): the four lanes
+    // of an entry share them by shuffles, so a warp load touches 8 rows once
     uint2 cw[9];
-    uint32_t sw[9];
+    uint32_t sw3[3], sw[9];
     auto load_tile = [&](int t) {
         const int64_t r = sRow[t * TM + de];
         if (r >= 0) {
@@ -883,15 +885,20 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
             const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + r * (D / 16));
 #pragma unroll
             for (int j = 0; j < 9; ++j) cw[j] = __ldg(crow + dq + 4 * j);
-#pragma unroll
-            for (int j = 0; j < 9; ++j) sw[j] = __ldg(srow + j);
+            sw3[0] = __ldg(srow + dq);
+            sw3[1] = __ldg(srow + 4 + dq);
+            sw3[2] = __ldg(srow + 8 - 8 * (dq != 0));   // word 8 for lane 0 (the others reload word 0, unused)
         } else {
 #pragma unroll
-            for (int j = 0; j < 9; ++j) {
-                cw[j] = make_uint2(0u, 0u);
-                sw[j] = 0u;
-            }
+            for (int j = 0; j < 9; ++j) cw[j] = make_uint2(0u, 0u);
+            sw3[0] = sw3[1] = sw3[2] = 0u;
         }
+    };
+    // the entry's nine scale words in every lane of the entry (word j from its lane j mod 4)
+    auto share_scales = [&]() {
+#pragma unroll
+        for (int j = 0; j < 9; ++j)
+            sw[j] = __shfl_sync(0xFFFFFFFFu, j < 4 ? sw3[0] : (j < 8 ? sw3[1] : sw3[2]), (lane & ~3) | (j & 3));
     };
     // dequantise channel groups dq + 4 j, j in [j0, j1), of entry de into the Khat tile
     uint8_t *kbase = sK + warp * KT_SBO + (lane >> 2) * 16;   // (de >> 3) == warp
@@ -1011,6 +1018,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
             tc::fence_after();
             const bool valid = sRow[t * TM + de] >= 0;
             if (t == 0 && prev_hbase >= 0) emit_out(0, 2);
+            share_scales();
             dequant(std::integral_constant<int, 0>{}, std::integral_constant<int, 4>{}, valid, [&](int i) {
                 if (t > 0 && tid == 0) pv_mmas(t - 1, 2 + (i >> 1), (i & 1) * (TM / 32), ((i & 1) + 1) * (TM / 32));
             });
