@@ -822,8 +822,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
     const uint32_t bar_o = bar_q + 16;                          // P V MMAs of a tile done
     const uint32_t bar_o1 = bar_q + 24;                         // its first two channel blocks done
 
-    // dequantisation: entry de of a tile, lane dq of its four; channel groups dq + 4 j
-    const int de = 8 * warp + (lane >> 2), dq = lane & 3;
+    // dequantisation: entry de of a tile, lane dq of its four (lanes e, e + 8, e + 16, e + 24:
+    // a quarter-warp holds eight entries, so its 16-byte tile stores meet every bank once);
+    // channel groups dq + 4 j
+    const int de = 8 * warp + (lane & 7), dq = lane >> 3;
     const int quarter = warp & 3, hh = warp >> 2;    // TMEM lane quarter, 16-head group
 
     if (tid == 0) {
@@ -894,14 +896,14 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
             sw3[0] = sw3[1] = sw3[2] = 0u;
         }
     };
-    // the entry's nine scale words in every lane of the entry (word j from its lane j mod 4)
+    // the entry's nine scale words in every lane of the entry (word j from its lane with dq = j mod 4)
     auto share_scales = [&]() {
 #pragma unroll
         for (int j = 0; j < 9; ++j)
-            sw[j] = __shfl_sync(0xFFFFFFFFu, j < 4 ? sw3[0] : (j < 8 ? sw3[1] : sw3[2]), (lane & ~3) | (j & 3));
+            sw[j] = __shfl_sync(0xFFFFFFFFu, j < 4 ? sw3[0] : (j < 8 ? sw3[1] : sw3[2]), (lane & 7) | ((j & 3) << 3));
     };
     // dequantise channel groups dq + 4 j, j in [j0, j1), of entry de into the Khat tile
-    uint8_t *kbase = sK + warp * KT_SBO + (lane >> 2) * 16;   // (de >> 3) == warp
+    uint8_t *kbase = sK + warp * KT_SBO + (lane & 7) * 16;   // (de >> 3) == warp
     auto dequant = [&](auto j0_c, auto j1_c, bool valid, auto &&before_group) {
         constexpr int j0 = decltype(j0_c)::value, j1 = decltype(j1_c)::value;
 #pragma unroll
