@@ -74,20 +74,21 @@ __device__ uint32_t block_kth_largest(const uint32_t *keys, int n, int K, uint32
     for (int pass = 0; pass < 3; ++pass) {
         const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
         const uint32_t dmask = pass == 2 ? 1023u : 2047u;
-        reinterpret_cast<uint4 *>(hist)[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4 *>(hist)[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4 *>(hist)[tid] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4 *>(hist)[tid + RS_THREADS] = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
         for (int i = tid; i < n; i += RS_THREADS) {
             const uint32_t key = keys[i];
             if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dmask], 1u);
         }
         __syncthreads();
-        uint32_t h[8], own = 0;   // this thread's bins 8 tid .. 8 tid + 7
+        // this thread's bins 8 tid .. 8 tid + 7, as two 16-byte reads (eight word
+        // reads at a stride of eight words would meet each bank eight times)
+        const uint4 ha = reinterpret_cast<const uint4 *>(hist)[2 * tid], hb = reinterpret_cast<const uint4 *>(hist)[2 * tid + 1];
+        const uint32_t h[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+        uint32_t own = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            h[j] = hist[8 * tid + j];
-            own += h[j];
-        }
+        for (int j = 0; j < 8; ++j) own += h[j];
         const uint32_t incl = warp_suffix(own);
         if (lane == 0) scratch[warp] = incl;   // warp totals
         __syncthreads();
