@@ -767,7 +767,6 @@ constexpr float TK_MAX_SLACK = 8.f;                            // P <= 2^8 betwe
 static_assert((HB / 8) * 128 == KT_SBO - TK_P_IN_GROUP, "P fills the rotary channels of an 8-entry group");
 static_assert(TK_O_COL + (DV / 128) * HB <= TMEM_COLS, "TMEM columns");
 static_assert(TK_SMEM <= 227 * 1024, "shared memory");
-static_assert(HB * QRAW_STRIDE <= KT_BYTES, "Q staging fits in the Khat region");
 
 // Reduce-scatter of 16 values over the 32 lanes of a warp: afterwards lanes l
 // and l ^ 1 both hold the reduction over all lanes of value (l >> 1) & 15.
@@ -852,24 +851,26 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
         h0_ = (int)(it - bt_ * a.hblocks) * HB;
         b_ = bt_ / a.T;
     };
-    // the Q rows of an item: one bulk copy per head row, issuers spread over the warps
+    // the Q rows of an item: one bulk copy per head row into the Q tile (bf16 rows of
+    // 1152 bytes, converted there in place), issuers spread over the warps
     auto issue_q = [&](int64_t bt_, int h0_) {
         if ((tid & 7) == 0) {
             const int hr = tid >> 3;
             mbar_arrive_expect_tx(bar_q, D * 2);
-            bulk_g2s(tc::smem_u32(smem + OFF_QRAW + hr * QRAW_STRIDE), a.q + ((bt_ * a.H) + h0_ + hr) * (int64_t)D,
-                     D * 2, bar_q);
+            bulk_g2s(tc::smem_u32(sQ + hr * (D * 2)), a.q + ((bt_ * a.H) + h0_ + hr) * (int64_t)D, D * 2, bar_q);
         }
     };
-    // the KV row of this thread's selected entry (entry tid < ntiles * TM <= THREADS), -1 if none
-    auto row_of = [&](int64_t bt_, int64_t b_) -> int64_t {
+    // the KV row of selected entry e of token bt_, -1 if none; bad indices flagged if asked
+    auto row_at = [&](int64_t bt_, int64_t b_, int e, bool flag) -> int64_t {
         int64_t len = a.kv_len ? (int64_t)a.kv_len[bt_] : a.N;
         len = len < a.N ? len : a.N;
-        const int64_t j = (tid < a.K) ? (int64_t)__ldg(a.idx + bt_ * a.K + tid) : -1;
+        const int64_t j = (e < a.K) ? (int64_t)__ldg(a.idx + bt_ * a.K + e) : -1;
         const bool v = j >= 0 && j < len;
-        if (!v && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
+        if (flag && !v && j != -1) flag_error(a.err_flag, CSA2_FLAG_BAD_INDEX);
         return v ? b_ * a.N + j : -1;
     };
+    // the KV row of this thread's selected entry (entry tid < ntiles * TM <= THREADS)
+    auto row_of = [&](int64_t bt_, int64_t b_) -> int64_t { return row_at(bt_, b_, tid, true); };
     coords(item, bt, b, h0);
     issue_q(bt, h0);
     if (tid < ntiles * TM) sRow[tid] = row_of(bt, b);
@@ -880,8 +881,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
     // of an entry share them by shuffles, so a warp load touches 8 rows once
     uint2 cw[9];
     uint32_t sw3[3], sw[9];
-    auto load_tile = [&](int t) {
-        const int64_t r = sRow[t * TM + de];
+    auto load_row = [&](int64_t r) {
         if (r >= 0) {
             const uint2 *crow = reinterpret_cast<const uint2 *>(a.codes + r * (D / 2));
             const uint32_t *srow = reinterpret_cast<const uint32_t *>(a.scales + r * (D / 16));
@@ -896,6 +896,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
             sw3[0] = sw3[1] = sw3[2] = 0u;
         }
     };
+    auto load_tile = [&](int t) { load_row(sRow[t * TM + de]); };
     // the entry's nine scale words in every lane of the entry (word j from its lane with dq = j mod 4)
     auto share_scales = [&]() {
 #pragma unroll
@@ -956,52 +957,60 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
                 a.out[(prev_hbase + 16 * hh + jj) * (int64_t)DV + c] = __uint_as_float(r[jj]) * sILp[16 * hh + jj];
         }
     };
+    // ---- Q (bf16 rows in the Q tile) -> registers -> per-head power-of-two scale -> the
+    // f16 core-matrix tile in place.  Thread (G = tid / 8, j = tid mod 8) takes row
+    // 8 (G mod 8) + j, chunks (j + G / 8) mod 8 + 8 k: the eight lanes of a quarter-warp
+    // read eight rows at eight chunk residues and write eight rows of one core matrix,
+    // so neither side meets a bank twice.  Every raw row is read before the barrier
+    // that publishes the maxima, and written over only after it.
     auto convert_q = [&]() {
-    // ---- Q -> registers -> per-head power-of-two scale -> f16 core-matrix tile (as the cluster kernel)
         ok = tc::mbar_wait(bar_q, cnt_q & 1, MAX_POLLS) && ok;
         ++cnt_q;
-        {
-            const int hq = 8 * (warp & 7) + (lane & 7), cpos = lane >> 3, c0 = 36 * (warp >> 3);
-            const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE + (c0 + cpos) * 16;
-            uint4 qv[9];
+        const int qG = tid >> 3, qj = tid & 7;
+        const int qh = 8 * (qG & 7) + qj, qc0 = (qj + (qG >> 3)) & 7;
+        uint4 qv[9];
 #pragma unroll
-            for (int i = 0; i < 9; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + i * 64);
-            // max |q| on the bf16 bit patterns: a finite magnitude orders as its 15 low bits
-            // (two per word, compared as unsigned 16-bit halves); four independent chains
-            uint32_t m4[4] = {0u, 0u, 0u, 0u};
+        for (int k = 0; k < 9; ++k) qv[k] = *reinterpret_cast<const uint4 *>(sQ + qh * (D * 2) + (qc0 + 8 * k) * 16);
+        // max |q| on the bf16 bit patterns: a finite magnitude orders as its 15 low bits
+        // (two per word, compared as unsigned 16-bit halves); four independent chains
+        uint32_t m4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int i = 0; i < 9; ++i) {
-                const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+        for (int k = 0; k < 9; ++k) {
+            const uint32_t w4[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) m4[k] = __vmaxu2(m4[k], w4[k] & 0x7FFF7FFFu);
-            }
-            uint32_t mb2 = __vmaxu2(__vmaxu2(m4[0], m4[1]), __vmaxu2(m4[2], m4[3]));
-            mb2 = max(mb2 & 0xFFFFu, mb2 >> 16);
-            float mx = __uint_as_float(mb2 << 16);
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-            if (cpos == 0) atomicMax(sQmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
-            __syncthreads();   // also: every read of the Q staging (in the Khat region) is done
-            mx = __uint_as_float(sQmax[hq]);
-            const int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
-            int sh = 14 - e2;   // max |q| * 2^sh in [2^14, 2^15)
-            sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
-            const float up = ldexpf(1.0f, sh);
-            uint8_t *qdst = sQ + (hq >> 3) * Q_SBO + (hq & 7) * 16 + (c0 + cpos) * 128;
-#pragma unroll
-            for (int i = 0; i < 9; ++i) {
-                const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-                uint32_t o[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
-                *reinterpret_cast<uint4 *>(qdst + i * 512) = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
+            for (int u = 0; u < 4; ++u) m4[u] = __vmaxu2(m4[u], w4[u] & 0x7FFF7FFFu);
         }
+        uint32_t mb2 = __vmaxu2(__vmaxu2(m4[0], m4[1]), __vmaxu2(m4[2], m4[3]));
+        mb2 = max(mb2 & 0xFFFFu, mb2 >> 16);
+        atomicMax(sQmax + qh, mb2 << 16);   // the float bits of |q|: bit order = value order
+        __syncthreads();
+        const float mx = __uint_as_float(sQmax[qh]);
+        const int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
+        int sh = 14 - e2;   // max |q| * 2^sh in [2^14, 2^15)
+        sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
+        const float up = ldexpf(1.0f, sh);
+        uint8_t *qdst = sQ + (qh >> 3) * Q_SBO + (qh & 7) * 16;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+            const uint32_t w4[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                o[u] = pack_f16x2(__uint_as_float(w4[u] << 16) * up, __uint_as_float(w4[u] & 0xFFFF0000u) * up);
+            *reinterpret_cast<uint4 *>(qdst + (qc0 + 8 * k) * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if (qG < 8) sCs[qh] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;   // x log2(e)
     };
+    bool tile0_loaded = false;
     for (;;) {   // the items of this CTA: blockIdx.x, + gridDim.x, ...
-        load_tile(0);
+        // the next item of this CTA, if any: the code rows of its first tile and its Q
+        // rows are fetched during this item's last tile
+        const int64_t nitem = item + gridDim.x;
+        const bool has_next = nitem < a.items;
+        int64_t nbt = 0, nb = 0;
+        int nh0 = 0;
+        if (has_next) coords(nitem, nbt, nb, nh0);
+        if (!tile0_loaded) load_tile(0);
         convert_q();
         for (int t = 0; t < ntiles; ++t) {
             // P V of tile t-1 is issued here: its first two channel blocks, then the
@@ -1053,10 +1062,14 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
                     tc::mma_f16(tmem + TK_S_COL, tc::desc_at(da_s, ks * 256), tc::desc_at(db_s, ks * 256), idesc_s, true);
                 tc::commit(bar_s);
             }
-            if (t + 1 < ntiles) load_tile(t + 1);   // lands while this tile is finished
+            if (t + 1 < ntiles)
+                load_tile(t + 1);   // lands while this tile is finished
+            else if (has_next)
+                load_row(row_at(nbt, nb, de, false));   // the next item's first tile
             ok = tc::mbar_wait(bar_s, cnt_s & 1, MAX_POLLS) && ok;
             ++cnt_s;
             tc::fence_after();
+            if (t + 1 == ntiles && has_next) issue_q(nbt, nh0);   // the Q tile is free once the last S is done
 
 
             // logits of this warp's 32 entries x 16 heads; the tile's per-head maximum
@@ -1149,21 +1162,15 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
                 a.lse[(bt * a.H) + h0 + tid] = (l > 0.f && mx != -INFINITY) ? (mx + log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
         prev_hbase = (bt * a.H) + h0;
-        // the next item's Q rows and indices are fetched now (the Khat region, which
-        // stages Q, is free once P V is done)
-        const int64_t nitem = item + gridDim.x;
-        const bool more = ok && nitem < a.items;
-        int64_t nbt = 0, nb = 0, nrow = -1;
-        int nh0 = 0;
-        if (more) {
-            coords(nitem, nbt, nb, nh0);
-            issue_q(nbt, nh0);
-            if (tid < ntiles * TM) nrow = row_of(nbt, nb);
-        }
+        int64_t nrow = -1;
+        if (has_next && tid < ntiles * TM) nrow = row_of(nbt, nb);
         tc::fence_before();
         __syncthreads();   // sILp complete; every read of this item's sL and sM is done
         tc::fence_after();
-        if (!more) {
+        if (!has_next || !ok) {
+            // (after a timeout the next item's Q copy is still waited for: no copy
+            // into this CTA's shared memory may be in flight when it exits)
+            if (has_next) (void)tc::mbar_wait(bar_q, cnt_q & 1, MAX_POLLS);
             emit_out(0, DV / 128);
             break;
         }
@@ -1178,6 +1185,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
         bt = nbt;
         b = nb;
         h0 = nh0;
+        tile0_loaded = true;
     }
     if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
     tc::fence_before();
