@@ -1164,10 +1164,12 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
         prev_hbase = (bt * a.H) + h0;
         int64_t nrow = -1;
         if (has_next && tid < ntiles * TM) nrow = row_of(nbt, nb);
+        // one decision for the whole CTA (a timeout in any thread ends its work); the
+        // barrier also completes sILp and every read of this item's sL and sM
         tc::fence_before();
-        __syncthreads();   // sILp complete; every read of this item's sL and sM is done
+        const bool stop = __syncthreads_or(!ok) != 0 || !has_next;
         tc::fence_after();
-        if (!has_next || !ok) {
+        if (stop) {
             // (after a timeout the next item's Q copy is still waited for: no copy
             // into this CTA's shared memory may be in flight when it exits)
             if (has_next) (void)tc::mbar_wait(bar_q, cnt_q & 1, MAX_POLLS);
