@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         bulk_commit();
     };
     if (S > 1) stage_slice(0);                 // overlaps the wait for the slowest CTA
-    if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
+    if (!ok) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);   // any thread whose wait gave up
     tc::fence_async_smem();
     tc::fence_before();
     cluster.sync();                            // every CTA's P V is done: its Khat region may be written
@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         // sparse branch's share
         ok = tc::mbar_wait(bar_rx, 0, MAX_POLLS) && ok;   // (no bytes expected: completes the phase)
         __syncthreads();                                   // the weights of the block above
-        if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
+        if (!ok) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);   // any thread whose wait gave up
         const int64_t hbase = (bt * a.H) + h0 + 16 * hh;
         // two 128-channel blocks at a time: their sparse-branch values are
         // loaded together, after the TMEM loads' wait
@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     if (tid == 0) bulk_wait_read0();           // staging reads done before this CTA may exit
     ok = tc::mbar_wait(bar_rx, 0, MAX_POLLS) && ok;   // the other CTAs' slices have landed
     __syncthreads();
-    if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
+    if (!ok) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);   // any thread whose wait gave up
 
     // ---- 7. combine this CTA's channel slice with the weights: its own part
     // straight from TMEM in fp32 (the TMEM lane mapping: lane = channel, 16
@@ -1189,7 +1189,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
         h0 = nh0;
         tile0_loaded = true;
     }
-    if (!ok && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
+    if (!ok) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);   // any thread whose wait gave up
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
