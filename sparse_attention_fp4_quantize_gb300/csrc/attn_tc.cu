@@ -729,12 +729,15 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
 // Many query tokens: one CTA per (token, 64 heads) over all of its K <= 512
 // selected entries in one pass with an online softmax, no cluster merge (used
 // when a launch has enough (token, head-block) items to fill the GPU on its
-// own, e.g. a prefill chunk).  512 threads; the same 128-entry tile and MMA
-// shapes as above.  Per 128-entry tile t:
-//  - the entry's 288 code bytes and 36 scale bytes were loaded into registers
-//    while tile t-1 was computed (tile 0: while Q was converted), 8 bytes of
-//    codes per thread and load, four lanes per entry, so one warp load touches
-//    8 rows with one 32-byte sector each;
+// own, e.g. a prefill chunk).  Persistent: at most one CTA per SM, taking the
+// items blockIdx.x, + gridDim.x, ...  512 threads; the same 128-entry tile
+// and MMA shapes as above.  Per 128-entry tile t:
+//  - the entry's 288 code bytes were loaded into registers while tile t-1
+//    was computed (the first tile of an item: during the previous item's last
+//    tile), 8 bytes per thread and load, four lanes per entry (lanes e,
+//    e + 8, e + 16, e + 24), so one warp load touches 8 rows with one 32-byte
+//    sector each and a quarter-warp's 16-byte tile stores cover 8 entries;
+//    each lane loads three of the entry's nine scale words, shared by shuffles;
 //  - the 576 channels are dequantised into the Khat tile in two parts:
 //    channels 0..255 once P V of tile t-1 has read its first two channel
 //    blocks (its last two still running), the rest once it is done, the first
@@ -746,8 +749,11 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
 //  - P_t in f16, laid out MN-major in the Khat tile's rotary channels (dead
 //    once S_t is done); O^T += Vhat_t^T . P_t^T into TMEM columns [64, 320)
 //    is issued at the start of tile t+1, ahead of its dequantisation.
-// Finally out = O / L and lse = (M + log2 L) ln 2 per head, L summed over the
-// f16-rounded P as the MMAs consumed it.
+// Once an item's last S is done the Q tile is free: the next item's Q rows
+// (bf16) are copied into it and, after the item's last P V, converted there
+// in place.  Finally out = O / L and lse = (M + log2 L) ln 2 per head, L
+// summed over the f16-rounded P as the MMAs consumed it; O stays in TMEM and
+// is stored during the next item's first tile.
 constexpr uint32_t TK_OFF_K = 0;
 constexpr uint32_t TK_OFF_Q = KT_BYTES;                        // Q tile
 constexpr uint32_t TK_P_IN_GROUP = (DV / 8) * 128;             // P: the rotary core matrices of each 8-entry group
