@@ -398,6 +398,252 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// BLOCKMAX with the queries on the TMEM lanes.  The same pipeline (a producer
+// warp, an MMA warp and 16 epilogue warps over two accumulators) with the MMA
+// transposed: per tile of 64 keys and per head h, D_h [128 queries x 64 keys]
+// = Q_h . K^T (two kind::f8f6f4 MMAs, M128 N64 K32) into TMEM columns
+// [256 buf + 64 h, +64).  An epilogue thread owns one query (its TMEM lane) and
+// 16 keys of every tile: the head sum of a (query, key) pair reads the four
+// heads' columns of its own lane and the maximum over a block of 8 keys stays
+// in the thread, so neither needs a shuffle, and the query's weights and row
+// length stay in registers for the whole work item.  The query tile arrives
+// as one 3D tensor copy per head (the heads of a row are 64 bytes apart).
+constexpr int BQ = 128;                          // queries per tile (MMA M: one TMEM lane each)
+constexpr int BK = 64;                           // keys per tile (MMA N)
+constexpr int BKTILES_PER_ITEM = 32;             // key tiles per work item (2048 keys)
+constexpr uint32_t BQ_HEAD_BYTES = BQ * 64;      // 8 KB: one head of the query tile
+constexpr uint32_t BQ_BYTES = 4 * BQ_HEAD_BYTES;
+constexpr uint32_t BK_BYTES = BK * 64;           // 4 KB per stage
+constexpr uint32_t BOFF_K = 0;
+constexpr uint32_t BOFF_Q = BOFF_K + STAGES * BK_BYTES;   // 2 query tiles
+constexpr uint32_t BOFF_BAR = BOFF_Q + 2 * BQ_BYTES;
+constexpr uint32_t BOFF_TMEM = BOFF_BAR + NBARS * 8;
+constexpr uint32_t BOFF_ABORT = BOFF_TMEM + 4;
+constexpr uint32_t BSMEM_USED = BOFF_ABORT + 4;
+constexpr uint32_t BSMEM = (BSMEM_USED + 1024) > 120 * 1024 ? (BSMEM_USED + 1024) : 120 * 1024;
+static_assert(BOFF_Q % 1024 == 0 && BK_BYTES % 1024 == 0 && BQ_HEAD_BYTES % 1024 == 0, "swizzled tiles are 1024-aligned");
+static_assert(4 * BK * 2 <= (int)TMEM_COLS, "two accumulators of four heads");
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+            "r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// Work item -> (sequence, 128-query tile, key-tile range) and the key tiles that
+// hold a key visible to one of its queries (one warp; every lane gets the result).
+struct BItem {
+    int64_t b;
+    int t0, kt0, ntiles;
+};
+__device__ __forceinline__ BItem bitem_of(const PrefillArgs &a, int64_t item, int lane) {
+    BItem it;
+    const int kr = (int)(item % a.kranges);
+    const int64_t rest = item / a.kranges;
+    const int qt = (int)(rest % a.qtiles);
+    it.b = rest / a.qtiles;
+    it.t0 = qt * BQ;
+    it.kt0 = kr * BKTILES_PER_ITEM;
+    const int kt1 = min(a.ktiles, it.kt0 + BKTILES_PER_ITEM);
+    int m = 0;
+#pragma unroll
+    for (int u = 0; u < BQ / 32; ++u) {
+        const int tq = it.t0 + lane + 32 * u;
+        if (tq < a.T) {
+            const int64_t len = (int64_t)a.kv_len[it.b * a.T + tq];
+            m = max(m, (int)(len < 0 ? 0 : (len < a.N ? len : a.N)));
+        }
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    it.ntiles = max(0, min(kt1, (m + BK - 1) / BK) - it.kt0);
+    return it;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    index_blockmax_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                             PrefillArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + BOFF_TMEM);
+    volatile int *abort_word = reinterpret_cast<volatile int *>(smem + BOFF_ABORT);
+    const uint32_t sbase = tc::smem_u32(smem);
+    const uint32_t bar0 = sbase + BOFF_BAR;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull = [&](int j) { return bar0 + 8u * (2 * STAGES + j); };
+    auto tempty = [&](int j) { return bar0 + 8u * (2 * STAGES + 2 + j); };
+    auto qfull = [&](int j) { return bar0 + 8u * (2 * STAGES + 4 + j); };
+    auto qempty = [&](int j) { return bar0 + 8u * (2 * STAGES + 6 + j); };
+    const float NEG_INF = __int_as_float(0xff800000);
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(full(s), 1);
+            tc::mbar_init(empty(s), 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            tc::mbar_init(tfull(j), 1);
+            tc::mbar_init(tempty(j), EPI_WARPS);
+            tc::mbar_init(qfull(j), 1);
+            tc::mbar_init(qempty(j), 1);
+        }
+        *abort_word = 0;
+        tc::mbar_init_fence();
+    }
+    if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+    pdl_launch_dependents();
+
+    if (warp == PRODUCER_WARP) {
+        // ---- TMA: the item's query tile (four heads), then its visible key tiles through the ring
+        uint32_t kcount = 0, qcount = 0;
+        bool run = true;
+        for (int64_t item = blockIdx.x; run && item < a.items; item += gridDim.x) {
+            const BItem it = bitem_of(a, item, lane);
+            const int qb = qcount & 1;
+            if (!wait_or_abort(qempty(qb), ((qcount >> 1) & 1) ^ 1, abort_word, 256)) break;
+            if (lane == 0) {
+                mbar_expect_tx(qfull(qb), BQ_BYTES);
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                    tma_load_3d(sbase + BOFF_Q + qb * BQ_BYTES + h * BQ_HEAD_BYTES, &qmap, 0, h,
+                                (int)(it.b * a.T + it.t0), qfull(qb));
+            }
+            ++qcount;
+            for (int i = 0; i < it.ntiles; ++i) {
+                const int s = kcount % STAGES;
+                if (!wait_or_abort(empty(s), ((kcount / STAGES) & 1) ^ 1, abort_word, 256)) {
+                    run = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_expect_tx(full(s), BK_BYTES);
+                    tma_load_2d(sbase + BOFF_K + s * BK_BYTES, &kmap, 0, (int)(it.b * a.N + (int64_t)(it.kt0 + i) * BK),
+                                full(s));
+                }
+                ++kcount;
+            }
+        }
+        if (*abort_word) {
+            // copies still in flight land before the CTA leaves (bounded)
+            for (uint32_t c = kcount > STAGES ? kcount - STAGES : 0; c < kcount; ++c)
+                tc::mbar_wait(full(c % STAGES), (c / STAGES) & 1, MAX_POLLS);
+            for (uint32_t c = qcount > 2 ? qcount - 2 : 0; c < qcount; ++c)
+                tc::mbar_wait(qfull(c & 1), (c >> 1) & 1, MAX_POLLS);
+        }
+    } else if (warp == MMA_WARP) {
+        // ---- tcgen05: per key tile and head, two K = 32 MMAs into the head's accumulator
+        constexpr uint32_t idesc = tc::idesc_e4m3_f32(BQ, BK, false, false);
+        uint32_t kcount = 0, qcount = 0, acount = 0;
+        bool run = true;
+        for (int64_t item = blockIdx.x; run && item < a.items; item += gridDim.x) {
+            const BItem it = bitem_of(a, item, lane);
+            const int qb = qcount & 1;
+            if (!wait_or_abort(qfull(qb), (qcount >> 1) & 1, abort_word, 64)) break;
+            tc::fence_after();
+            const uint32_t qaddr = sbase + BOFF_Q + qb * BQ_BYTES;
+            for (int i = 0; i < it.ntiles; ++i) {
+                const int s = kcount % STAGES, buf = acount & 1;
+                if (!wait_or_abort(full(s), (kcount / STAGES) & 1, abort_word, 64) ||
+                    !wait_or_abort(tempty(buf), ((acount >> 1) & 1) ^ 1, abort_word, 64)) {
+                    run = false;
+                    break;
+                }
+                tc::fence_after();
+                if (lane == 0) {
+                    const uint32_t kaddr = sbase + BOFF_K + s * BK_BYTES;
+#pragma unroll
+                    for (int h = 0; h < 4; ++h)
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks)
+                            tc::mma_f8(tmem + buf * 256 + h * BK, desc_sw64(qaddr + h * BQ_HEAD_BYTES + ks * 32),
+                                       desc_sw64(kaddr + ks * 32), idesc, ks > 0);
+                    tc::commit(empty(s));
+                    tc::commit(tfull(buf));
+                }
+                __syncwarp();
+                ++kcount;
+                ++acount;
+            }
+            if (lane == 0) tc::commit(qempty(qb));   // the query tile is free once these MMAs are done
+            __syncwarp();
+            ++qcount;
+        }
+    } else {
+        // ---- epilogue: warp w reads TMEM lane quarter w & 3 (32 queries, lane = query) and
+        // the 16 keys 16 (w >> 2) .. +15 of every tile, four heads of each
+        const int lq = warp & 3, kg = warp >> 2;
+        uint32_t acount = 0;
+        bool run = true;
+        for (int64_t item = blockIdx.x; run && item < a.items; item += gridDim.x) {
+            const BItem it = bitem_of(a, item, lane);
+            const int tq = it.t0 + 32 * lq + lane;   // this thread's query
+            const bool qv = tq < a.T;
+            const int64_t row = it.b * a.T + (qv ? tq : 0);
+            float4 wq = make_float4(0.f, 0.f, 0.f, 0.f);
+            int len = 0;   // N <= 2^18
+            if (qv) {
+                wq = make_float4(a.w[row * 4], a.w[row * 4 + 1], a.w[row * 4 + 2], a.w[row * 4 + 3]);
+                const int64_t l = (int64_t)a.kv_len[row];
+                len = (int)(l < 0 ? 0 : (l < a.N ? l : a.N));
+            }
+            uint32_t *brow = a.bmax + row * a.nblk;
+            for (int i = 0; i < it.ntiles; ++i) {
+                const int buf = acount & 1;
+                if (!wait_or_abort(tfull(buf), (acount >> 1) & 1, abort_word)) {
+                    run = false;
+                    break;
+                }
+                tc::fence_after();
+                uint32_t r[4][16];
+                const uint32_t ta = tmem + ((uint32_t)(32 * lq) << 16) + buf * 256 + 16 * kg;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) tc::tmem_ld16(ta + h * BK, r[h]);
+                tc::tmem_ld_wait();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty(buf));   // the accumulator is free
+                const int key0 = (it.kt0 + i) * BK + 16 * kg;
+                float m[2] = {NEG_INF, NEG_INF};
+                if (key0 + 16 <= len) {   // all of this thread's keys are visible to its query
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t hv[4] = {r[0][j], r[1][j], r[2][j], r[3][j]};
+                        m[j >> 3] = fmaxf(m[j >> 3], head_sum2(wq, hv));   // twice the score
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t hv[4] = {r[0][j], r[1][j], r[2][j], r[3][j]};
+                        const float v = key0 + j < len ? head_sum2(wq, hv) : NEG_INF;
+                        m[j >> 3] = fmaxf(m[j >> 3], v);
+                    }
+                }
+                if (qv) {
+                    const int blk = key0 >> 3;   // this thread's first block
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (8 * (int64_t)(blk + u) < a.N) brow[blk + u] = score_key(0.5f * m[u]);
+                }
+                ++acount;
+            }
+        }
+    }
+    if (*abort_word && tid == 0) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
 }  // namespace
 
 bool index_score_prefill_tc_supported(int T, csa2_dtype dt) { return dt == CSA2_FP8_E4M3 && T >= 64; }
@@ -433,6 +679,29 @@ static csa2_status rows64_map(CUtensorMap *m, const void *base, uint64_t rows, u
     const cuuint32_t box[2] = {64, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("%s: cuTensorMapEncodeTiled failed (%d)", what, (int)r);
+        return CSA2_ERR_CUDA;
+    }
+    return CSA2_OK;
+}
+
+// A tensor map over the query rows [rows][4 heads][64 bytes] as (64 bytes, head,
+// row), boxes of one head of box_rows rows, 64-byte swizzled in shared memory;
+// rows past the end read as zero.
+static csa2_status heads64_map(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_rows, const char *what) {
+    const EncodeTiledFn f = encode_tiled();
+    if (!f) {
+        set_error("%s: cuTensorMapEncodeTiled is not available from the driver", what);
+        return CSA2_ERR_CUDA;
+    }
+    const cuuint64_t dims[3] = {64, 4, rows};
+    const cuuint64_t strides[2] = {64, 256};
+    const cuuint32_t box[3] = {64, 1, box_rows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -492,7 +761,29 @@ csa2_status launch_prefill_block_max(int B, int T, int64_t N, const void *q, con
     PrefillArgs a = prefill_args(B, T, N, w, kv_len, err_flag);
     a.bmax = bmax;
     a.nblk = nblk;
-    return launch_prefill<EPI_BLOCKMAX>(a, q, k, stream);
+    a.qtiles = (T + BQ - 1) / BQ;
+    a.ktiles = (int)((N + BK - 1) / BK);
+    a.kranges = (a.ktiles + BKTILES_PER_ITEM - 1) / BKTILES_PER_ITEM;
+    a.items = (int64_t)B * a.qtiles * a.kranges;
+    if (a.items == 0) return CSA2_OK;
+    // TMA row coordinates are 32-bit
+    if ((int64_t)B * T + BQ > 0x7FFFFFFF || (int64_t)B * N + BK > 0x7FFFFFFF) {
+        set_error("index_blockmax_tc: B*T or B*N beyond 2^31 rows");
+        return CSA2_ERR_UNSUPPORTED;
+    }
+    CUtensorMap qm, km;
+    csa2_status st = heads64_map(&qm, q, (uint64_t)B * T, BQ, "index_blockmax_tc (q)");
+    if (st != CSA2_OK) return st;
+    st = rows64_map(&km, k, (uint64_t)B * N, BK, "index_blockmax_tc (k)");
+    if (st != CSA2_OK) return st;
+    static bool smem_set[64];
+    CSA2_CUDA_CALL(ensure_smem_limit((const void *)index_blockmax_tc_kernel, (int)BSMEM, smem_set),
+                   "index_blockmax_tc: smem attribute");
+    const int64_t grid = a.items < num_sms() ? a.items : num_sms();
+    CSA2_CUDA_CALL(launch_pdl(index_blockmax_tc_kernel, dim3((unsigned)grid), dim3(THREADS), BSMEM, stream, qm, km, a),
+                   "index_blockmax_tc_kernel launch");
+    CSA2_LAUNCH_CHECK("index_blockmax_tc_kernel");
+    return CSA2_OK;
 }
 
 }  // namespace csa2
