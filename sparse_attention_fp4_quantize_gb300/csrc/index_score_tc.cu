@@ -23,15 +23,13 @@
 //    the query's kv_len become -inf.  Each warp owns a TMEM lane quarter and
 //    16 queries, read 8 queries (32 columns) at a time.
 // Key tiles at or beyond every query's kv_len are neither loaded nor
-// multiplied (SCORES writes -inf there).  Two epilogues share the pipeline:
-//  SCORES   writes fp32 [B, T, N]; each warp store covers 32 consecutive keys
-//           of one query (128 B);
-//  BLOCKMAX (first pass of the fused dense indexer csa2_index_topk_dense,
-//           which never writes the score matrix) keeps the order-preserving
-//           key of each 8-key block's maximum score.  Three xor-shuffle steps
-//           reduce over the 8 lanes (= keys) of a block and transpose at the
-//           same time (each step keeps half of the queries), so one 32-lane
-//           store writes the 8 queries x 4 blocks of a warp.
+// multiplied (-inf is written there).  The epilogue writes fp32 [B, T, N];
+// each warp store covers 32 consecutive keys of one query (128 B).
+//
+// The first pass of the fused dense indexer (csa2_index_topk_dense, which
+// never writes the score matrix) keeps only the order-preserving key of each
+// 8-key block's maximum score; its kernel (index_blockmax_tc_kernel, below)
+// uses the same pipeline with the MMA transposed, queries on the TMEM lanes.
 // Every mbarrier wait is bounded; a thread that gives up raises a shared
 // abort word that every other wait polls, so all roles leave their loops,
 // the producer waits (bounded) for the copies it issued, and the CTA frees
@@ -43,8 +41,6 @@
 
 namespace csa2 {
 namespace {
-
-enum { EPI_SCORES = 0, EPI_BLOCKMAX = 1 };
 
 constexpr int QT = 64;                 // queries per tile
 constexpr int QR = QT * 4;             // query-head rows (MMA N)
@@ -83,7 +79,7 @@ struct PrefillArgs {
     uint32_t *err_flag;
     int qtiles, ktiles, kranges;
     int64_t items;
-    // BLOCKMAX: keys of the 8-key block maxima, [B*T, nblk]
+    // block maxima (index_blockmax_tc_kernel): keys of the 8-key block maxima, [B*T, nblk]
     uint32_t *bmax;
     int64_t nblk;
 };
@@ -185,7 +181,6 @@ __device__ __forceinline__ Item item_of(const PrefillArgs &a, int64_t item, int 
     return it;
 }
 
-template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     index_score_prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                                   PrefillArgs a) {
@@ -320,8 +315,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int64_t row0 = it.b * a.T + it.t0 + 16 * qg;
             for (int kt = it.kt0; kt < it.kt1; ++kt) {
                 const bool did = kt - it.kt0 < it.ntiles;
-                // a tile past every query's kv_len has nothing for the block maxima
-                if (EPI != EPI_SCORES && !did) continue;
                 const int buf = acount & 1;
                 if (did) {
                     if (!wait_or_abort(tfull(buf), (acount >> 1) & 1, abort_word)) {
@@ -356,35 +349,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     const int64_t rowh = row0 + 8 * h;
                     const int nq = a.T - (it.t0 + q0);   // queries of these eight that exist
-                    if constexpr (EPI == EPI_SCORES) {
-                        if (key < a.N) {
+                    if (key < a.N) {
 #pragma unroll
-                            for (int qq = 0; qq < 8; ++qq)
-                                if (qq < nq) a.scores[(rowh + qq) * a.N + key] = 0.5f * s[qq];
-                        }
-                    } else {
-                        // Max over the 8 keys of each block, transposed on the way:
-                        // at each xor step a lane keeps half of its queries and
-                        // takes the partner's values for them.  Lane l ends with
-                        // the block max of query 4 b0 + 2 b1 + b2 (b = bits of l)
-                        // over keys 8 (l >> 3) .. +7 of its 32: one store for all.
-                        const bool b0 = lane & 1, b1 = (lane >> 1) & 1, b2 = (lane >> 2) & 1;
-                        float x[4], y[2];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float send = b0 ? s[j] : s[4 + j], keep = b0 ? s[4 + j] : s[j];
-                            x[j] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 1));
-                        }
-#pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            const float send = b1 ? x[j] : x[2 + j], keep = b1 ? x[2 + j] : x[j];
-                            y[j] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2));
-                        }
-                        const float send = b2 ? y[0] : y[1], keep = b2 ? y[1] : y[0];
-                        const float m = 0.5f * fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 4));
-                        const int qs = 4 * b0 + 2 * b1 + b2;
-                        const int64_t blk = (key - lane + 8 * (lane >> 3)) >> 3;   // this lane's block
-                        if (qs < nq && 8 * blk < a.N) a.bmax[(rowh + qs) * a.nblk + blk] = score_key(m);
+                        for (int qq = 0; qq < 8; ++qq)
+                            if (qq < nq) a.scores[(rowh + qq) * a.N + key] = 0.5f * s[qq];
                     }
                 }
                 if (did) ++acount;
@@ -723,7 +691,6 @@ static PrefillArgs prefill_args(int B, int T, int64_t N, const float *w, const i
     return a;
 }
 
-template <int EPI>
 static csa2_status launch_prefill(const PrefillArgs &a, const void *q, const void *k, cudaStream_t stream) {
     if (a.items == 0) return CSA2_OK;
     // TMA row coordinates are 32-bit
@@ -737,10 +704,10 @@ static csa2_status launch_prefill(const PrefillArgs &a, const void *q, const voi
     st = rows64_map(&km, k, (uint64_t)a.B * a.N, KT, "index_score_prefill_tc (k)");
     if (st != CSA2_OK) return st;
     static bool smem_set[64];
-    CSA2_CUDA_CALL(ensure_smem_limit((const void *)index_score_prefill_tc_kernel<EPI>, (int)SMEM, smem_set),
+    CSA2_CUDA_CALL(ensure_smem_limit((const void *)index_score_prefill_tc_kernel, (int)SMEM, smem_set),
                    "index_score_prefill_tc: smem attribute");
     const int64_t grid = a.items < num_sms() ? a.items : num_sms();
-    CSA2_CUDA_CALL(launch_pdl(index_score_prefill_tc_kernel<EPI>, dim3((unsigned)grid), dim3(THREADS), SMEM, stream,
+    CSA2_CUDA_CALL(launch_pdl(index_score_prefill_tc_kernel, dim3((unsigned)grid), dim3(THREADS), SMEM, stream,
                               qm, km, a),
                    "index_score_prefill_tc_kernel launch");
     CSA2_LAUNCH_CHECK("index_score_prefill_tc_kernel");
@@ -752,7 +719,7 @@ csa2_status launch_index_score_prefill_tc(int B, int T, int64_t N, const void *q
                                           cudaStream_t stream) {
     PrefillArgs a = prefill_args(B, T, N, w, kv_len, err_flag);
     a.scores = scores;
-    return launch_prefill<EPI_SCORES>(a, q, k, stream);
+    return launch_prefill(a, q, k, stream);
 }
 
 csa2_status launch_prefill_block_max(int B, int T, int64_t N, const void *q, const float *w, const void *k,
