@@ -202,8 +202,24 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 // FP8W = false: the sparse branch (FP4 entries gathered by idx).  FP8W = true:
 // the sliding-window branch (the first swa_len E4M3 rows of the window,
 // contiguous, no scales) merged at the end with the sparse branch's output.
-template <bool FP8W>
+// 32 lanes x N consecutive fp32 TMEM columns (N = 4 or 16).
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+    static_assert(N == 4 || N == 16, "column counts");
+    if constexpr (N == 16) {
+        tc::tmem_ld16(taddr, r);
+    } else {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(taddr));
+    }
+}
+
+template <bool FP8W, int NH>
 __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
+    static_assert(NH == HB || (NH == HB / 4 && !FP8W), "64 heads per CTA, or 16 for few-token launches");
+    constexpr int HPT = NH / 4;                 // heads per thread where a warp pair of lane quarter x head group works
+    constexpr int RSHN = NH + 4;                // halves per channel row of an exchanged slice
     extern __shared__ __align__(128) uint8_t smem[];
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
@@ -214,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     const int64_t bt = group / a.hblocks;
     const int hblk = (int)(group - bt * a.hblocks);
     const int64_t b = bt / a.T;
-    const int h0 = hblk * HB;
+    const int h0 = hblk * NH;
 
     uint8_t *sK = smem + OFF_K;
     uint8_t *sQ = smem + OFF_Q;
@@ -241,7 +257,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     const int sel = rank * TM + e;
 
     if (tid == 0) {
-        tc::mbar_init(bar_q, HB);    // one arrival per head row
+        tc::mbar_init(bar_q, NH);    // one arrival per head row
         tc::mbar_init(bar_ld, TM);   // one arrival per entry
         tc::mbar_init(bar_s, 1);
         tc::mbar_init(bar_o, 1);
@@ -249,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         tc::mbar_init_fence();
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
-    if (tid < HB) reinterpret_cast<uint32_t *>(sM)[tid] = 0u;   // per-head max |q| (bits), used by 2a
+    if (tid < NH) reinterpret_cast<uint32_t *>(sM)[tid] = 0u;   // per-head max |q| (bits), used by 2a
     __syncthreads();
     // cluster barrier, first half: this CTA runs; the wait comes before the first remote store
     if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -270,7 +286,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     // qt = (e / 8) mod 4, which spreads them over all 16 warps (8 or 16 each):
     // a warp issues its lanes' bulk copies one after another.
     const bool issuer = qt == ((e >> 3) & 3);
-    if (issuer && e < HB) {        // Q rows do not depend on the indices: first
+    if (issuer && e < NH) {        // Q rows do not depend on the indices: first
         const uint16_t *qrow = a.q + ((bt * a.H) + h0 + e) * (int64_t)D;
         mbar_arrive_expect_tx(bar_q, D * 2);
         bulk_g2s(tc::smem_u32(smem + OFF_QRAW + e * QRAW_STRIDE), qrow, D * 2, bar_q);
@@ -314,40 +330,46 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         // lanes: 8 heads x 4 chunk positions, so both the staged-row reads and the
         // tile stores touch every bank once per 128 bytes; a warp pair covers the
         // 72 chunks of its 8 heads (36 each, 9 per thread)
+        // (with 16 heads per CTA only the four warps of rows 0..15 convert)
         const int hq = 8 * (warp & 7) + (lane & 7), cpos = lane >> 3, c0 = 36 * (warp >> 3);
-        const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE + (c0 + cpos) * 16;
-        uint4 qv[9];
-#pragma unroll
-        for (int i = 0; i < 9; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + i * 64);
-        float mx = 0.f;
-#pragma unroll
-        for (int i = 0; i < 9; ++i) {
-            const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+        const bool qrow = hq < NH;   // warp-uniform
         uint32_t *hmax = reinterpret_cast<uint32_t *>(sM);
-        if (cpos == 0) atomicMax(hmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
-        __syncthreads();
-        mx = __uint_as_float(hmax[hq]);
-        int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
-        int sh = 14 - e2;  // max |q| * 2^sh in [2^14, 2^15)
-        sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
-        const float up = ldexpf(1.0f, sh);
-        uint8_t *qdst = sQ + (hq >> 3) * Q_SBO + (hq & 7) * 16 + (c0 + cpos) * 128;
+        uint4 qv[9];
+        if (qrow) {
+            const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE + (c0 + cpos) * 16;
 #pragma unroll
-        for (int i = 0; i < 9; ++i) {
-            const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-            uint32_t o[4];
+            for (int i = 0; i < 9; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + i * 64);
+            float mx = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
-            *reinterpret_cast<uint4 *>(qdst + i * 512) = make_uint4(o[0], o[1], o[2], o[3]);
+            for (int i = 0; i < 9; ++i) {
+                const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+            if (cpos == 0) atomicMax(hmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
         }
-        if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
+        __syncthreads();
+        if (qrow) {
+            const float mx = __uint_as_float(hmax[hq]);
+            int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
+            int sh = 14 - e2;  // max |q| * 2^sh in [2^14, 2^15)
+            sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
+            const float up = ldexpf(1.0f, sh);
+            uint8_t *qdst = sQ + (hq >> 3) * Q_SBO + (hq & 7) * 16 + (c0 + cpos) * 128;
+#pragma unroll
+            for (int i = 0; i < 9; ++i) {
+                const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
+                *reinterpret_cast<uint4 *>(qdst + i * 512) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
+        }
     }
     // ---- 2b. staged codes -> registers (the Khat tile overwrites the staging area)
     // The 36 16-channel groups of an entry are dequantised in two halves (groups
@@ -395,7 +417,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     };
     // ---- 3. S^T = Khat . Q^T  (M = 128 entries, N = 64 heads, K = 576): 18 k-steps per half
     const uint32_t a0s = tc::smem_u32(sK), b0s = tc::smem_u32(sQ);
-    constexpr uint32_t idesc_s = tc::idesc_f16_f32(TM, HB, false, false);
+    constexpr uint32_t idesc_s = tc::idesc_f16_f32(TM, NH, false, false);
     dequant_half(0, [](int) {});
     tc::fence_async_smem();
     tc::fence_before();
@@ -438,16 +460,16 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     }
 
     // ---- 4a. S^T -> shared memory, transposed to [head][entry] (the Q tile is free now)
-    const int quarter = warp & 3, hh = warp >> 2;   // TMEM lane quarter, 16-column group
+    const int quarter = warp & 3, hh = warp >> 2;   // TMEM lane quarter, group of HPT columns (heads)
     {
-        uint32_t r[16];
-        tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + S_COL + 16 * hh, r);
+        uint32_t r[HPT];
+        tmem_ld_n(tmem + ((uint32_t)(32 * quarter) << 16) + S_COL + HPT * hh, r);
         tc::tmem_ld_wait();
         const int ee = 32 * quarter + lane;
         const bool v = ok && sValid[ee];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-            const int h = 16 * hh + jj;
+        for (int jj = 0; jj < HPT; ++jj) {
+            const int h = HPT * hh + jj;
             sT[h * ST_STRIDE + ee] = v ? __uint_as_float(r[jj]) * sCs[h] : -INFINITY;
         }
     }
@@ -455,29 +477,29 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
 
     // ---- 4b. softmax per head over this CTA's entries; P -> f16 core-matrix tile [head][entry]
     {
-        const int h = tid >> 3, part = tid & 7;   // 8 threads per head, entries 8 i + part
-        float z[16];
+        constexpr int TPH = THREADS / NH, EPT = TM / TPH;   // threads per head, entries per thread
+        const int h = tid / TPH, part = tid % TPH;           // entries TPH i + part
+        float z[EPT];
         float mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            z[i] = sT[h * ST_STRIDE + 8 * i + part];
+        for (int i = 0; i < EPT; ++i) {
+            z[i] = sT[h * ST_STRIDE + TPH * i + part];
             mx = fmaxf(mx, z[i]);
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
-        float sum = 0.f;
-        uint8_t *pdst = sP + (h >> 3) * P_SBO + (h & 7) * 16 + part * 2;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int o = 1; o < TPH; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        float sum = 0.f;
+        uint8_t *pdst = sP + (h >> 3) * P_SBO + (h & 7) * 16;
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
             const float p = (mx == -INFINITY || z[i] == -INFINITY) ? 0.f : ex2(z[i] - mx);
             const __half ph = __float2half_rn(p);
             sum += __half2float(ph);
-            *reinterpret_cast<__half *>(pdst + i * 128) = ph;   // entry 8 i + part
+            const int en = TPH * i + part;   // entry
+            *reinterpret_cast<__half *>(pdst + (en >> 3) * 128 + (en & 7) * 2) = ph;
         }
-        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+#pragma unroll
+        for (int o = 1; o < TPH; o <<= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
         if (part == 0) {
             sM[h] = mx;
             sL[h] = sum;
@@ -496,26 +518,26 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     if (tid == 0) {
         const uint64_t da = tc::desc_noswizzle(tc::smem_u32(sK), KT_SBO, 128),
                        db = tc::desc_noswizzle(tc::smem_u32(sP), 128, P_SBO);
-        constexpr uint32_t idesc = tc::idesc_f16_f32(TM, HB, true, false);
+        constexpr uint32_t idesc = tc::idesc_f16_f32(TM, NH, true, false);
 #pragma unroll
         for (int mb = 0; mb < DV / 128; ++mb)
 #pragma unroll
             for (int ks = 0; ks < TM / 16; ++ks)
-                tc::mma_f16(tmem + O_COL + mb * HB, tc::desc_at(da, ks * 2 * KT_SBO + mb * 16 * 128),
+                tc::mma_f16(tmem + O_COL + mb * NH, tc::desc_at(da, ks * 2 * KT_SBO + mb * 16 * 128),
                             tc::desc_at(db, ks * 256), idesc, ks > 0);
         tc::commit(bar_o);
     }
     if (S > 1) {   // every CTA runs: publish this CTA's (max, sum) per head in every CTA of the cluster
         asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-        if (tid < HB)
+        if (tid < NH)
             for (int c = 0; c < S; ++c) {
-                float *st = cluster.map_shared_rank(sStats, c) + rank * 2 * HB;
+                float *st = cluster.map_shared_rank(sStats, c) + rank * 2 * NH;
                 st[tid] = sM[tid];
-                st[HB + tid] = sL[tid];
+                st[NH + tid] = sL[tid];
             }
-    } else if (tid < HB) {
+    } else if (tid < NH) {
         sStats[tid] = sM[tid];
-        sStats[HB + tid] = sL[tid];
+        sStats[NH + tid] = sL[tid];
     }
     ok = tc::mbar_wait(bar_o, 0, MAX_POLLS) && ok;
     pdl_launch_dependents();   // the next kernel may launch during the exchange
@@ -528,14 +550,14 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     // slowest CTA); after it the TMA engine copies the slices into the owners'
     // shared memory (bulk shared -> remote shared, completing on the owner's
     // mbarrier).  The own slice is written in place (the Khat tile is free).
-    const uint32_t slice_bytes = slice_bytes_for(W);
+    const uint32_t slice_bytes = (uint32_t)W * RSHN * 2;
     uint8_t *stage = smem + OFF_Q;             // sT is dead; P stays above the staging
     uint8_t *recv = smem + OFF_K;              // received slices, by source rank
     if (tid == 0) asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_rx),
                                "r"((uint32_t)(S - 1) * slice_bytes) : "memory");
-    float il[16];                               // 1 / L of this thread's 16 heads
+    float il[HPT];                              // 1 / L of this thread's HPT heads
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) il[jj] = sIL[16 * hh + jj];
+    for (int jj = 0; jj < HPT; ++jj) il[jj] = sIL[HPT * hh + jj];
     // slice o of the sending order (own slice last): stage it, and for another
     // CTA's slice copy it once the cluster barrier has passed
     auto stage_slice = [&](int o) {
@@ -543,12 +565,12 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         uint8_t *dst = (oo == rank) ? recv + (size_t)rank * slice_bytes : stage + (size_t)o * slice_bytes;
         for (int bi = 0; bi < bpo; ++bi) {
             const int mb = oo * bpo + bi;
-            uint32_t r[16];
-            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * HB + 16 * hh, r);
+            uint32_t r[HPT];
+            tmem_ld_n(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * NH + HPT * hh, r);
             tc::tmem_ld_wait();
-            uint8_t *row = dst + (size_t)(bi * 128 + 32 * quarter + lane) * (RSH * 2) + 32 * hh;
+            uint8_t *row = dst + (size_t)(bi * 128 + 32 * quarter + lane) * (RSHN * 2) + 2 * HPT * hh;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
+            for (int q4 = 0; q4 < HPT / 4; ++q4)
                 *reinterpret_cast<uint2 *>(row + 8 * q4) =
                     make_uint2(pack_f16x2(__uint_as_float(r[4 * q4]) * il[4 * q4], __uint_as_float(r[4 * q4 + 1]) * il[4 * q4 + 1]),
                                pack_f16x2(__uint_as_float(r[4 * q4 + 2]) * il[4 * q4 + 2], __uint_as_float(r[4 * q4 + 3]) * il[4 * q4 + 3]));
@@ -570,14 +592,14 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     cluster.sync();                            // every CTA's P V is done: its Khat region may be written
     if (S > 1 && tid == 0) send_slice(0);
     // combine weights L_c 2^(m_c - M) / sum_c' L_c' 2^(m_c' - M) from every CTA's (max, sum)
-    if (tid < HB) {
+    if (tid < NH) {
         float mc[MAX_S], lc[MAX_S];
         float M = -INFINITY;
 #pragma unroll
         for (int c = 0; c < MAX_S; ++c) {
             if (c < S) {
-                mc[c] = sStats[c * 2 * HB + tid];
-                lc[c] = sStats[c * 2 * HB + HB + tid];
+                mc[c] = sStats[c * 2 * NH + tid];
+                lc[c] = sStats[c * 2 * NH + NH + tid];
                 M = fmaxf(M, mc[c]);
             }
         }
@@ -586,14 +608,14 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         for (int c = 0; c < MAX_S; ++c) {
             if (c < S) {
                 const float wc = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : lc[c] * ex2(mc[c] - M);
-                sW[c * HB + tid] = wc;
+                sW[c * NH + tid] = wc;
                 L += wc;
             }
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
         for (int c = 0; c < MAX_S; ++c)
-            if (c < S) sW[c * HB + tid] *= inv;
+            if (c < S) sW[c * NH + tid] *= inv;
         sLse[tid] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
         if constexpr (FP8W) {
             // merge with the sparse branch: the softmax over both branches' entries
@@ -610,7 +632,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
                 }
 #pragma unroll
                 for (int c = 0; c < MAX_S; ++c)
-                    if (c < S) sW[c * HB + tid] *= alpha;
+                    if (c < S) sW[c * NH + tid] *= alpha;
                 sLse[tid] = lo;
             }
             sBeta[tid] = beta;
@@ -624,36 +646,36 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         ok = tc::mbar_wait(bar_rx, 0, MAX_POLLS) && ok;   // (no bytes expected: completes the phase)
         __syncthreads();                                   // the weights of the block above
         if (!ok) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);   // any thread whose wait gave up
-        const int64_t hbase = (bt * a.H) + h0 + 16 * hh;
+        const int64_t hbase = (bt * a.H) + h0 + HPT * hh;
         // two 128-channel blocks at a time: their sparse-branch values are
         // loaded together, after the TMEM loads' wait
 #pragma unroll 1
         for (int mb = 0; mb < DV / 128; mb += 2) {
-            uint32_t r[2][16];
-            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * HB + 16 * hh, r[0]);
-            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + (mb + 1) * HB + 16 * hh, r[1]);
+            uint32_t r[2][HPT];
+            tmem_ld_n(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + mb * NH + HPT * hh, r[0]);
+            tmem_ld_n(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + (mb + 1) * NH + HPT * hh, r[1]);
             tc::tmem_ld_wait();
-            float os[2][16];
+            float os[2][HPT];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int c = (mb + u) * 128 + 32 * quarter + lane;
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
+                for (int jj = 0; jj < HPT; ++jj)
                     os[u][jj] = (FP8W && a.o_sparse) ? a.o_sparse[(hbase + jj) * (int64_t)DV + c] : 0.f;   // may alias out
             }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int c = (mb + u) * 128 + 32 * quarter + lane;
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int h = 16 * hh + jj;
+                for (int jj = 0; jj < HPT; ++jj) {
+                    const int h = HPT * hh + jj;
                     float v = __uint_as_float(r[u][jj]) * il[jj] * sW[h];
                     if (FP8W) v += sBeta[h] * os[u][jj];
                     a.out[(hbase + jj) * (int64_t)DV + c] = v;
                 }
             }
         }
-        if (a.lse && tid < HB) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
+        if (a.lse && tid < NH) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
@@ -678,45 +700,48 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
     {
         const int c_lo = rank * W;
         for (int bi = 0; bi < bpo; ++bi) {
-            uint32_t r[16];
-            tc::tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + (rank * bpo + bi) * HB + 16 * hh, r);
+            uint32_t r[HPT];
+            tmem_ld_n(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + (rank * bpo + bi) * NH + HPT * hh, r);
             tc::tmem_ld_wait();
             const int cl = bi * 128 + 32 * quarter + lane;   // channel within the slice
-            const int64_t orow = (bt * a.H) + h0 + 16 * hh;
+            const int64_t orow = (bt * a.H) + h0 + HPT * hh;
+            constexpr int GH = HPT < 8 ? HPT : 8;            // heads per combine group (four per 8-byte read)
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float acc[8];
+            for (int half = 0; half < HPT / GH; ++half) {
+                float acc[GH];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int jj = 8 * half + i;
-                    acc[i] = __uint_as_float(r[jj]) * il[jj] * sW[rank * HB + 16 * hh + jj];
+                for (int i = 0; i < GH; ++i) {
+                    const int jj = GH * half + i;
+                    acc[i] = __uint_as_float(r[jj]) * il[jj] * sW[rank * NH + HPT * hh + jj];
                 }
 #pragma unroll
                 for (int src = 0; src < MAX_S; ++src) {
                     if (src < S && src != rank) {
-                        const uint8_t *rp = recv + (size_t)src * slice_bytes + (size_t)cl * (RSH * 2) + 32 * hh + 16 * half;
-                        const uint2 v0 = *reinterpret_cast<const uint2 *>(rp);
-                        const uint2 v1 = *reinterpret_cast<const uint2 *>(rp + 8);
-                        const float *wsrc = sW + src * HB + 16 * hh + 8 * half;
-                        const float2 a01 = __half22float2(*reinterpret_cast<const __half2 *>(&v0.x));
-                        const float2 a23 = __half22float2(*reinterpret_cast<const __half2 *>(&v0.y));
-                        const float2 a45 = __half22float2(*reinterpret_cast<const __half2 *>(&v1.x));
-                        const float2 a67 = __half22float2(*reinterpret_cast<const __half2 *>(&v1.y));
-                        acc[0] += wsrc[0] * a01.x; acc[1] += wsrc[1] * a01.y; acc[2] += wsrc[2] * a23.x;
-                        acc[3] += wsrc[3] * a23.y; acc[4] += wsrc[4] * a45.x; acc[5] += wsrc[5] * a45.y;
-                        acc[6] += wsrc[6] * a67.x; acc[7] += wsrc[7] * a67.y;
+                        const uint8_t *rp =
+                            recv + (size_t)src * slice_bytes + (size_t)cl * (RSHN * 2) + 2 * HPT * hh + 2 * GH * half;
+                        const float *wsrc = sW + src * NH + HPT * hh + GH * half;
+#pragma unroll
+                        for (int g4 = 0; g4 < GH / 4; ++g4) {
+                            const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * g4);
+                            const float2 a01 = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+                            const float2 a23 = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+                            acc[4 * g4] += wsrc[4 * g4] * a01.x;
+                            acc[4 * g4 + 1] += wsrc[4 * g4 + 1] * a01.y;
+                            acc[4 * g4 + 2] += wsrc[4 * g4 + 2] * a23.x;
+                            acc[4 * g4 + 3] += wsrc[4 * g4 + 3] * a23.y;
+                        }
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int64_t oi = (orow + 8 * half + i) * (int64_t)DV + c_lo + cl;
+                for (int i = 0; i < GH; ++i) {
+                    const int64_t oi = (orow + GH * half + i) * (int64_t)DV + c_lo + cl;
                     float v = acc[i];
-                    if (FP8W && a.o_sparse) v += sBeta[16 * hh + 8 * half + i] * a.o_sparse[oi];   // may alias out
+                    if (FP8W && a.o_sparse) v += sBeta[HPT * hh + GH * half + i] * a.o_sparse[oi];   // may alias out
                     a.out[oi] = v;
                 }
             }
         }
-        if (rank == 0 && a.lse && tid < HB) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
+        if (rank == 0 && a.lse && tid < NH) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
     }
     tc::fence_before();   // every warp's TMEM loads are done before the columns are freed
     __syncthreads();
@@ -1207,14 +1232,19 @@ bool sparse_attn_tc_supported(int D_, int dv, int H, int K) {
     return D_ == D && dv == DV && H % HB == 0 && K >= 1 && K <= MAX_S * TM;
 }
 
-template <bool FP8W>
+// Entries split over a cluster of 1, 2 or 4 CTAs (the channel slices divide 512).
+static int cluster_size_for(int entries) {
+    const int tiles = (entries + TM - 1) / TM;
+    return tiles <= 1 ? 1 : (tiles <= 2 ? 2 : 4);
+}
+
+template <bool FP8W, int NH>
 static csa2_status launch_tc(TcArgs &a, int B, int entries, cudaStream_t stream) {
     static bool smem_set[64];
-    CSA2_CUDA_CALL(ensure_smem_limit((const void *)sparse_attn_tc_kernel<FP8W>, (int)SMEM, smem_set),
+    CSA2_CUDA_CALL(ensure_smem_limit((const void *)sparse_attn_tc_kernel<FP8W, NH>, (int)SMEM, smem_set),
                    "sparse_attn_tc: smem attribute");
-    const int tiles = (entries + TM - 1) / TM;
-    a.csize = tiles <= 1 ? 1 : (tiles <= 2 ? 2 : 4);   // 1, 2 or 4: the channel slices divide 512
-    a.hblocks = a.H / HB;
+    a.csize = cluster_size_for(entries);
+    a.hblocks = a.H / NH;
     const int64_t grid = (int64_t)B * a.T * a.hblocks * a.csize;
     if (grid > 0x7FFFFFFF) {
         set_error("sparse_attn_tc: grid too large");
@@ -1233,7 +1263,7 @@ static csa2_status launch_tc(TcArgs &a, int B, int entries, cudaStream_t stream)
     attr[1] = pdl_attribute();
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    CSA2_CUDA_CALL(cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<FP8W>, a), "sparse_attn_tc_kernel launch");
+    CSA2_CUDA_CALL(cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<FP8W, NH>, a), "sparse_attn_tc_kernel launch");
     CSA2_LAUNCH_CHECK("sparse_attn_tc_kernel");
     return CSA2_OK;
 }
@@ -1265,8 +1295,12 @@ csa2_status launch_sparse_attn_tc(int B, int T, int H, int K, int64_t N, const v
     a.T = T; a.H = H; a.K = K; a.N = N;
     a.q = (const uint16_t *)q; a.codes = codes; a.scales = scales; a.idx = idx; a.kv_len = kv_len;
     a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.err_flag = err_flag;
-    if (use_token_kernel((int64_t)B * T * (H / HB))) return launch_tc_tokens(a, B, stream);
-    return launch_tc<false>(a, B, K, stream);
+    const int64_t items = (int64_t)B * T * (H / HB);
+    if (use_token_kernel(items)) return launch_tc_tokens(a, B, stream);
+    // few tokens: each token's heads split over four CTA groups of 16 while that grid
+    // still fits one wave of SMs (every per-head phase of a CTA shrinks fourfold)
+    if (items * 4 * cluster_size_for(K) <= (int64_t)num_sms()) return launch_tc<false, HB / 4>(a, B, K, stream);
+    return launch_tc<false, HB>(a, B, K, stream);
 }
 
 csa2_status launch_swa_attn_tc(int B, int T, int H, const void *q, const uint8_t *kv8, int W, const int32_t *swa_len,
@@ -1276,7 +1310,7 @@ csa2_status launch_swa_attn_tc(int B, int T, int H, const void *q, const uint8_t
     a.T = T; a.H = H; a.K = W; a.N = W;
     a.q = (const uint16_t *)q; a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.err_flag = err_flag;
     a.kv8 = kv8; a.W = W; a.swa_len = swa_len; a.o_sparse = o_sparse; a.lse_sparse = lse_sparse;
-    return launch_tc<true>(a, B, W, stream);
+    return launch_tc<true, HB>(a, B, W, stream);
 }
 
 }  // namespace csa2
