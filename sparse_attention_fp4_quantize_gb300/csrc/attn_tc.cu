@@ -327,48 +327,90 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
 
     // ---- 2a. staged Q -> registers, per-head power-of-two scale, f16 core-matrix tile [head][channel]
     {
-        // lanes: 8 heads x 4 chunk positions, so both the staged-row reads and the
-        // tile stores touch every bank once per 128 bytes; a warp pair covers the
-        // 72 chunks of its 8 heads (36 each, 9 per thread)
-        // (with 16 heads per CTA only the four warps of rows 0..15 convert)
-        const int hq = 8 * (warp & 7) + (lane & 7), cpos = lane >> 3, c0 = 36 * (warp >> 3);
-        const bool qrow = hq < NH;   // warp-uniform
-        uint32_t *hmax = reinterpret_cast<uint32_t *>(sM);
-        uint4 qv[9];
-        if (qrow) {
-            const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE + (c0 + cpos) * 16;
+        if constexpr (NH == HB) {
+            // lanes: 8 heads x 4 chunk positions, so both the staged-row reads and the
+            // tile stores touch every bank once per 128 bytes; a warp pair covers the
+            // 72 chunks of its 8 heads (36 each, 9 per thread)
+            const int hq = 8 * (warp & 7) + (lane & 7), cpos = lane >> 3, c0 = 36 * (warp >> 3);
+            uint32_t *hmax = reinterpret_cast<uint32_t *>(sM);
+            uint4 qv[9];
+            {
+                const uint8_t *qraw = smem + OFF_QRAW + hq * QRAW_STRIDE + (c0 + cpos) * 16;
 #pragma unroll
-            for (int i = 0; i < 9; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + i * 64);
-            float mx = 0.f;
+                for (int i = 0; i < 9; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qraw + i * 64);
+                float mx = 0.f;
 #pragma unroll
-            for (int i = 0; i < 9; ++i) {
-                const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+                for (int i = 0; i < 9; ++i) {
+                    const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
+                    for (int k = 0; k < 4; ++k)
+                        mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
+                }
+                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+                if (cpos == 0) atomicMax(hmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
             }
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-            if (cpos == 0) atomicMax(hmax + hq, __float_as_uint(mx));   // |q| >= 0: bit order = value order
-        }
-        __syncthreads();
-        if (qrow) {
-            const float mx = __uint_as_float(hmax[hq]);
-            int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
-            int sh = 14 - e2;  // max |q| * 2^sh in [2^14, 2^15)
-            sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
-            const float up = ldexpf(1.0f, sh);
-            uint8_t *qdst = sQ + (hq >> 3) * Q_SBO + (hq & 7) * 16 + (c0 + cpos) * 128;
+            __syncthreads();
+            {
+                const float mx = __uint_as_float(hmax[hq]);
+                int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
+                int sh = 14 - e2;  // max |q| * 2^sh in [2^14, 2^15)
+                sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
+                const float up = ldexpf(1.0f, sh);
+                uint8_t *qdst = sQ + (hq >> 3) * Q_SBO + (hq & 7) * 16 + (c0 + cpos) * 128;
 #pragma unroll
-            for (int i = 0; i < 9; ++i) {
-                const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-                uint32_t o[4];
+                for (int i = 0; i < 9; ++i) {
+                    const uint32_t w4[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+                    uint32_t o[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
-                *reinterpret_cast<uint4 *>(qdst + i * 512) = make_uint4(o[0], o[1], o[2], o[3]);
+                    for (int k = 0; k < 4; ++k)
+                        o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
+                    *reinterpret_cast<uint4 *>(qdst + i * 512) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
             }
-            if (cpos == 0 && c0 == 0) sCs[hq] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
+        } else {
+            // 16 rows: 24 threads per row take three chunks each (warps 0..11); the eight
+            // lanes of a quarter-warp take eight rows and chunks (2 j + s) mod 24 + 24 m,
+            // so both the staged-row reads and the tile stores meet every bank once
+            const int G = tid >> 3, jq = tid & 7;
+            const bool act = tid < 3 * THREADS / 4;   // warp-uniform
+            const int row = 8 * (G & 1) + jq, sg = G >> 1, cb = (2 * jq + sg) % 24;
+            uint32_t *hmax = reinterpret_cast<uint32_t *>(sM);
+            uint4 qv[3];
+            if (act) {
+                const uint8_t *qraw = smem + OFF_QRAW + row * QRAW_STRIDE;
+#pragma unroll
+                for (int m = 0; m < 3; ++m) qv[m] = *reinterpret_cast<const uint4 *>(qraw + (cb + 24 * m) * 16);
+                float mx = 0.f;
+#pragma unroll
+                for (int m = 0; m < 3; ++m) {
+                    const uint32_t w4[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
+                }
+                atomicMax(hmax + row, __float_as_uint(mx));   // |q| >= 0: bit order = value order
+            }
+            __syncthreads();
+            if (act) {
+                const float mx = __uint_as_float(hmax[row]);
+                int e2 = (mx > 0.f) ? ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127) : 0;
+                int sh = 14 - e2;  // max |q| * 2^sh in [2^14, 2^15)
+                sh = sh < -60 ? -60 : (sh > 60 ? 60 : sh);
+                const float up = ldexpf(1.0f, sh);
+                uint8_t *qdst = sQ + (row >> 3) * Q_SBO + (row & 7) * 16;
+#pragma unroll
+                for (int m = 0; m < 3; ++m) {
+                    const uint32_t w4[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        o[k] = pack_f16x2(__uint_as_float(w4[k] << 16) * up, __uint_as_float(w4[k] & 0xFFFF0000u) * up);
+                    *reinterpret_cast<uint4 *>(qdst + (cb + 24 * m) * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                if (sg == 0) sCs[row] = a.sm_scale * ldexpf(1.0f, -sh) * 1.4426950408889634f;  // x log2(e)
+            }
         }
     }
     // ---- 2b. staged codes -> registers (the Khat tile overwrites the staging area)
