@@ -730,10 +730,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         __syncthreads();
         if (tid == 0) send_slice(o);
     }
-    if (tid == 0) bulk_wait_read0();           // staging reads done before this CTA may exit
-    ok = tc::mbar_wait(bar_rx, 0, MAX_POLLS) && ok;   // the other CTAs' slices have landed
-    __syncthreads();
-    if (!ok) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);   // any thread whose wait gave up
+    __syncthreads();                           // the combine weights above
 
     // ---- 7. combine this CTA's channel slice with the weights: its own part
     // straight from TMEM in fp32 (the TMEM lane mapping: lane = channel, 16
@@ -745,6 +742,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
             uint32_t r[HPT];
             tmem_ld_n(tmem + ((uint32_t)(32 * quarter) << 16) + O_COL + (rank * bpo + bi) * NH + HPT * hh, r);
             tc::tmem_ld_wait();
+            if (bi == 0) ok = tc::mbar_wait(bar_rx, 0, MAX_POLLS) && ok;   // the other CTAs' slices (the own load overlaps)
             const int cl = bi * 128 + 32 * quarter + lane;   // channel within the slice
             const int64_t orow = (bt * a.H) + h0 + HPT * hh;
             constexpr int GH = HPT < 8 ? HPT : 8;            // heads per combine group (four per 8-byte read)
@@ -785,6 +783,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         }
         if (rank == 0 && a.lse && tid < NH) a.lse[(bt * a.H) + h0 + tid] = sLse[tid];
     }
+    if (!ok) flag_error(a.err_flag, CSA2_FLAG_TIMEOUT);   // any thread whose wait gave up
+    if (tid == 0) bulk_wait_read0();           // staging reads done before this CTA may exit
     tc::fence_before();   // every warp's TMEM loads are done before the columns are freed
     __syncthreads();
     tc::fence_after();
