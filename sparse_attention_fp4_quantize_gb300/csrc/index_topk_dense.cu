@@ -178,7 +178,7 @@ struct RescoreArgs {
 };
 
 __global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArgs a) {
-    extern __shared__ __align__(16) uint32_t dyn[];   // [nblk] maxima | [16 ceil(K/2)] candidate keys | [K] blocks
+    extern __shared__ __align__(16) uint32_t dyn[];   // [nblk] maxima | [16 ceil(K/2)] candidate keys | [2 ceil(K/2)] blocks
     __shared__ __align__(16) uint32_t hist[2048];
     __shared__ uint32_t scratch[RS_WARPS + 2];
     pdl_wait();
@@ -209,29 +209,34 @@ __global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArg
         block_emit(sBm, nb, tau, above, a.K, sBlk, [](int i) { return (int32_t)i; }, scratch);
         nsel = a.K;
     }
+    if (tid == 0 && (nsel & 1)) sBlk[nsel] = -1;   // the odd tile's second block: no position
     __syncthreads();
 
     // ---- rescore the 8 nsel candidates: a tile is two blocks (16 keys); lane
     // (g, t4) loads 16 bytes of keys g and g + 8, the decode scorer's FP8
-    // mma.sync fragments (4 heads as columns 0-3 of n8)
+    // mma.sync fragments (4 heads as columns 0-3 of n8).  Positions are below
+    // 2^18, so a block's position test and its byte offset are 32-bit
+    // arithmetic (block -1 wraps to a position past every row length).
     const uint4 q8 = (g < 4) ? __ldg(reinterpret_cast<const uint4 *>(a.q + (r * 4 + g) * 64 + 16 * t4))
                              : make_uint4(0u, 0u, 0u, 0u);
     const float w0 = (t4 < 2) ? a.w[r * 4 + 2 * t4] : 0.f;
     const float w1 = (t4 < 2) ? a.w[r * 4 + 2 * t4 + 1] : 0.f;
     const int ntile = (nsel + 1) / 2;
-    const uint8_t *kb = a.k + b * a.N * 64;
+    const uint8_t *kq = a.k + b * a.N * 64 + g * 64 + 16 * t4;   // this lane's 16 bytes of key g of block 0
+    const uint32_t ulen = (uint32_t)len;
+    const int2 *sBlk2 = reinterpret_cast<const int2 *>(sBlk);
     for (int t0 = warp; t0 < ntile; t0 += 4 * RS_WARPS) {
         uint4 raw[4][2];
         bool v[4][2];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int tl = t0 + u * RS_WARPS;
+            const int2 bb = tl < ntile ? sBlk2[tl] : make_int2(-1, -1);
+            const uint32_t blk[2] = {(uint32_t)bb.x, (uint32_t)bb.y};
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                const int bi = 2 * tl + rr;
-                const int64_t p = bi < nsel ? (int64_t)sBlk[bi] * 8 + g : len;
-                v[u][rr] = tl < ntile && p < len;
-                raw[u][rr] = v[u][rr] ? __ldg(reinterpret_cast<const uint4 *>(kb + p * 64 + 16 * t4))
+                v[u][rr] = blk[rr] * 8u + (uint32_t)g < ulen;
+                raw[u][rr] = v[u][rr] ? __ldg(reinterpret_cast<const uint4 *>(kq + (size_t)(blk[rr] * 512u)))
                                       : make_uint4(0u, 0u, 0u, 0u);
             }
         }
@@ -310,10 +315,10 @@ extern "C" csa2_status csa2_index_topk_dense(int B, int T, int64_t N, const void
     RescoreArgs ra;
     ra.T = T; ra.N = N; ra.K = K; ra.bmax = bmax; ra.nblk = nblk;
     ra.q = (const uint8_t *)q_idx; ra.w = w; ra.k = (const uint8_t *)k_idx; ra.kv_len = kv_len; ra.idx = idx;
-    const size_t smem = (size_t)(nblk + 16 * (int64_t)((K + 1) / 2) + K) * 4;
+    const size_t smem = (size_t)(nblk + 18 * (int64_t)((K + 1) / 2)) * 4;
     static bool smem_set[64];
     CSA2_CUDA_CALL(ensure_smem_limit((const void *)dense_rescore_kernel,
-                                     (int)((nblk_for(MAX_N) + 9 * CSA2_MAX_K) * 4), smem_set),
+                                     (int)((nblk_for(MAX_N) + 18 * ((CSA2_MAX_K + 1) / 2)) * 4), smem_set),
                    "dense_rescore_kernel: smem attribute");
     CSA2_CUDA_CALL(launch_pdl(dense_rescore_kernel, dim3((unsigned)((int64_t)B * T)), dim3(RS_THREADS), smem, s, ra),
                    "dense_rescore_kernel launch");
