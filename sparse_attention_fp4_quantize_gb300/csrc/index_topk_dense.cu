@@ -124,43 +124,64 @@ __device__ uint32_t block_kth_largest(const uint32_t *keys, int n, int K, uint32
 }
 
 // Writes to out[0, K): every i < n with keys[i] > T, then keys[i] == T until K
-// are taken (T = 0: every nonzero key), then -1; pos(i) gives the output id.
-// above = the number of keys > T (known to the caller from the selection).
-// Slots come from one shared atomic per warp and 32 keys (ballots order the
-// lanes), so the writes never contend on a single counter lane by lane.
+// are taken, lowest i first (T = 0: every nonzero key), then -1; pos(i) gives
+// the output id.  above = the number of keys > T (known to the caller from the
+// selection).  Warp w owns a contiguous run of the keys: a first pass counts
+// its keys above and at T, the warps' counts give each warp its first slots,
+// and a second pass writes the ids in position order (ballot prefixes, no
+// atomics).  scratch: at least 2 RS_WARPS words; the caller's next barrier
+// separates this from another use of it.
 template <typename PosFn>
 __device__ void block_emit(const uint32_t *keys, int n, uint32_t T, uint32_t above, int K, int32_t *out, PosFn pos,
                            uint32_t *scratch) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) {
-        scratch[RS_WARPS] = 0u;
-        scratch[RS_WARPS + 1] = 0u;
-    }
-    __syncthreads();
     const uint32_t room = above < (uint32_t)K ? (uint32_t)K - above : 0u;
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int base = 32 * warp; base < n; base += RS_THREADS) {
+    const bool ties = T != 0u && room != 0u;
+    int R = (n + RS_WARPS - 1) / RS_WARPS;
+    R = (R + 31) & ~31;
+    const int w0 = min(n, warp * R), w1 = min(n, w0 + R);
+    uint32_t cg = 0u, ce = 0u;
+    for (int base = w0; base < w1; base += 32) {
         const int i = base + lane;
-        const uint32_t key = i < n ? keys[i] : 0u;
-        const uint32_t gt = __ballot_sync(0xFFFFFFFFu, key > T);
-        const uint32_t eq = __ballot_sync(0xFFFFFFFFu, T != 0u && i < n && key == T);
-        if (gt) {
-            uint32_t b0 = 0;
-            if (lane == 0) b0 = atomicAdd(&scratch[RS_WARPS], (uint32_t)__popc(gt));
-            b0 = __shfl_sync(0xFFFFFFFFu, b0, 0);
-            const uint32_t s = b0 + (uint32_t)__popc(gt & lt);
-            if (((gt >> lane) & 1u) && s < (uint32_t)K) out[s] = pos(i);
-        }
-        if (eq && room) {
-            uint32_t b1 = 0;
-            if (lane == 0) b1 = atomicAdd(&scratch[RS_WARPS + 1], (uint32_t)__popc(eq));
-            b1 = __shfl_sync(0xFFFFFFFFu, b1, 0);
-            const uint32_t t = b1 + (uint32_t)__popc(eq & lt);
-            if (((eq >> lane) & 1u) && t < room) out[above + t] = pos(i);
-        }
+        const uint32_t k = i < w1 ? keys[i] : 0u;
+        cg += __popc(__ballot_sync(0xFFFFFFFFu, k > T));
+        if (ties) ce += __popc(__ballot_sync(0xFFFFFFFFu, k == T));
+    }
+    if (lane == 0) {
+        scratch[warp] = cg;
+        scratch[RS_WARPS + warp] = ce;
     }
     __syncthreads();
-    const uint32_t taken = min((uint32_t)K, scratch[RS_WARPS]) + min(room, scratch[RS_WARPS + 1]);
+    uint32_t slot = 0u, tie = 0u, te = 0u;
+#pragma unroll
+    for (int w2 = 0; w2 < RS_WARPS; ++w2) {
+        const uint32_t e2 = scratch[RS_WARPS + w2];
+        if (w2 < warp) {
+            slot += scratch[w2];
+            tie += e2;
+        }
+        te += e2;
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const uint32_t k = i < w1 ? keys[i] : 0u;
+        const uint32_t bg = __ballot_sync(0xFFFFFFFFu, k > T);
+        if ((bg >> lane) & 1u) {
+            const uint32_t s2 = slot + __popc(bg & lt);
+            if (s2 < (uint32_t)K) out[s2] = pos(i);
+        }
+        slot += __popc(bg);
+        if (ties) {
+            const uint32_t be = __ballot_sync(0xFFFFFFFFu, k == T);
+            if ((be >> lane) & 1u) {
+                const uint32_t t2 = tie + __popc(be & lt);
+                if (t2 < room) out[above + t2] = pos(i);
+            }
+            tie += __popc(be);
+        }
+    }
+    const uint32_t taken = min((uint32_t)K, above) + min(room, te);
     for (int i = (int)taken + tid; i < K; i += RS_THREADS) out[i] = -1;
 }
 
@@ -180,7 +201,7 @@ struct RescoreArgs {
 __global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArgs a) {
     extern __shared__ __align__(16) uint32_t dyn[];   // [nblk] maxima | [16 ceil(K/2)] candidate keys | [2 ceil(K/2)] blocks
     __shared__ __align__(16) uint32_t hist[2048];
-    __shared__ uint32_t scratch[RS_WARPS + 2];
+    __shared__ uint32_t scratch[2 * RS_WARPS + 2];
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
