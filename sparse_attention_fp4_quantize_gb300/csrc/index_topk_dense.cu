@@ -60,7 +60,8 @@ __device__ __forceinline__ uint32_t warp_suffix(uint32_t v) {   // sum over lane
     return v;
 }
 
-// The K-th largest of n >= K >= 1 keys in shared memory, by the whole CTA:
+// The K-th largest of n >= K >= 1 keys in shared memory (16-byte aligned, zero
+// from n up to a multiple of 4), by the whole CTA:
 // three radix passes over the digits [31:21], [20:10], [9:0].  Each pass
 // histograms the keys that share the prefix found so far (2048 shared bins,
 // shared atomics), then the thread whose 8 bins hold the K-th key from the
@@ -77,9 +78,12 @@ __device__ uint32_t block_kth_largest(const uint32_t *keys, int n, int K, uint32
         reinterpret_cast<uint4 *>(hist)[tid] = make_uint4(0u, 0u, 0u, 0u);
         reinterpret_cast<uint4 *>(hist)[tid + RS_THREADS] = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
-        for (int i = tid; i < n; i += RS_THREADS) {
-            const uint32_t key = keys[i];
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & dmask], 1u);
+        for (int i = tid; 4 * i < n; i += RS_THREADS) {   // keys [n, 4 ceil(n / 4)) are zero
+            const uint4 v = reinterpret_cast<const uint4 *>(keys)[i];
+            if ((v.x & mask) == prefix) atomicAdd(&hist[(v.x >> sh) & dmask], 1u);
+            if ((v.y & mask) == prefix) atomicAdd(&hist[(v.y >> sh) & dmask], 1u);
+            if ((v.z & mask) == prefix) atomicAdd(&hist[(v.z >> sh) & dmask], 1u);
+            if ((v.w & mask) == prefix) atomicAdd(&hist[(v.w >> sh) & dmask], 1u);
         }
         __syncthreads();
         // this thread's bins 8 tid .. 8 tid + 7, as two 16-byte reads (eight word
@@ -224,6 +228,8 @@ __global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArg
         const uint32_t *row = a.bmax + r * a.nblk;
         for (int i = tid; 4 * i < nb; i += RS_THREADS) cp_async16((uint32_t)__cvta_generic_to_shared(sBm + 4 * i), row + 4 * i);
         asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        if (tid == ((nb - 1) >> 2) % RS_THREADS)   // the thread that copied the last group zeroes its tail
+            for (int j = nb; j < ((nb + 3) & ~3); ++j) sBm[j] = 0u;
         __syncthreads();
         uint32_t above;
         const uint32_t tau = block_kth_largest(sBm, nb, a.K, hist, scratch, above);
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArg
     const float w0 = (t4 < 2) ? a.w[r * 4 + 2 * t4] : 0.f;
     const float w1 = (t4 < 2) ? a.w[r * 4 + 2 * t4 + 1] : 0.f;
     const int ntile = (nsel + 1) / 2;
-    const uint8_t *kq = a.k + b * a.N * 64 + g * 64 + 16 * t4;   // this lane's 16 bytes of key g of block 0
+    const uint8_t *kq = a.k + b * a.N * 64 + 16 * t4;   // this lane's 16 bytes of the sequence's first key
     const uint32_t ulen = (uint32_t)len;
     const int2 *sBlk2 = reinterpret_cast<const int2 *>(sBlk);
     for (int t0 = warp; t0 < ntile; t0 += 4 * RS_WARPS) {
@@ -255,10 +261,10 @@ __global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArg
             const int2 bb = tl < ntile ? sBlk2[tl] : make_int2(-1, -1);
             const uint32_t blk[2] = {(uint32_t)bb.x, (uint32_t)bb.y};
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                v[u][rr] = blk[rr] * 8u + (uint32_t)g < ulen;
-                raw[u][rr] = v[u][rr] ? __ldg(reinterpret_cast<const uint4 *>(kq + (size_t)(blk[rr] * 512u)))
-                                      : make_uint4(0u, 0u, 0u, 0u);
+            for (int rr = 0; rr < 2; ++rr) {   // a slot past the row reads the first key (its score is dropped)
+                const uint32_t p = blk[rr] * 8u + (uint32_t)g;
+                v[u][rr] = p < ulen;
+                raw[u][rr] = __ldg(reinterpret_cast<const uint4 *>(kq + (v[u][rr] ? p * 64u : 0u)));
             }
         }
 #pragma unroll
