@@ -11,19 +11,20 @@
 // maximum is largest (ties at tau broken arbitrarily) is <= tau.  So the
 // Top-K of the scores inside those K blocks (8K candidates) is a Top-K of the
 // row, the same argument as the hierarchical pool's.  The rescoring below
-// uses the FP8 mma.sync tiling of the decode scorer while the block maxima
-// come from the tensor-core pass, so the two may round a score differently
-// in the last bits of fp32: a difference only at the K-th value, inside the
-// selection's tie band.
+// uses warp MMAs on keys converted to f16 while the block maxima come from
+// the tensor-core pass, so the two may sum a score in a different order and
+// differ in the last bits of fp32: a difference only at the K-th value,
+// inside the selection's tie band.
 //
 // Kernels, in stream order:
-//  1. index_score_prefill_tc_kernel<BLOCKMAX>: keys of the 8-position block
-//     maxima, [B*T, nblk] (the dense tcgen05 pass over every (query, key));
+//  1. index_blockmax_tc_kernel: keys of the 8-position block maxima,
+//     [B*T, nblk] (the dense tcgen05 pass over every (query, key));
 //  2. dense_rescore_kernel: one CTA per query.  The row's block maxima are
 //     staged in shared memory; tau and the K blocks by a block-wide radix
 //     select; the 8K candidates gathered (blocks are 512 contiguous bytes of
-//     keys) and rescored with FP8 mma.sync; the Top-K of their scores by the
-//     same radix select, written in any order, -1 padded.
+//     keys) and rescored with f16 mma.sync (FP8 -> f16 in registers, exact);
+//     the Top-K of their scores by the same radix select, written in
+//     position order of the candidates, -1 padded.
 #include "common.cuh"
 
 namespace csa2 {
@@ -240,12 +241,21 @@ __global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArg
     __syncthreads();
 
     // ---- rescore the 8 nsel candidates: a tile is two blocks (16 keys); lane
-    // (g, t4) loads 16 bytes of keys g and g + 8, the decode scorer's FP8
-    // mma.sync fragments (4 heads as columns 0-3 of n8).  Positions are below
-    // 2^18, so a block's position test and its byte offset are 32-bit
-    // arithmetic (block -1 wraps to a position past every row length).
+    // (g, t4) loads the 16 bytes of channels 16 t4 .. 16 t4 + 15 of key g of
+    // each block (MMA rows g and g + 8; the 4 heads are columns 0-3 of n8) and
+    // converts them to f16 (exact) for four m16n8k16 MMAs: MMA j takes the
+    // lane's channels 16 t4 + 4 j .. + 3 as its k = 2 t4, 2 t4 + 1, 2 t4 + 8,
+    // 2 t4 + 9, the query the same way (the FP8 warp MMA costs several times
+    // the f16 one's instructions here, and the query is converted once).
+    // Positions are below 2^18, so a block's position test and its byte offset
+    // are 32-bit arithmetic (block -1 wraps to a position past every row length).
     const uint4 q8 = (g < 4) ? __ldg(reinterpret_cast<const uint4 *>(a.q + (r * 4 + g) * 64 + 16 * t4))
                              : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t qlo[4], qhi[4];
+    e4m3x4_to_f16x2x2(q8.x, qlo[0], qhi[0]);
+    e4m3x4_to_f16x2x2(q8.y, qlo[1], qhi[1]);
+    e4m3x4_to_f16x2x2(q8.z, qlo[2], qhi[2]);
+    e4m3x4_to_f16x2x2(q8.w, qlo[3], qhi[3]);
     const float w0 = (t4 < 2) ? a.w[r * 4 + 2 * t4] : 0.f;
     const float w1 = (t4 < 2) ? a.w[r * 4 + 2 * t4 + 1] : 0.f;
     const int ntile = (nsel + 1) / 2;
@@ -271,8 +281,15 @@ __global__ void __launch_bounds__(RS_THREADS, 4) dense_rescore_kernel(RescoreArg
         for (int u = 0; u < 4; ++u) {
             const int tl = t0 + u * RS_WARPS;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_e4m3_16832(acc, raw[u][0].x, raw[u][1].x, raw[u][0].y, raw[u][1].y, q8.x, q8.y);
-            mma_e4m3_16832(acc, raw[u][0].z, raw[u][1].z, raw[u][0].w, raw[u][1].w, q8.z, q8.w);
+            const uint32_t w0r[4] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w};
+            const uint32_t w1r[4] = {raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t a0, a2, a1, a3;
+                e4m3x4_to_f16x2x2(w0r[j], a0, a2);   // row g: channels +0,+1 | +2,+3
+                e4m3x4_to_f16x2x2(w1r[j], a1, a3);   // row g + 8
+                mma_f16_16816(acc, a0, a1, a2, a3, qlo[j], qhi[j]);
+            }
             float s0 = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);
             float s1 = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);
             s0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
