@@ -97,6 +97,37 @@ __device__ __forceinline__ float head_sum2(const float4 wq, const uint32_t *r) {
     return __fmaf_rn(wq.w, relu2(r[3]), s);
 }
 
+// Packed pairs of fp32 (sm_100 family): each lane of an f32x2 multiply or
+// fused multiply-add rounds as its scalar instruction would, so two keys'
+// head sums in one register pair equal two head_sum2 results bit for bit.
+__device__ __forceinline__ float relu2f(uint32_t v) {   // 2 max(x, 0), as in head_sum2
+    const float x = __uint_as_float(v);
+    return __fadd_rn(x, fabsf(x));
+}
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {   // the three-input form of fmaxf
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // K-major operand tile in the 64-byte swizzled canonical layout (rows of 64
 // bytes, 8-row atoms of 512 bytes, as the TMA writes it with SWIZZLE_64B).
 __device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
@@ -563,6 +594,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t l = (int64_t)a.kv_len[row];
                 len = (int)(l < 0 ? 0 : (l < a.N ? l : a.N));
             }
+            const uint64_t w2[4] = {f2_pack(wq.x, wq.x), f2_pack(wq.y, wq.y), f2_pack(wq.z, wq.z), f2_pack(wq.w, wq.w)};
             uint32_t *brow = a.bmax + row * a.nblk;
             for (int i = 0; i < it.ntiles; ++i) {
                 const int buf = acount & 1;
@@ -583,9 +615,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 float m[2] = {NEG_INF, NEG_INF};
                 if (key0 + 16 <= len) {   // all of this thread's keys are visible to its query
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const uint32_t hv[4] = {r[0][j], r[1][j], r[2][j], r[3][j]};
-                        m[j >> 3] = fmaxf(m[j >> 3], head_sum2(wq, hv));   // twice the score
+                    for (int j = 0; j < 16; j += 2) {   // keys j, j + 1 as one packed pair: head_sum2 of each
+                        uint64_t s2 = f2_mul(f2_pack(relu2f(r[0][j]), relu2f(r[0][j + 1])), w2[0]);
+                        s2 = f2_fma(f2_pack(relu2f(r[1][j]), relu2f(r[1][j + 1])), w2[1], s2);
+                        s2 = f2_fma(f2_pack(relu2f(r[2][j]), relu2f(r[2][j + 1])), w2[2], s2);
+                        s2 = f2_fma(f2_pack(relu2f(r[3][j]), relu2f(r[3][j + 1])), w2[3], s2);
+                        float lo, hi;
+                        f2_unpack(s2, lo, hi);
+                        m[j >> 3] = max3f(m[j >> 3], lo, hi);   // twice the scores
                     }
                 } else {
 #pragma unroll
