@@ -159,6 +159,11 @@ __device__ __forceinline__ void e2m1x8_scaled(uint32_t w, uint32_t sc, uint32_t 
     r[3] = hmul2(h3, sc);
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {   // the three-input form of fmaxf
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 __device__ __forceinline__ float ex2(float x) {
     float r;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -524,17 +529,18 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         float z[EPT];
         float mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < EPT; ++i) {
-            z[i] = sT[h * ST_STRIDE + TPH * i + part];
-            mx = fmaxf(mx, z[i]);
-        }
+        for (int i = 0; i < EPT; ++i) z[i] = sT[h * ST_STRIDE + TPH * i + part];
+#pragma unroll
+        for (int i = 0; i < EPT; i += 2) mx = max3f(mx, z[i], z[i + 1]);
 #pragma unroll
         for (int o = 1; o < TPH; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        // an entry at -inf gives ex2(-inf) = 0; a head with no entry (mx = -inf) subtracts 0
+        const float mxs = mx == -INFINITY ? 0.f : mx;
         float sum = 0.f;
         uint8_t *pdst = sP + (h >> 3) * P_SBO + (h & 7) * 16;
 #pragma unroll
         for (int i = 0; i < EPT; ++i) {
-            const float p = (mx == -INFINITY || z[i] == -INFINITY) ? 0.f : ex2(z[i] - mx);
+            const float p = ex2(z[i] - mxs);
             const __half ph = __float2half_rn(p);
             sum += __half2float(ph);
             const int en = TPH * i + part;   // entry
