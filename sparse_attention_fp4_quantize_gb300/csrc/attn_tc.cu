@@ -1198,21 +1198,28 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
             {
                 float pf[16];
                 uint32_t pk[8];
+                if (v) {   // a valid entry reached its heads' running maxima: they are finite
 #pragma unroll
-                for (int jj = 0; jj < 16; jj += 2) {
-                    float p2[2];
+                    for (int j4 = 0; j4 < 16; j4 += 4) {   // four heads' maxima and logit factors per 16-byte load
+                        const float4 mx4 = *reinterpret_cast<const float4 *>(sM + 16 * hh + j4);
+                        const float4 cs4 = *reinterpret_cast<const float4 *>(sCs + 16 * hh + j4);
+                        const float mx[4] = {mx4.x, mx4.y, mx4.z, mx4.w}, cs[4] = {cs4.x, cs4.y, cs4.z, cs4.w};
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int hd = 16 * hh + jj + u;
-                        const float mx = sM[hd];
-                        const float zz = __uint_as_float(r[jj + u]) * sCs[hd];
-                        p2[u] = (!v || mx == -INFINITY) ? 0.f : ex2(zz - mx);
+                        for (int u = 0; u < 4; u += 2) {
+                            const float z0 = __uint_as_float(r[j4 + u]) * cs[u];
+                            const float z1 = __uint_as_float(r[j4 + u + 1]) * cs[u + 1];
+                            const __half2 hp = __floats2half2_rn(ex2(z0 - mx[u]), ex2(z1 - mx[u + 1]));
+                            pk[(j4 + u) / 2] = *reinterpret_cast<const uint32_t *>(&hp);
+                            const float2 back = __half22float2(hp);
+                            pf[j4 + u] = back.x;
+                            pf[j4 + u + 1] = back.y;
+                        }
                     }
-                    const __half2 hp = __floats2half2_rn(p2[0], p2[1]);
-                    pk[jj / 2] = *reinterpret_cast<const uint32_t *>(&hp);
-                    const float2 back = __half22float2(hp);
-                    pf[jj] = back.x;
-                    pf[jj + 1] = back.y;
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) pf[jj] = 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) pk[jj] = 0u;
                 }
                 uint8_t *pdst = sK + (ee >> 3) * KT_SBO + TK_P_IN_GROUP + (ee & 7) * 16;
                 *reinterpret_cast<uint4 *>(pdst + (2 * hh) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
