@@ -515,9 +515,12 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_kernel(TcArgs a) {
         const int ee = 32 * quarter + lane;
         const bool v = ok && sValid[ee];
 #pragma unroll
-        for (int jj = 0; jj < HPT; ++jj) {
-            const int h = HPT * hh + jj;
-            sT[h * ST_STRIDE + ee] = v ? __uint_as_float(r[jj]) * sCs[h] : -INFINITY;
+        for (int j4 = 0; j4 < HPT; j4 += 4) {   // four heads' logit factors per 16-byte load
+            const float4 cs4 = *reinterpret_cast<const float4 *>(sCs + HPT * hh + j4);
+            const float cs[4] = {cs4.x, cs4.y, cs4.z, cs4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                sT[(HPT * hh + j4 + u) * ST_STRIDE + ee] = v ? __uint_as_float(r[j4 + u]) * cs[u] : -INFINITY;
         }
     }
     __syncthreads();
@@ -1160,7 +1163,12 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
             {
                 float z[16];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) z[jj] = v ? __uint_as_float(r[jj]) * sCs[16 * hh + jj] : -INFINITY;
+                for (int j4 = 0; j4 < 16; j4 += 4) {   // four heads' logit factors per 16-byte load
+                    const float4 cs4 = *reinterpret_cast<const float4 *>(sCs + 16 * hh + j4);
+                    const float cs[4] = {cs4.x, cs4.y, cs4.z, cs4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) z[j4 + u] = v ? __uint_as_float(r[j4 + u]) * cs[u] : -INFINITY;
+                }
                 const float m = lane_reduce16<true>(z, lane);
                 if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = m;
             }
