@@ -1160,35 +1160,51 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_attn_tc_tokens_kernel(TcArg
             tc::tmem_ld_wait();
             const int ee = 32 * quarter + lane;
             const bool v = ok && sRow[t * TM + ee] >= 0;
+            // The running maxima move only when some logit of the tile exceeds
+            // them by more than the slack (also the first finite one: M = -inf).
+            // Each thread tests its own 16 values; when no thread finds one, the
+            // tile's per-head maxima are not needed and M, L and O stay as they are.
+            bool any_ex;
             {
                 float z[16];
+                bool exceed = false;
 #pragma unroll
-                for (int j4 = 0; j4 < 16; j4 += 4) {   // four heads' logit factors per 16-byte load
+                for (int j4 = 0; j4 < 16; j4 += 4) {   // four heads' logit factors and maxima per 16-byte load
                     const float4 cs4 = *reinterpret_cast<const float4 *>(sCs + 16 * hh + j4);
-                    const float cs[4] = {cs4.x, cs4.y, cs4.z, cs4.w};
+                    const float4 mx4 = *reinterpret_cast<const float4 *>(sM + 16 * hh + j4);
+                    const float cs[4] = {cs4.x, cs4.y, cs4.z, cs4.w}, mo[4] = {mx4.x, mx4.y, mx4.z, mx4.w};
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) z[j4 + u] = v ? __uint_as_float(r[j4 + u]) * cs[u] : -INFINITY;
+                    for (int u = 0; u < 4; ++u) {
+                        z[j4 + u] = v ? __uint_as_float(r[j4 + u]) * cs[u] : -INFINITY;
+                        exceed |= z[j4 + u] > mo[u] + TK_MAX_SLACK;
+                    }
                 }
-                const float m = lane_reduce16<true>(z, lane);
-                if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = m;
-            }
-            __syncthreads();
-            bool resc = false;
-            if (tid < HB) {
-                const float mt = fmaxf(fmaxf(sPart[tid], sPart[HB + tid]), fmaxf(sPart[2 * HB + tid], sPart[3 * HB + tid]));
-                const float mo = sM[tid];
-                float al = 1.f;
-                if (mt > mo + TK_MAX_SLACK) {   // also the first finite maximum (mo = -inf)
-                    resc = mo != -INFINITY;
-                    al = resc ? ex2(mo - mt) : 0.f;
-                    sM[tid] = mt;
-                    sL[tid] *= al;
+                any_ex = __syncthreads_or(exceed) != 0;
+                if (any_ex) {
+                    const float m = lane_reduce16<true>(z, lane);
+                    if ((lane & 1) == 0) sPart[quarter * HB + 16 * hh + (lane >> 1)] = m;
                 }
-                sAlpha[tid] = al;
             }
-            tc::fence_before();
-            const bool any_resc = __syncthreads_or(resc) != 0;
-            tc::fence_after();
+            bool any_resc = false;
+            if (any_ex) {
+                __syncthreads();
+                bool resc = false;
+                if (tid < HB) {
+                    const float mt = fmaxf(fmaxf(sPart[tid], sPart[HB + tid]), fmaxf(sPart[2 * HB + tid], sPart[3 * HB + tid]));
+                    const float mo = sM[tid];
+                    float al = 1.f;
+                    if (mt > mo + TK_MAX_SLACK) {   // also the first finite maximum (mo = -inf)
+                        resc = mo != -INFINITY;
+                        al = resc ? ex2(mo - mt) : 0.f;
+                        sM[tid] = mt;
+                        sL[tid] *= al;
+                    }
+                    sAlpha[tid] = al;
+                }
+                tc::fence_before();
+                any_resc = __syncthreads_or(resc) != 0;
+                tc::fence_after();
+            }
             if (any_resc) {   // O^T *= alpha per head column (P V of t-1 is complete)
 #pragma unroll 1
                 for (int mb = 0; mb < DV / 128; ++mb) {
