@@ -101,21 +101,24 @@ def test_dense_short_and_empty_rows(csa2):
     assert sorted(got[0, 2][got[0, 2] >= 0].tolist()) == list(range(7))
 
 
-def test_dense_all_ties(csa2):
-    """w = 0 makes every visible score 0: any K visible positions are a valid
-    answer; they must be distinct and visible."""
+@pytest.mark.parametrize("first_pos", [16000, 40000])
+def test_dense_all_ties(csa2, first_pos):
+    """w = 0 makes every visible score 0.  Ties go to the lowest positions, as
+    in the oracle's Top-K, so each row takes positions 0 .. K-1 (every visible
+    one when there are fewer): with about 500 blocks per row every block is a
+    candidate; with 625 blocks the K tied block maxima are the lowest K blocks."""
     B, T, N, K = 1, 64, 5000, 512
     q = gen.normal_e4m3(33, 1, (B, T, 4, 64))
     k = gen.normal_e4m3(33, 2, (B, N, 64))
     w = torch.zeros(B, T, 4)
-    kl = _causal_lengths(T, N, 16000).repeat(B)
+    kl = _causal_lengths(T, N, first_pos).repeat(B)
     got = _dense(csa2, q, w, k, kl, K)
     for t in range(T):
         ids = got[0, t]
         n = min(K, int(kl[t]))
         sel = ids[ids >= 0]
-        assert len(sel) == n and len(set(sel.tolist())) == n
-        assert (sel < int(kl[t])).all()
+        assert sorted(sel.tolist()) == list(range(n))
+        assert (ids[n:] == -1).all()
 
 
 def test_dense_prefill_chunk_full_size(csa2):
