@@ -408,16 +408,14 @@ def _extra_workloads(dev, stream, peak_gbs):
     csa2.csa2_index_score(0, q0, w0, k3, kl3, full3, stream=stream)
     pool3 = torch.empty(w3.B, 1, 2048, dtype=torch.int32, device=dev)
     csa2.csa2_build_pool(full3, kl3, pool3, stream=stream)
-    rs3 = torch.empty(w3.B, 1, 16384, device=dev)
     idx3 = torch.empty(w3.B, 1, 512, dtype=torch.int32, device=dev)
     planes = [gen.fp4_planes(w3.seed, 40 + l, w3.B * w3.N, 576, device=dev) for l in range(4)]
     qs = [gen.normal_bf16(w3.seed, 200 + l, (w3.B, 1, 64, 576), device=dev) for l in range(4)]
     outs3 = [torch.empty(w3.B, 1, 64, 512, device=dev) for _ in range(4)]
     ws3 = csa2.workspace_for_attn(w3.B, 1, 64, 576, 512, 512, device=dev)
 
-    def group():
-        csa2.csa2_index_score(1, q1, w1, k3, kl3, rs3, pool_blocks=pool3, stream=stream)
-        csa2.csa2_topk(1, rs3, idx3, pool_blocks=pool3, stream=stream)
+    def group():   # the fused Reindex indexer (score + Top-512 in the pool, one launch), as in the decode step
+        csa2.csa2_index_topk(1, q1, w1, k3, kl3, idx3, pool_blocks=pool3, stream=stream)
         for l in range(4):   # the next Reuse layer's selected rows are hinted into L2 (as in the decode step)
             nxt = planes[l + 1] if l < 3 else (None, None)
             csa2.csa2_sparse_attn_fp4_prefetch(1 if l == 0 else 2, qs[l], planes[l][0], planes[l][1], w3.N, idx3,

@@ -144,9 +144,10 @@ def test_full_group_decode_chain(csa2, wl):
 
 def test_reindex_reuse_group_at_1m(csa2):
     """B=8 sequences of 262144 entries: pool from a Full layer's scores, one
-    Reindex layer (own q, w) -> Top-512 inside the pool, then the Reindex
-    layer and 3 Reuse layers attend with those indices, each over its own
-    FP4 KV."""
+    Reindex layer (own q, w) -> Top-512 inside the pool (the unfused chain
+    against the oracle, the fused indexer against the chain), then the
+    Reindex layer and 3 Reuse layers attend with those indices, each over its
+    own FP4 KV."""
     w = gen.REINDEX_REUSE_1M
     B, N, D, dv, H, K, P = w.B, w.N, w.D, w.dv, w.H, w.K, w.P
     kv_len = gen.kv_lengths(w)
@@ -194,6 +195,16 @@ def test_reindex_reuse_group_at_1m(csa2):
     for b in np.nonzero(pools_same)[0]:
         check_selection(g_idx[b, 0], ref_idx[b, 0], lambda ids: np.array([ref_pos_score[(b, int(j))] for j in ids]),
                         K, "reindex top-512")
+    # the fused indexer (the decode step's call; one launch, rows over 8-CTA clusters at this
+    # length) scores with the same tiling, so it selects the chain's set row for row
+    idx_f = torch.full((B, 1, K), -7, dtype=torch.int32, device=DEV)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    csa2.csa2_index_topk(1, q1, w1, k_idx, kl, idx_f, pool_blocks=pool, err_flag=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    g_f = idx_f.cpu().numpy()
+    for b in range(B):
+        assert sorted(g_f[b, 0].tolist()) == sorted(g_idx[b, 0].tolist())
 
     # 4 attention layers over their own KV, all with the Reindex layer's indices
     sm = gen.softmax_scale(D)
