@@ -432,23 +432,39 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
         }
         return (int32_t)blk;
     };
-    // the ids of this warp's first two chunks are loaded together (lanes
+    // Reindex: the ids of this warp's first two chunks are loaded together (lanes
     // 0-15: chunk warp, lanes 16-31: chunk warp + kWarps), off the chain of
-    // dependent loads of each chunk
-    const int32_t pre_blk = full ? -1 : pool_ids(warp + (lane >= 16 ? kWarps : 0), lane & 15);
+    // dependent loads of each chunk.  The load is only issued here: the first
+    // key loads go out at the positions an identity pool gives (pool slot p
+    // holding block p, as a Full layer writes it when every block of the row
+    // fits), and the ids are checked once those loads are in flight.
+    const int pre_cb = warp + (lane >= 16 ? kWarps : 0);
+    const int64_t pre_pidx = (beg + (int64_t)pre_cb * 128) / 8 + (lane & 15);
+    const bool pre_in = !full && pre_cb < nchunks && pre_pidx < a.P;
+    const int64_t pre_raw = pre_in ? (int64_t)a.pool_in[row * a.P + pre_pidx] : -1;
+    int32_t pre_blk = -1;
+    bool spec_ok = false;   // the warp's two chunks see an identity pool: the identity loads stand
     // Reindex: the slice's checked pool block ids are kept in shared memory (the
     // block-key area, unused without a pool to build), for the output ids
     int32_t *sBlk = reinterpret_cast<int32_t *>(bkeys);
-    if (!full) {
-        const int cb = warp + (lane >= 16 ? kWarps : 0);
-        if (cb < nchunks) sBlk[cb * 16 + (lane & 15)] = pre_blk;
-    }
+    auto check_pre = [&]() {   // every lane of the warp
+        int64_t blk = pre_raw;
+        if (blk < -1 || blk >= nblocks_n) {
+            flag_error(a.err_flag, CSA2_FLAG_BAD_POOL);
+            blk = -1;
+        }
+        pre_blk = (int32_t)blk;
+        if (pre_in) sBlk[pre_cb * 16 + (lane & 15)] = pre_blk;
+        // the identity's positions are this slot's: block p, or no block past the row
+        const bool same = !pre_in || blk == pre_pidx || (blk == -1 && pre_pidx * 8 >= len);
+        spec_ok = __all_sync(0xFFFFFFFFu, same);
+    };
     // A warp scores its chunks (cb = warp, warp + kWarps, ...) in halves of 4
     // groups (64 candidates), software-pipelined over two register buffers:
     // the loads of half k + 1 are in flight while half k is scored.
     const int nhalf = warp < nchunks ? 2 * ((nchunks - warp + kWarps - 1) / kWarps) : 0;
     int32_t chunk_blk = -1;   // Reindex, chunks past the first two: ids reloaded per chunk
-    auto load_half = [&](int k, uint4 (&raw)[4][2], bool (&v)[4][2]) {
+    auto load_half = [&](int k, uint4 (&raw)[4][2], bool (&v)[4][2], bool ident) {
         const int it = k >> 1, cb = warp + kWarps * it, i0 = cb * 128 + 64 * (k & 1);
         if (!full && it >= 2 && (k & 1) == 0) {
             chunk_blk = lane < 16 ? pool_ids(cb, lane) : -1;
@@ -462,7 +478,7 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
             for (int r = 0; r < 2; ++r) {
                 const int i = i0 + 16 * c + g + 8 * r;
                 int64_t j;
-                if (full) {
+                if (full || ident) {   // Reindex with an identity pool: candidate beg + i is position beg + i
                     j = beg + i;
                 } else {
                     const int32_t blk = __shfl_sync(0xFFFFFFFFu, ids, base_lane + 2 * c + r);
@@ -494,11 +510,16 @@ __global__ void __launch_bounds__(kThreads) index_topk_kernel(FusedArgs a) {
     {
         uint4 ra[4][2], rb[4][2];
         bool va[4][2], vb[4][2];
-        if (nhalf > 0) load_half(0, ra, va);
+        if (nhalf > 0) load_half(0, ra, va, !full);
+        if (!full) {
+            check_pre();
+            if (!spec_ok && nhalf > 0) load_half(0, ra, va, false);   // not an identity pool: the real ids
+        }
+        const bool ident = !full && spec_ok;   // for the warp's first two chunks (k < 4)
         for (int k = 0; k < nhalf; k += 2) {   // nhalf is even
-            load_half(k + 1, rb, vb);
+            load_half(k + 1, rb, vb, ident && k + 1 < 4);
             score_half(k, ra, va);
-            if (k + 2 < nhalf) load_half(k + 2, ra, va);
+            if (k + 2 < nhalf) load_half(k + 2, ra, va, ident && k + 2 < 4);
             score_half(k + 1, rb, vb);
         }
     }
